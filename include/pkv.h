@@ -1,0 +1,266 @@
+/*
+ * pkv.h — C ABI of libpkv: single-token decode attention over a paged KV
+ * cache, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (three web pages on the KV cache):
+ *   [NOTES] "KV cache: the engine behind fast LLM inference"
+ *           (curiosity-9m6.pages.dev/notes/0043)
+ *   [VIS]   KV cache visualization (cuuduongthancong.com/~galles/visualization/KVCache.html)
+ *   [GUIDE] jovanaeducation.com/guides/l-is-2
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Shapes.  B = batch (sequences), Hq = query heads, Hkv = KV heads,
+ * G = Hq / Hkv (query heads per KV head; consecutive query heads
+ * h = kvh*G .. kvh*G+G-1 share KV head kvh), D = head_dim, bs = block_size
+ * (tokens per block), NB = number of blocks in the pool.
+ *
+ * Layouts (all row-major, all device buffers owned by the caller):
+ *   k_cache, v_cache   [NB][Hkv][bs][D]  element type = the pool's kv_dtype.
+ *                      Each (block, KV head) tile of bs*D elements is contiguous.
+ *   k_scales, v_scales [NB][Hkv][bs]     fp16, int8 pools only (one scale per
+ *                      cached token per KV head); NULL otherwise.
+ *   q                  [B][Hq][D]        q_dtype.
+ *   out                [B][Hq][D]        fp32.
+ *   block_tables       [B][max_blocks_per_seq] int32: entry j of row b is the
+ *                      physical block that holds tokens j*bs .. j*bs+bs-1 of
+ *                      sequence b ([VIS] "PagedAttention: the cache in blocks").
+ *   seq_lens           [B] int32: tokens cached for each sequence, counting the
+ *                      token appended in this step.
+ *   slot_mapping       [T] int32: cache slot of each new token,
+ *                      slot = block * bs + offset; slot < 0 marks a padding
+ *                      token that is skipped.
+ * Device pointers must be 16-byte aligned.
+ *
+ * Errors.  Every call returns a pkv_status.  Argument and shape errors are
+ * reported synchronously, before anything is launched.  Device calls are
+ * asynchronous on the given stream and return the launch status; bad
+ * indices met on the device (slot or block id outside the pool, a sequence
+ * length beyond its block table) are recorded in the pool's device error
+ * word, the offending access is skipped (nothing traps), and
+ * pkv_check_error() reports them.
+ *
+ * Threads.  A pool's host bookkeeping (alloc/share/free/reserve) is not
+ * thread safe; serialise those calls per pool.  Device calls may be issued
+ * from any thread.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum {
+    PKV_F32 = 0,
+    PKV_F16 = 1,
+    PKV_BF16 = 2,
+    PKV_I8 = 3
+} pkv_dtype;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = -1,     /* bad argument, shape or pointer alignment            */
+    PKV_ERR_NO_BLOCKS = -2,   /* the pool has too few free blocks                    */
+    PKV_ERR_CUDA = -3,        /* a CUDA runtime call failed (or no device)           */
+    PKV_ERR_UNSUPPORTED = -4, /* valid but not a compiled shape / dtype combination  */
+    PKV_ERR_BAD_INDEX = -5,   /* device saw a slot / block id / length out of range  */
+    PKV_ERR_TIMEOUT = -6      /* a bounded device wait gave up                       */
+} pkv_status;
+
+typedef struct pkv_pool pkv_pool; /* opaque; host-side bookkeeping only */
+
+/* Human-readable name of a status code (static string). */
+const char *pkv_status_string(int status);
+
+/* ====================================================================== */
+/* Block pool (host).                                                      */
+/* ====================================================================== */
+
+/*
+ * kv_block_pool_init — describe one shared pool of fixed-size cache blocks.
+ * [VIS] "PagedAttention: the cache in blocks" (blocks of a fixed number of
+ * tokens drawn from one shared pool); [GUIDE] "Paging: borrow the trick
+ * operating systems already use".
+ *
+ *   out          receives the new pool (owned by the caller; free with
+ *                kv_block_pool_destroy).
+ *   num_blocks   NB >= 1; NB * block_size must be < 2^31.
+ *   block_size   power of two, 1..256 (>= 8 for int8 pools).
+ *   num_kv_heads Hkv >= 1.
+ *   head_dim     64 or 128.
+ *   kv_dtype     element type of the cache: F32, F16, BF16, or I8 (int8 codes
+ *                with per-token-per-head fp16 scales).
+ *
+ * The pool keeps a free list (all NB blocks free at start), one reference
+ * count per block, and a 4-byte device error word on the current device.  It
+ * does not own the cache memory: the caller allocates k_cache / v_cache of
+ * kv_cache_bytes() each (and k_scales / v_scales of kv_scales_bytes() for
+ * int8).  If no CUDA device is usable the pool is still created for its host
+ * calls, and every device call on it returns PKV_ERR_CUDA.
+ * Returns PKV_OK, PKV_ERR_INVALID or PKV_ERR_UNSUPPORTED.
+ */
+int kv_block_pool_init(pkv_pool **out, int num_blocks, int block_size, int num_kv_heads,
+                       int head_dim, pkv_dtype kv_dtype);
+
+/* Free the pool's host state and its device error word.  NULL is a no-op. */
+void kv_block_pool_destroy(pkv_pool *pool);
+
+/* Bytes of one of k_cache / v_cache: NB * Hkv * bs * D * sizeof(kv_dtype). */
+size_t kv_cache_bytes(const pkv_pool *pool);
+
+/* Bytes of one of k_scales / v_scales: NB * Hkv * bs * 2 for int8 pools, else 0. */
+size_t kv_scales_bytes(const pkv_pool *pool);
+
+/* Number of blocks currently on the free list. */
+int kv_num_free_blocks(const pkv_pool *pool);
+
+/* Reference count of block id (0 = free), or PKV_ERR_INVALID for a bad id. */
+int kv_block_refcount(const pkv_pool *pool, int32_t id);
+
+/*
+ * kv_block_alloc — take n blocks off the free list, reference count 1 each,
+ * ids written to out_ids[0..n).  Blocks are handed out on demand
+ * ([GUIDE] "Paging…": handed out on demand, reclaimed when the request ends).
+ * All-or-nothing: PKV_ERR_NO_BLOCKS (and no change) if fewer than n are free.
+ */
+int kv_block_alloc(pkv_pool *pool, int n, int32_t *out_ids);
+
+/*
+ * kv_block_share — add one reference to each of ids[0..n), so that another
+ * request can point at the same blocks ([VIS] "PagedAttention: the cache in
+ * blocks": requests with the same prompt prefix point at the same blocks).
+ * All-or-nothing: PKV_ERR_INVALID if any id is out of range or free.
+ */
+int kv_block_share(pkv_pool *pool, const int32_t *ids, int n);
+
+/*
+ * kv_block_free — drop one reference from each of ids[0..n); a block whose
+ * count reaches 0 returns to the free list.  All-or-nothing: PKV_ERR_INVALID
+ * (no change) if any id is out of range or already free, counting repeats.
+ */
+int kv_block_free(pkv_pool *pool, const int32_t *ids, int n);
+
+/*
+ * kv_reserve_slots — host bookkeeping of one append step (prefill or decode).
+ * For each sequence b with seq_lens[b] tokens already cached and num_new[b]
+ * new tokens (num_new == NULL means 1 each), allocate a new block whenever a
+ * new token's position starts a block ([VIS] "PagedAttention…": a request
+ * takes a new block only when its last block is full, so at most one block per
+ * request is partly empty), record it in the host array block_tables
+ * ([B][max_blocks_per_seq], updated in place), and write the slot of every
+ * new token to slot_mapping (sequence-major, sum(num_new) entries).
+ * All-or-nothing: PKV_ERR_NO_BLOCKS if the pool cannot cover the step,
+ * PKV_ERR_INVALID if a table row would overflow max_blocks_per_seq.
+ * seq_lens itself is not modified.
+ */
+int kv_reserve_slots(pkv_pool *pool, int batch, const int32_t *seq_lens, const int32_t *num_new,
+                     int32_t *block_tables, int max_blocks_per_seq, int32_t *slot_mapping);
+
+/*
+ * kv_slot_mapping — pure host computation of slots from existing block
+ * tables: token j of sequence b sits at position start[b] + j, in logical
+ * block p / bs at offset p % bs, so its slot is
+ * block_tables[b][p / bs] * bs + p % bs.  num_new == NULL means 1 each.
+ * Returns PKV_ERR_INVALID if a position falls outside its table row.
+ */
+int kv_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq, int block_size,
+                    int batch, const int32_t *start, const int32_t *num_new,
+                    int32_t *slot_mapping);
+
+/* ====================================================================== */
+/* Device calls.                                                           */
+/* ====================================================================== */
+
+/*
+ * kv_append — write the new tokens' K and V rows into the cache.
+ * [NOTES] "What happens at each decoding step", step 4; [GUIDE] "How the
+ * cache turns the loop cheap" (only the new token's key and value are
+ * computed, then stored).  With num_tokens = a whole prompt it is the bulk
+ * write of prefill.
+ *
+ *   k_new, v_new  device [T][Hkv][D], element type in_dtype.
+ *   slot_mapping  device [T] int32 (see conventions; < 0 = skip).
+ *   k_cache, v_cache  device caches of the pool's layout.
+ *   k_scales, v_scales  device fp16 [NB][Hkv][bs] for int8 pools, else NULL.
+ *
+ * fp pools: in_dtype must equal the pool's kv_dtype; rows are copied bit for
+ * bit.  int8 pools ([NOTES] "Quantized KV cache"): in_dtype F16, BF16 or F32;
+ * each (token, head) row x of D values is quantized in fp32 as
+ *   amax = max|x_i|, s = fp16_round_nearest_even(amax / 127),
+ *   code_i = clamp(round_half_even(x_i / s), -127, 127)   (codes 0 if s == 0)
+ * and s is stored as that token's scale.  Inputs must be finite with
+ * |x| <= 65504.  A slot outside [0, NB*bs) sets PKV_ERR_BAD_INDEX in the
+ * error word and that token is skipped.  num_tokens == 0 is a no-op.
+ */
+int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
+              const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,
+              void *k_scales, void *v_scales, pkv_stream_t stream);
+
+/*
+ * paged_decode_workspace_bytes — size of the scratch buffer that
+ * paged_decode_attention needs for a batch of `batch` sequences and
+ * num_q_heads query heads on the pool's device.  The workspace holds
+ * per-piece partial softmax states and one counter per (sequence, KV head).
+ * Returns 0 for invalid arguments.
+ */
+size_t paged_decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads);
+
+/*
+ * paged_decode_attention — one decode step of attention for a batch.
+ * [NOTES] "Concept" and step 3 of "What happens at each decoding step": for
+ * every sequence b and query head h, with kvh = h / G,
+ *   out[b][h] = softmax(scale * q[b][h] . K_b^T) . V_b
+ * over the seq_lens[b] cached rows K_b, V_b of KV head kvh, reached through
+ * block_tables[b] ([VIS] "PagedAttention: the cache in blocks"; GQA sharing
+ * from [VIS] "How much memory").  int8 pools dequantize each row as
+ * code * scale.  scale is normally 1/sqrt(D).
+ *
+ *   q          device [B][Hq][D]; q_dtype = kv_dtype for fp pools, F16 or
+ *              BF16 for int8 pools.
+ *   num_q_heads  Hq, a multiple of Hkv with G in {1, 2, 4, 8}.
+ *   block_tables, seq_lens  device int32 (see conventions).  A length of 0
+ *              gives a zero output row; a length above
+ *              max_blocks_per_seq * bs, or a block id outside [0, NB), sets
+ *              PKV_ERR_BAD_INDEX and the sequence's output is unspecified.
+ *   max_seq_len  an upper bound of seq_lens (only sizes the launch, so the
+ *              host never waits for the device).
+ *   out        device fp32 [B][Hq][D].
+ *   workspace  device scratch of at least paged_decode_workspace_bytes();
+ *              its counters must be zero before the first call (e.g. zeroed
+ *              by the caller at allocation); every call leaves them zero.  A
+ *              workspace must not be shared by calls that run concurrently.
+ *              After a call that reported PKV_ERR_TIMEOUT, zero it again.
+ *
+ * Batch is limited to 4096 sequences per call (PKV_ERR_UNSUPPORTED beyond).
+ * Split-K: the batch's K/V tiles are divided evenly over the GPU's SMs; a
+ * sequence split across several CTAs is merged by the last CTA to finish it.
+ * The result does not depend on timing.
+ */
+int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
+                           int num_q_heads, const void *k_cache, const void *v_cache,
+                           const void *k_scales, const void *v_scales,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, int batch, int max_seq_len, float scale,
+                           float *out, void *workspace, size_t workspace_bytes,
+                           pkv_stream_t stream);
+
+/*
+ * pkv_check_error — synchronise the stream, read and clear the pool's device
+ * error word.  Returns PKV_OK, PKV_ERR_BAD_INDEX, PKV_ERR_TIMEOUT (a bounded
+ * wait inside a kernel gave up; the kernel returned without finishing), or
+ * PKV_ERR_CUDA.
+ */
+int pkv_check_error(const pkv_pool *pool, pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

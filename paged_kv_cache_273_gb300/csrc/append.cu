@@ -1,0 +1,182 @@
+// kv_append: write the new tokens' K and V rows into the paged cache.
+//
+// "KV cache: the engine behind fast LLM inference", "What happens at each
+// decoding step", step 4: only the new token's key and value are computed,
+// and they join the cache.  The cache slot of a token comes from its block
+// table (KV cache visualization page, "PagedAttention: the cache in blocks").
+//
+// fp caches: a bit copy, 16 bytes per thread.  int8 caches ("Quantized KV
+// cache" on the same page): one warp per (token, head, K-or-V) row computes the
+// row's absolute maximum, an fp16 scale amax/127 and round-half-even codes.
+
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace pkv {
+namespace {
+
+using namespace dev;
+
+// One thread per 16-byte chunk of a (token, head) row, K and V in the same
+// pass.  chunks_per_row = D * eb / 16.
+__global__ void __launch_bounds__(256) append_copy_kernel(
+    const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+    const int32_t *__restrict__ slot_mapping, int64_t total_chunks, int chunks_per_row,
+    int num_kv_heads, int block_size, int64_t num_slots, uint4 *__restrict__ k_cache,
+    uint4 *__restrict__ v_cache, unsigned int *__restrict__ err)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < total_chunks;
+         c += stride) {
+        const int64_t row = c / chunks_per_row;          // (token, head)
+        const int chunk = (int)(c - row * chunks_per_row);
+        const int64_t t = row / num_kv_heads;
+        const int h = (int)(row - t * num_kv_heads);
+        const int32_t slot = __ldg(slot_mapping + t);
+        if (slot < 0)
+            continue;                                     // padding token
+        if ((int64_t)slot >= num_slots) {
+            atomicOr(err, PKV_EBIT_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / block_size;
+        const int64_t off = slot - blk * block_size;
+        const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * chunks_per_row + chunk;
+        k_cache[dst] = __ldg(k_new + c);
+        v_cache[dst] = __ldg(v_new + c);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float load_as_float(const T *p);
+template <>
+__device__ __forceinline__ float load_as_float<float>(const float *p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float load_as_float<__half>(const __half *p) { return __half2float(__ldg(p)); }
+template <>
+__device__ __forceinline__ float load_as_float<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    return __bfloat162float(__ldg(p));
+}
+
+// One warp per (token, head, K|V) row.  D = 32 * E.
+template <typename T, int E>
+__global__ void __launch_bounds__(256) append_q8_kernel(
+    const T *__restrict__ k_new, const T *__restrict__ v_new,
+    const int32_t *__restrict__ slot_mapping, int64_t num_rows /* T*Hkv */, int num_kv_heads,
+    int block_size, int64_t num_slots, int8_t *__restrict__ k_cache, int8_t *__restrict__ v_cache,
+    __half *__restrict__ k_scales, __half *__restrict__ v_scales, unsigned int *__restrict__ err)
+{
+    constexpr int D = 32 * E;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t w = warp; w < 2 * num_rows; w += nwarps) {
+        const bool is_v = w >= num_rows;
+        const int64_t row = is_v ? w - num_rows : w;
+        const int64_t t = row / num_kv_heads;
+        const int h = (int)(row - t * num_kv_heads);
+        const int32_t slot = __ldg(slot_mapping + t);
+        if (slot < 0)
+            continue;
+        if ((int64_t)slot >= num_slots) {
+            if (lane == 0)
+                atomicOr(err, PKV_EBIT_SLOT);
+            continue;
+        }
+        const T *src = (is_v ? v_new : k_new) + row * D + lane * E;
+        float x[E];
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            x[e] = load_as_float<T>(src + e);
+            amax = fmaxf(amax, fabsf(x[e]));
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, m));
+        // IEEE fp32 division and round-to-nearest-even conversions only.
+        const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
+        const float s = __half2float(s16);
+        const int64_t blk = slot / block_size;
+        const int64_t off = slot - blk * block_size;
+        const int64_t srow = (blk * num_kv_heads + h) * block_size + off;
+        int8_t *dst = (is_v ? v_cache : k_cache) + srow * D + lane * E;
+        static_assert(E == 2 || E == 4, "two or four codes per lane");
+        uint32_t word = 0;
+#pragma unroll
+        for (int u = 0; u < E; ++u) {
+            int code = 0;
+            if (s != 0.0f) {
+                float c = rintf(__fdiv_rn(x[u], s));     // round half to even
+                c = fminf(fmaxf(c, -127.0f), 127.0f);
+                code = (int)c;
+            }
+            word |= (uint32_t)(code & 0xff) << (8 * u);
+        }
+        if (E == 4)
+            *reinterpret_cast<uint32_t *>(dst) = word;
+        else
+            *reinterpret_cast<uint16_t *>(dst) = (uint16_t)word;
+        if (lane == 0)
+            (is_v ? v_scales : k_scales)[srow] = s16;
+    }
+}
+
+int grid_for(int64_t work_items, int threads, int num_sms)
+{
+    int64_t blocks = (work_items + threads - 1) / threads;
+    int64_t cap = (int64_t)num_sms * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    return (int)blocks;
+}
+
+}  // namespace
+
+int launch_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
+                  const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,
+                  void *k_scales, void *v_scales, pkv_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int H = pool->num_kv_heads, D = pool->head_dim, bs = pool->block_size;
+    const int64_t num_slots = (int64_t)pool->num_blocks * bs;
+    if (pool->kv_dtype != PKV_I8) {
+        const int chunks_per_row = D * dtype_bytes(pool->kv_dtype) / 16;
+        const int64_t total = (int64_t)num_tokens * H * chunks_per_row;
+        const int threads = 256;
+        append_copy_kernel<<<grid_for(total, threads, pool->num_sms), threads, 0, s>>>(
+            static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
+            total, chunks_per_row, H, bs, num_slots, static_cast<uint4 *>(k_cache),
+            static_cast<uint4 *>(v_cache), pool->d_err);
+    } else {
+        const int64_t rows = (int64_t)num_tokens * H;
+        const int threads = 256;
+        const int grid = grid_for(2 * rows * 32, threads, pool->num_sms);
+        int8_t *kc = static_cast<int8_t *>(k_cache);
+        int8_t *vc = static_cast<int8_t *>(v_cache);
+        __half *ks = static_cast<__half *>(k_scales);
+        __half *vs = static_cast<__half *>(v_scales);
+#define PKV_Q8(T, E)                                                                        \
+    append_q8_kernel<T, E><<<grid, threads, 0, s>>>(static_cast<const T *>(k_new),          \
+                                                    static_cast<const T *>(v_new),          \
+                                                    slot_mapping, rows, H, bs, num_slots, kc, \
+                                                    vc, ks, vs, pool->d_err)
+        if (D == 128) {
+            if (in_dtype == PKV_F16) PKV_Q8(__half, 4);
+            else if (in_dtype == PKV_BF16) PKV_Q8(__nv_bfloat16, 4);
+            else PKV_Q8(float, 4);
+        } else {
+            if (in_dtype == PKV_F16) PKV_Q8(__half, 2);
+            else if (in_dtype == PKV_BF16) PKV_Q8(__nv_bfloat16, 2);
+            else PKV_Q8(float, 2);
+        }
+#undef PKV_Q8
+    }
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

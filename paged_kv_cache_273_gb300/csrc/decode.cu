@@ -1,0 +1,91 @@
+// Host side of paged_decode_attention: workspace sizing and the dispatch to
+// the kernel instantiation for the pool's K/V dtype (each dtype is compiled
+// in its own translation unit, decode_<dtype>.cu).
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "pkv_internal.h"
+
+#include "decode_kernel.cuh"
+
+// Instantiated in decode_<dtype>.cu.
+namespace pkv {
+namespace kern {
+extern template int launch_d<PKV_F32>(const pkv_pool *, int, const Params &, int, int, cudaStream_t);
+extern template int launch_d<PKV_F16>(const pkv_pool *, int, const Params &, int, int, cudaStream_t);
+extern template int launch_d<PKV_BF16>(const pkv_pool *, int, const Params &, int, int, cudaStream_t);
+extern template int launch_d<PKV_I8>(const pkv_pool *, int, const Params &, int, int, cudaStream_t);
+}  // namespace kern
+}  // namespace pkv
+
+namespace pkv {
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+size_t decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads)
+{
+    const int G = num_q_heads / pool->num_kv_heads;
+    const size_t counters = align_up((size_t)batch * pool->num_kv_heads * sizeof(int), 256);
+    const size_t entries = (size_t)std::max(pool->num_sms, 1) + (size_t)batch * pool->num_kv_heads;
+    const size_t partials = entries * (size_t)G * (pool->head_dim + 2) * sizeof(float);
+    return counters + align_up(partials, 256);
+}
+
+int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
+                  const void *k_cache, const void *v_cache, const void *k_scales,
+                  const void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
+                  const int32_t *seq_lens, int batch, int max_seq_len, float scale, float *out,
+                  void *workspace, size_t workspace_bytes, pkv_stream_t stream)
+{
+    (void)workspace_bytes;
+    const int Hkv = pool->num_kv_heads;
+    const int G = num_q_heads / Hkv;
+    const int64_t tiles_bound =
+        (int64_t)batch * Hkv * (((int64_t)max_seq_len + kern::TILE - 1) / kern::TILE);
+    if (tiles_bound >= ((int64_t)1 << 31))
+        return PKV_ERR_UNSUPPORTED;
+    kern::Params prm{};
+    prm.q = q;
+    prm.k_cache = static_cast<const unsigned char *>(k_cache);
+    prm.v_cache = static_cast<const unsigned char *>(v_cache);
+    prm.k_scales = static_cast<const __half *>(k_scales);
+    prm.v_scales = static_cast<const __half *>(v_scales);
+    prm.block_tables = block_tables;
+    prm.seq_lens = seq_lens;
+    prm.out = out;
+    const size_t counters = align_up((size_t)batch * Hkv * sizeof(int), 256);
+    prm.counters = static_cast<int *>(workspace);
+    prm.partials = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + counters);
+    prm.err = pool->d_err;
+    prm.batch = batch;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = Hkv;
+    prm.block_size = pool->block_size;
+    int lg = 0;
+    while ((1 << lg) < pool->block_size)
+        ++lg;
+    prm.bs_log2 = lg;
+    prm.max_blocks_per_seq = max_blocks_per_seq;
+    prm.max_seq_len = max_seq_len;
+    const int64_t table_cap = (int64_t)max_blocks_per_seq * pool->block_size;
+    prm.len_cap = (int)std::min<int64_t>(max_seq_len, table_cap);
+    prm.num_blocks = pool->num_blocks;
+    prm.q_dtype = q_dtype;
+    prm.q_bytes = dtype_bytes(q_dtype);
+    prm.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (pool->kv_dtype) {
+    case PKV_F32: return kern::launch_d<PKV_F32>(pool, G, prm, batch, max_seq_len, s);
+    case PKV_F16: return kern::launch_d<PKV_F16>(pool, G, prm, batch, max_seq_len, s);
+    case PKV_BF16: return kern::launch_d<PKV_BF16>(pool, G, prm, batch, max_seq_len, s);
+    case PKV_I8: return kern::launch_d<PKV_I8>(pool, G, prm, batch, max_seq_len, s);
+    }
+    return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace pkv

@@ -1,0 +1,173 @@
+// Device-side helpers for libpkv kernels (sm_103a): mbarriers, bulk async
+// copies into shared memory, bounded waits, and 16-bit / 8-bit unpacking.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace dev {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+// A bounded wait gives up after about one second of device time.
+constexpr uint64_t WAIT_LIMIT_NS = 1ull << 30;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk copy) proxy.
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase with the given parity has completed.  Gives up (and
+// returns false) after WAIT_LIMIT_NS, or at once when *abort is set by any
+// thread of the CTA; the caller then records the timeout and winds down.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0) {
+            if (*abort)
+                return false;
+            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS)
+                return false;
+        }
+    }
+}
+
+// Bulk (non-tensor) async copy global -> this CTA's shared memory; completion
+// is counted in bytes on the mbarrier.  dst, src 16-byte aligned; bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Same with an L2 eviction-priority hint (policy from createpolicy).
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+        "%2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---- unpacking -------------------------------------------------------------
+
+// Two bf16 packed in a word -> two floats (exact: bf16 is the top half of f32).
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t w)
+{
+    __half2 h = *reinterpret_cast<__half2 *>(&w);
+    return __half22float2(h);
+}
+
+// Byte i (0..3) of a word of four int8 codes -> exact float, via the biased
+// byte placed in the mantissa of 2^23 (code + 128 + 2^23) minus (2^23 + 128).
+template <int I>
+__device__ __forceinline__ float i8_to_float(uint32_t biased)
+{
+    const uint32_t f = __byte_perm(biased, 0x4B000000u, 0x7440u + I);
+    return __uint_as_float(f) - 8388736.0f;
+}
+
+// Mixed-precision FMA: fp32 accumulate of the product of two bf16 (or fp16)
+// halves taken from packed words; the product is exact in fp32.
+__device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float c)
+{
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t.reg .f32 t;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 t, al, bl, %3;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, t;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float fma_f16x2(uint32_t a, uint32_t b, float c)
+{
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t.reg .f32 t;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 t, al, bl, %3;\n\t"
+        "fma.rn.f32.f16 %0, ah, bh, t;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+
+}  // namespace dev
+}  // namespace pkv

@@ -1,0 +1,345 @@
+// Host side of libpkv: the shared block pool, its free list and reference
+// counts, slot bookkeeping, argument validation, and the device error word.
+//
+// The block pool follows the KV cache visualization page, "PagedAttention:
+// the cache in blocks": fixed-size blocks from one shared pool, a block table
+// per request, a new block only when the last one is full, and shared prefix
+// blocks.  Blocks are reclaimed when their last reference goes away
+// (jovanaeducation.com/guides/l-is-2, "Paging: borrow the trick operating
+// systems already use").
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <new>
+#include <unordered_map>
+
+#include "pkv_internal.h"
+
+namespace {
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_status_string(int status)
+{
+    switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID: return "invalid argument";
+    case PKV_ERR_NO_BLOCKS: return "not enough free blocks";
+    case PKV_ERR_CUDA: return "CUDA error or no device";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PKV_ERR_BAD_INDEX: return "slot, block id or sequence length out of range";
+    case PKV_ERR_TIMEOUT: return "bounded device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int kv_block_pool_init(pkv_pool **out, int num_blocks, int block_size, int num_kv_heads,
+                       int head_dim, pkv_dtype kv_dtype)
+{
+    if (!out)
+        return PKV_ERR_INVALID;
+    *out = nullptr;
+    if (num_blocks < 1 || num_kv_heads < 1 || !is_pow2(block_size) || block_size > 256)
+        return PKV_ERR_INVALID;
+    if ((int64_t)num_blocks * block_size >= ((int64_t)1 << 31))
+        return PKV_ERR_INVALID;
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_F16 && kv_dtype != PKV_BF16 && kv_dtype != PKV_I8)
+        return PKV_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128)
+        return PKV_ERR_UNSUPPORTED;
+    if (block_size < 4 || (kv_dtype == PKV_I8 && block_size < 8))
+        return PKV_ERR_UNSUPPORTED;
+
+    pkv_pool *p = new (std::nothrow) pkv_pool;
+    if (!p)
+        return PKV_ERR_INVALID;
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->num_kv_heads = num_kv_heads;
+    p->head_dim = head_dim;
+    p->kv_dtype = kv_dtype;
+    p->refcount.assign(num_blocks, 0);
+    p->free_stack.resize(num_blocks);
+    for (int i = 0; i < num_blocks; ++i)          // pops yield 0, 1, 2, ...
+        p->free_stack[i] = num_blocks - 1 - i;
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+        cudaDeviceProp prop;
+        unsigned int *err = nullptr;
+        if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess &&
+            cudaMalloc(&err, sizeof(unsigned int)) == cudaSuccess) {
+            if (cudaMemset(err, 0, sizeof(unsigned int)) == cudaSuccess) {
+                p->has_device = true;
+                p->device = dev;
+                p->num_sms = prop.multiProcessorCount;
+                p->max_smem_optin = (int)prop.sharedMemPerBlockOptin;
+                p->d_err = err;
+            } else {
+                cudaFree(err);
+            }
+        }
+    }
+    cudaGetLastError();  // a missing device is not sticky for the caller
+    *out = p;
+    return PKV_OK;
+}
+
+void kv_block_pool_destroy(pkv_pool *pool)
+{
+    if (!pool)
+        return;
+    if (pool->d_err)
+        cudaFree(pool->d_err);
+    delete pool;
+}
+
+size_t kv_cache_bytes(const pkv_pool *pool)
+{
+    if (!pool)
+        return 0;
+    return (size_t)pool->num_blocks * pool->num_kv_heads * pool->block_size * pool->head_dim *
+           pkv::dtype_bytes(pool->kv_dtype);
+}
+
+size_t kv_scales_bytes(const pkv_pool *pool)
+{
+    if (!pool || pool->kv_dtype != PKV_I8)
+        return 0;
+    return (size_t)pool->num_blocks * pool->num_kv_heads * pool->block_size * 2;
+}
+
+int kv_num_free_blocks(const pkv_pool *pool)
+{
+    return pool ? (int)pool->free_stack.size() : PKV_ERR_INVALID;
+}
+
+int kv_block_refcount(const pkv_pool *pool, int32_t id)
+{
+    if (!pool || id < 0 || id >= pool->num_blocks)
+        return PKV_ERR_INVALID;
+    return pool->refcount[id];
+}
+
+int kv_block_alloc(pkv_pool *pool, int n, int32_t *out_ids)
+{
+    if (!pool || n < 0 || (n > 0 && !out_ids))
+        return PKV_ERR_INVALID;
+    if ((size_t)n > pool->free_stack.size())
+        return PKV_ERR_NO_BLOCKS;
+    for (int i = 0; i < n; ++i) {
+        int32_t id = pool->free_stack.back();
+        pool->free_stack.pop_back();
+        pool->refcount[id] = 1;
+        out_ids[i] = id;
+    }
+    return PKV_OK;
+}
+
+int kv_block_share(pkv_pool *pool, const int32_t *ids, int n)
+{
+    if (!pool || n < 0 || (n > 0 && !ids))
+        return PKV_ERR_INVALID;
+    for (int i = 0; i < n; ++i)
+        if (ids[i] < 0 || ids[i] >= pool->num_blocks || pool->refcount[ids[i]] <= 0)
+            return PKV_ERR_INVALID;
+    for (int i = 0; i < n; ++i)
+        ++pool->refcount[ids[i]];
+    return PKV_OK;
+}
+
+int kv_block_free(pkv_pool *pool, const int32_t *ids, int n)
+{
+    if (!pool || n < 0 || (n > 0 && !ids))
+        return PKV_ERR_INVALID;
+    std::unordered_map<int32_t, int> drops;
+    for (int i = 0; i < n; ++i) {
+        if (ids[i] < 0 || ids[i] >= pool->num_blocks)
+            return PKV_ERR_INVALID;
+        if (++drops[ids[i]] > pool->refcount[ids[i]])
+            return PKV_ERR_INVALID;               // double free / underflow
+    }
+    for (int i = 0; i < n; ++i) {
+        int32_t id = ids[i];
+        if (--pool->refcount[id] == 0)
+            pool->free_stack.push_back(id);
+    }
+    return PKV_OK;
+}
+
+int kv_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq, int block_size,
+                    int batch, const int32_t *start, const int32_t *num_new,
+                    int32_t *slot_mapping)
+{
+    if (batch < 0 || max_blocks_per_seq < 0 || block_size < 1 || (batch > 0 && (!start || !block_tables)))
+        return PKV_ERR_INVALID;
+    int64_t k = 0;
+    for (int b = 0; b < batch; ++b) {
+        int n = num_new ? num_new[b] : 1;
+        if (start[b] < 0 || n < 0)
+            return PKV_ERR_INVALID;
+        if (n > 0 && !slot_mapping)
+            return PKV_ERR_INVALID;
+        if ((int64_t)start[b] + n > (int64_t)max_blocks_per_seq * block_size)
+            return PKV_ERR_INVALID;
+        const int32_t *row = block_tables + (int64_t)b * max_blocks_per_seq;
+        for (int j = 0; j < n; ++j) {
+            int64_t pos = (int64_t)start[b] + j;
+            int64_t slot = (int64_t)row[pos / block_size] * block_size + pos % block_size;
+            slot_mapping[k++] = (int32_t)slot;
+        }
+    }
+    return PKV_OK;
+}
+
+int kv_reserve_slots(pkv_pool *pool, int batch, const int32_t *seq_lens, const int32_t *num_new,
+                     int32_t *block_tables, int max_blocks_per_seq, int32_t *slot_mapping)
+{
+    if (!pool || batch < 0 || max_blocks_per_seq < 0 ||
+        (batch > 0 && (!seq_lens || !block_tables)))
+        return PKV_ERR_INVALID;
+    const int bs = pool->block_size;
+    int64_t need = 0, total_new = 0;
+    for (int b = 0; b < batch; ++b) {
+        int n = num_new ? num_new[b] : 1;
+        if (seq_lens[b] < 0 || n < 0)
+            return PKV_ERR_INVALID;
+        int64_t before = ceil_div(seq_lens[b], bs);
+        int64_t after = ceil_div((int64_t)seq_lens[b] + n, bs);
+        if (after > max_blocks_per_seq)
+            return PKV_ERR_INVALID;
+        need += after - before;
+        total_new += n;
+    }
+    if (total_new > 0 && !slot_mapping)
+        return PKV_ERR_INVALID;
+    if (need > (int64_t)pool->free_stack.size())
+        return PKV_ERR_NO_BLOCKS;
+    int64_t k = 0;
+    for (int b = 0; b < batch; ++b) {
+        int n = num_new ? num_new[b] : 1;
+        int32_t *row = block_tables + (int64_t)b * max_blocks_per_seq;
+        for (int j = 0; j < n; ++j) {
+            int64_t pos = (int64_t)seq_lens[b] + j;
+            if (pos % bs == 0) {                  // first token of a new block
+                int32_t id;
+                kv_block_alloc(pool, 1, &id);     // cannot fail: counted above
+                row[pos / bs] = id;
+            }
+            slot_mapping[k++] = (int32_t)((int64_t)row[pos / bs] * bs + pos % bs);
+        }
+    }
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------------- device calls
+
+int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
+              const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,
+              void *k_scales, void *v_scales, pkv_stream_t stream)
+{
+    if (!pool || num_tokens < 0)
+        return PKV_ERR_INVALID;
+    if (pool->kv_dtype == PKV_I8) {
+        if (in_dtype != PKV_F16 && in_dtype != PKV_BF16 && in_dtype != PKV_F32)
+            return PKV_ERR_UNSUPPORTED;
+    } else if (in_dtype != pool->kv_dtype) {
+        return PKV_ERR_INVALID;
+    }
+    if (num_tokens == 0)
+        return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+        return PKV_ERR_INVALID;
+    if (!pkv::aligned16(k_new) || !pkv::aligned16(v_new) || !pkv::aligned16(k_cache) ||
+        !pkv::aligned16(v_cache) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3u))
+        return PKV_ERR_INVALID;
+    if (pool->kv_dtype == PKV_I8 && (!k_scales || !v_scales || !pkv::aligned16(k_scales) ||
+                                     !pkv::aligned16(v_scales)))
+        return PKV_ERR_INVALID;
+    if (!pool->has_device)
+        return PKV_ERR_CUDA;
+    return pkv::launch_append(pool, k_new, v_new, in_dtype, slot_mapping, num_tokens, k_cache,
+                              v_cache, k_scales, v_scales, stream);
+}
+
+size_t paged_decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads)
+{
+    if (!pool || batch < 0 || num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0)
+        return 0;
+    return pkv::decode_workspace_bytes(pool, batch, num_q_heads);
+}
+
+int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
+                           int num_q_heads, const void *k_cache, const void *v_cache,
+                           const void *k_scales, const void *v_scales,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, int batch, int max_seq_len, float scale,
+                           float *out, void *workspace, size_t workspace_bytes,
+                           pkv_stream_t stream)
+{
+    if (!pool || batch < 0 || max_blocks_per_seq < 0 || max_seq_len < 0 || num_q_heads < 1)
+        return PKV_ERR_INVALID;
+    if (num_q_heads % pool->num_kv_heads != 0)
+        return PKV_ERR_INVALID;
+    int G = num_q_heads / pool->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return PKV_ERR_UNSUPPORTED;
+    if (pool->kv_dtype == PKV_I8) {
+        if (q_dtype != PKV_F16 && q_dtype != PKV_BF16)
+            return PKV_ERR_UNSUPPORTED;
+    } else if (q_dtype != pool->kv_dtype) {
+        return PKV_ERR_INVALID;
+    }
+    if (batch > 4096)
+        return PKV_ERR_UNSUPPORTED;
+    if (batch == 0)
+        return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out || !workspace)
+        return PKV_ERR_INVALID;
+    if (!pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache) ||
+        !pkv::aligned16(out) || !pkv::aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return PKV_ERR_INVALID;
+    if (pool->kv_dtype == PKV_I8 && (!k_scales || !v_scales || !pkv::aligned16(k_scales) ||
+                                     !pkv::aligned16(v_scales)))
+        return PKV_ERR_INVALID;
+    if (!pool->has_device)
+        return PKV_ERR_CUDA;
+    if (workspace_bytes < pkv::decode_workspace_bytes(pool, batch, num_q_heads))
+        return PKV_ERR_INVALID;
+    return pkv::launch_decode(pool, q, q_dtype, num_q_heads, k_cache, v_cache, k_scales, v_scales,
+                              block_tables, max_blocks_per_seq, seq_lens, batch, max_seq_len,
+                              scale, out, workspace, workspace_bytes, stream);
+}
+
+int pkv_check_error(const pkv_pool *pool, pkv_stream_t stream)
+{
+    if (!pool)
+        return PKV_ERR_INVALID;
+    if (!pool->has_device)
+        return PKV_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned int h = 0;
+    if (cudaMemcpyAsync(&h, pool->d_err, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (h == 0)
+        return PKV_OK;
+    if (cudaMemsetAsync(pool->d_err, 0, sizeof(unsigned int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (h & PKV_EBIT_TIMEOUT)
+        return PKV_ERR_TIMEOUT;
+    return PKV_ERR_BAD_INDEX;
+}
+
+}  // extern "C"

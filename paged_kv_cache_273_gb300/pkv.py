@@ -1,0 +1,293 @@
+"""Python binding of libpkv (ctypes), one function per C-ABI entry point.
+
+Argument marshalling only: every step of the hot path runs in libpkv's CUDA
+kernels.  PyTorch supplies device memory and streams.  If libpkv.so has not
+been built, importing the library raises; there is no CPU fallback.
+
+Device tensors follow the layouts of ``include/pkv.h``:
+  k_cache, v_cache   [NB, Hkv, bs, D]   (float32 | float16 | bfloat16 | int8)
+  k_scales, v_scales [NB, Hkv, bs]      float16 (int8 pools only)
+  q                  [B, Hq, D];  out [B, Hq, D] float32
+  block_tables       [B, max_blocks_per_seq] int32;  seq_lens [B] int32
+  slot_mapping       [T] int32
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_F32, PKV_F16, PKV_BF16, PKV_I8 = 0, 1, 2, 3
+PKV_OK = 0
+PKV_ERR_INVALID = -1
+PKV_ERR_NO_BLOCKS = -2
+PKV_ERR_CUDA = -3
+PKV_ERR_UNSUPPORTED = -4
+PKV_ERR_BAD_INDEX = -5
+PKV_ERR_TIMEOUT = -6
+
+TORCH_DTYPE = {PKV_F32: torch.float32, PKV_F16: torch.float16, PKV_BF16: torch.bfloat16,
+               PKV_I8: torch.int8}
+PKV_DTYPE = {v: k for k, v in TORCH_DTYPE.items()}
+
+# Every symbol the header declares (checked by the tests).
+SYMBOLS = ("pkv_status_string", "kv_block_pool_init", "kv_block_pool_destroy", "kv_cache_bytes",
+           "kv_scales_bytes", "kv_num_free_blocks", "kv_block_refcount", "kv_block_alloc",
+           "kv_block_share", "kv_block_free", "kv_reserve_slots", "kv_slot_mapping", "kv_append",
+           "paged_decode_workspace_bytes", "paged_decode_attention", "pkv_check_error")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, status_string(status), status))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libpkv.so (built by ``paged_kv_cache_273_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libpkv.so is not built (%s); run "
+                              "`python -m paged_kv_cache_273_gb300.build`" % LIB_PATH)
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, I32P, SZ, F = (ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                             ctypes.c_size_t, ctypes.c_float)
+        lib.pkv_status_string.argtypes = [I]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.kv_block_pool_init.argtypes = [ctypes.POINTER(P), I, I, I, I, I]
+        lib.kv_block_pool_init.restype = I
+        lib.kv_block_pool_destroy.argtypes = [P]
+        lib.kv_block_pool_destroy.restype = None
+        lib.kv_cache_bytes.argtypes = [P]
+        lib.kv_cache_bytes.restype = SZ
+        lib.kv_scales_bytes.argtypes = [P]
+        lib.kv_scales_bytes.restype = SZ
+        lib.kv_num_free_blocks.argtypes = [P]
+        lib.kv_num_free_blocks.restype = I
+        lib.kv_block_refcount.argtypes = [P, ctypes.c_int32]
+        lib.kv_block_refcount.restype = I
+        lib.kv_block_alloc.argtypes = [P, I, I32P]
+        lib.kv_block_alloc.restype = I
+        lib.kv_block_share.argtypes = [P, I32P, I]
+        lib.kv_block_share.restype = I
+        lib.kv_block_free.argtypes = [P, I32P, I]
+        lib.kv_block_free.restype = I
+        lib.kv_reserve_slots.argtypes = [P, I, I32P, I32P, I32P, I, I32P]
+        lib.kv_reserve_slots.restype = I
+        lib.kv_slot_mapping.argtypes = [I32P, I, I, I, I32P, I32P, I32P]
+        lib.kv_slot_mapping.restype = I
+        lib.kv_append.argtypes = [P, P, P, I, P, I, P, P, P, P, P]
+        lib.kv_append.restype = I
+        lib.paged_decode_workspace_bytes.argtypes = [P, I, I]
+        lib.paged_decode_workspace_bytes.restype = SZ
+        lib.paged_decode_attention.argtypes = [P, P, I, I, P, P, P, P, P, I, P, I, I, F, P, P,
+                                               SZ, P]
+        lib.paged_decode_attention.restype = I
+        lib.pkv_check_error.argtypes = [P, P]
+        lib.pkv_check_error.restype = I
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> int:
+    if status < 0:
+        raise PkvError(status, where)
+    return status
+
+
+def _i32(a) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a
+
+
+def _i32p(a: np.ndarray | None):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _dptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Pool:
+    """Handle of a ``pkv_pool`` (host bookkeeping of one shared block pool)."""
+
+    def __init__(self, handle: int, num_blocks: int, block_size: int, num_kv_heads: int,
+                 head_dim: int, kv_dtype: int):
+        self.handle = ctypes.c_void_p(handle)
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        self.num_kv_heads = num_kv_heads
+        self.head_dim = head_dim
+        self.kv_dtype = kv_dtype
+
+    def close(self):
+        if self.handle:
+            load().kv_block_pool_destroy(self.handle)
+            self.handle = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # convenience: caller-owned device buffers of the right shape
+    def alloc_cache(self, device="cuda"):
+        shape = (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
+        dt = TORCH_DTYPE[self.kv_dtype]
+        k = torch.zeros(shape, dtype=dt, device=device)
+        v = torch.zeros(shape, dtype=dt, device=device)
+        if self.kv_dtype == PKV_I8:
+            sshape = shape[:3]
+            return (k, v, torch.zeros(sshape, dtype=torch.float16, device=device),
+                    torch.zeros(sshape, dtype=torch.float16, device=device))
+        return k, v, None, None
+
+
+# ------------------------------------------------------------------ pool (host)
+def kv_block_pool_init(num_blocks, block_size, num_kv_heads, head_dim, kv_dtype) -> Pool:
+    h = ctypes.c_void_p()
+    _check(load().kv_block_pool_init(ctypes.byref(h), num_blocks, block_size, num_kv_heads,
+                                     head_dim, int(kv_dtype)), "kv_block_pool_init")
+    return Pool(h.value, num_blocks, block_size, num_kv_heads, head_dim, int(kv_dtype))
+
+
+def kv_block_pool_destroy(pool: Pool) -> None:
+    pool.close()
+
+
+def kv_cache_bytes(pool: Pool) -> int:
+    return int(load().kv_cache_bytes(pool.handle))
+
+
+def kv_scales_bytes(pool: Pool) -> int:
+    return int(load().kv_scales_bytes(pool.handle))
+
+
+def kv_num_free_blocks(pool: Pool) -> int:
+    return _check(load().kv_num_free_blocks(pool.handle), "kv_num_free_blocks")
+
+
+def kv_block_refcount(pool: Pool, block_id: int) -> int:
+    return _check(load().kv_block_refcount(pool.handle, int(block_id)), "kv_block_refcount")
+
+
+def kv_block_alloc(pool: Pool, n: int) -> np.ndarray:
+    out = np.zeros(max(n, 1), np.int32)
+    _check(load().kv_block_alloc(pool.handle, n, _i32p(out)), "kv_block_alloc")
+    return out[:n]
+
+
+def kv_block_share(pool: Pool, ids) -> None:
+    ids = _i32(ids)
+    _check(load().kv_block_share(pool.handle, _i32p(ids), ids.size), "kv_block_share")
+
+
+def kv_block_free(pool: Pool, ids) -> None:
+    ids = _i32(ids)
+    _check(load().kv_block_free(pool.handle, _i32p(ids), ids.size), "kv_block_free")
+
+
+def kv_reserve_slots(pool: Pool, seq_lens, block_tables: np.ndarray, num_new=None) -> np.ndarray:
+    """Allocate blocks for one append step; block_tables (int32 numpy, C order) is updated
+    in place.  Returns the slot mapping."""
+    if block_tables.dtype != np.int32 or not block_tables.flags.c_contiguous:
+        raise ValueError("block_tables must be a C-contiguous int32 array")
+    sl = _i32(seq_lens)
+    nn = None if num_new is None else _i32(num_new)
+    total = sl.size if nn is None else int(nn.sum())
+    slots = np.zeros(max(total, 1), np.int32)
+    _check(load().kv_reserve_slots(pool.handle, sl.size, _i32p(sl), _i32p(nn),
+                                   _i32p(block_tables), block_tables.shape[1], _i32p(slots)),
+           "kv_reserve_slots")
+    return slots[:total]
+
+
+def kv_slot_mapping(block_tables, block_size: int, start, num_new=None) -> np.ndarray:
+    bt = _i32(block_tables)
+    st = _i32(start)
+    nn = None if num_new is None else _i32(num_new)
+    total = st.size if nn is None else int(nn.sum())
+    slots = np.zeros(max(total, 1), np.int32)
+    _check(load().kv_slot_mapping(_i32p(bt), bt.shape[1], block_size, st.size, _i32p(st),
+                                  _i32p(nn), _i32p(slots)), "kv_slot_mapping")
+    return slots[:total]
+
+
+# ------------------------------------------------------------------ device calls
+def kv_append(pool: Pool, k_new, v_new, slot_mapping, k_cache, v_cache, k_scales=None,
+              v_scales=None, stream=None) -> None:
+    if k_new.dtype not in PKV_DTYPE:
+        raise ValueError("unsupported k_new dtype %s" % k_new.dtype)
+    if slot_mapping.dtype != torch.int32:
+        raise ValueError("slot_mapping must be int32")
+    T = k_new.shape[0]
+    _check(load().kv_append(pool.handle, _dptr(k_new), _dptr(v_new), PKV_DTYPE[k_new.dtype],
+                            _dptr(slot_mapping), T, _dptr(k_cache), _dptr(v_cache),
+                            _dptr(k_scales), _dptr(v_scales), _stream(stream)), "kv_append")
+
+
+def paged_decode_workspace_bytes(pool: Pool, batch: int, num_q_heads: int) -> int:
+    return int(load().paged_decode_workspace_bytes(pool.handle, batch, num_q_heads))
+
+
+def alloc_workspace(pool: Pool, batch: int, num_q_heads: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace (its counters must start at zero)."""
+    n = paged_decode_workspace_bytes(pool, batch, num_q_heads)
+    if n == 0:
+        raise PkvError(PKV_ERR_INVALID, "paged_decode_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def paged_decode_attention(pool: Pool, q, k_cache, v_cache, block_tables, seq_lens, scale: float,
+                           out, workspace, max_seq_len: int, k_scales=None, v_scales=None,
+                           stream=None) -> None:
+    if q.dtype not in PKV_DTYPE:
+        raise ValueError("unsupported q dtype %s" % q.dtype)
+    if out.dtype != torch.float32:
+        raise ValueError("out must be float32")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_tables and seq_lens must be int32")
+    B, Hq, _ = q.shape
+    _check(load().paged_decode_attention(
+        pool.handle, _dptr(q), PKV_DTYPE[q.dtype], Hq, _dptr(k_cache), _dptr(v_cache),
+        _dptr(k_scales), _dptr(v_scales), _dptr(block_tables), block_tables.shape[1],
+        _dptr(seq_lens), B, int(max_seq_len), float(scale), _dptr(out), _dptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "paged_decode_attention")
+
+
+def pkv_check_error(pool: Pool, stream=None) -> int:
+    """Synchronise and read/clear the device error word; returns the status (no raise)."""
+    return int(load().pkv_check_error(pool.handle, _stream(stream) if torch.cuda.is_available()
+                                      else ctypes.c_void_p(None)))

@@ -36,7 +36,7 @@ class Workload:
     q_dtype: int
     src_dtype: int         # type of the generated K/V rows (f16 for the int8 cache)
     seed: int
-    lengths: str           # "fixed", "uniform", "loguniform"
+    lengths: str           # "tiny", "fixed", "uniform", "loguniform"
     len_lo: int
     len_hi: int
     decode_steps: int      # appended tokens after the prefix
@@ -54,7 +54,7 @@ WORKLOADS = {
     # 4 q / 2 KV heads, d 64, block size 4, 16 blocks; sequences end at 7 and 3
     # tokens after one decode step (a 3-token prompt plus 4 decode steps, and a
     # bare 3-token prompt).
-    "tiny": Workload("tiny", 4, 2, 64, 4, 2, F32, F32, F32, 0, "fixed", 0, 0, 1),
+    "tiny": Workload("tiny", 4, 2, 64, 4, 2, F32, F32, F32, 0, "tiny", 0, 0, 1),
     # GPT-2-small-shaped MHA layer: 12 = 12 heads, d 64, bs 16, 64 sequences
     # with lengths uniform in [1, 2048], fp16.
     "gpt2": Workload("gpt2", 12, 12, 64, 16, 64, F16, F16, F16, 1, "uniform", 1, 2048, 1),
@@ -89,6 +89,11 @@ class Inputs:
     step_v: np.ndarray
     step_q: np.ndarray            # [steps, B, Hq, D] raw (q of each decode step)
     sharers: np.ndarray           # [B] bool: sequence uses the shared prefix blocks
+    idle: np.ndarray              # [B] bool: empty sequence, no tokens appended
+
+    def lens_after_step(self, s: int) -> np.ndarray:
+        """Cached tokens of every sequence after decode step s (0-based)."""
+        return np.where(self.idle, 0, self.prefix_lens + s + 1).astype(np.int32)
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -117,7 +122,7 @@ def _values(rng: np.random.Generator, shape, dtype: int, outlier_p=0.0, outlier_
 
 
 def _lengths(rng: np.random.Generator, wl: Workload) -> np.ndarray:
-    if wl.name == "tiny":
+    if wl.lengths == "tiny":
         return np.array([7, 3], np.int64)
     if wl.lengths == "fixed":
         return np.full(wl.batch, wl.len_lo + wl.decode_steps, np.int64)
@@ -129,19 +134,21 @@ def _lengths(rng: np.random.Generator, wl: Workload) -> np.ndarray:
     raise ValueError(wl.lengths)
 
 
-def make_inputs(wl: Workload | str, tiny_lengths=None) -> Inputs:
+def make_inputs(wl: Workload | str, lengths=None) -> Inputs:
     """Draw the inputs of a workload.
 
-    tiny_lengths: for the tiny workload, the final lengths (default (7, 3));
-    (8, 4) is the other reading where 7 and 3 are the lengths before the step.
+    lengths: explicit final lengths (one per sequence) instead of the
+    workload's recipe; e.g. (8, 4) for the tiny workload is the reading in
+    which 7 and 3 are the lengths before the decode step.
     """
     if isinstance(wl, str):
         wl = WORKLOADS[wl]
     rng = np.random.default_rng(wl.seed)
-    B, Hq, Hkv, D, bs = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
     final = _lengths(rng, wl)
-    if wl.name == "tiny" and tiny_lengths is not None:
-        final = np.asarray(tiny_lengths, np.int64)
+    if lengths is not None:
+        final = np.asarray(lengths, np.int64)
+        wl = dataclasses.replace(wl, batch=len(final))
+    B, Hq, Hkv, D, bs = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
     steps = wl.decode_steps
 
     sharers = np.zeros(B, bool)
@@ -151,7 +158,9 @@ def make_inputs(wl: Workload | str, tiny_lengths=None) -> Inputs:
         sharers[who] = True
         # a sharer's decode step must land past the shared blocks
         final = np.where(sharers, np.maximum(final, P + steps), final)
-    prefix = final - steps
+    # An empty sequence (final length 0) takes no part in the decode steps.
+    idle = final == 0
+    prefix = np.where(idle, 0, final - steps)
     if np.any(prefix < 0):
         raise ValueError("lengths shorter than the decode steps")
 
@@ -160,7 +169,7 @@ def make_inputs(wl: Workload | str, tiny_lengths=None) -> Inputs:
     shared_blocks = P // bs if P > 0 else 0
     private = nblk - np.where(sharers, shared_blocks, 0)
     unique = int(private.sum()) + shared_blocks
-    if wl.name == "tiny":
+    if wl.name == "tiny" and unique <= 16:
         num_blocks = 16
     else:
         num_blocks = int(math.ceil(unique * (1.0 + wl.pool_slack)))
@@ -199,7 +208,7 @@ def make_inputs(wl: Workload | str, tiny_lengths=None) -> Inputs:
     sv = _values(rng, (steps, B, Hkv, D), wl.src_dtype, wl.outlier_p, wl.outlier_scale)
     sq = _values(rng, (steps, B, Hq, D), wl.q_dtype)
     return Inputs(wl, num_blocks, final.astype(np.int32), prefix.astype(np.int32), tables, hk, hv,
-                  offs, write, sk, sv, sq, sharers)
+                  offs, write, sk, sv, sq, sharers, idle)
 
 
 def positions_of_history(inp: Inputs) -> tuple[np.ndarray, np.ndarray]:
