@@ -440,11 +440,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const Params 
     }
     __syncthreads();
 
+    // The T tiles are split over P = min(grid, T) CTAs, so that every CTA
+    // that takes part owns at least one tile and the CTAs holding pieces of
+    // one sequence/head are consecutive (the merge counts on both).
     const int64_t T = s_tstart[B];
-    const int P = gridDim.x;
+    const int P = (int)min((int64_t)gridDim.x, T);
     const int cta = blockIdx.x;
-    const int64_t R0 = (int64_t)cta * T / P;
-    const int64_t R1 = (int64_t)(cta + 1) * T / P;
+    const int64_t R0 = cta < P ? (int64_t)cta * T / P : 0;
+    const int64_t R1 = cta < P ? (int64_t)(cta + 1) * T / P : 0;
     const int Hq = p.num_q_heads;
 
     if (warp == W) {
@@ -569,8 +572,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const Params 
         float *ps = psbuf + w * (TILE * G + G);
         float *mw = merge + w * G * (D + 2);
 
-        // Zero rows of empty sequences; sequence b is CTA (b % P)'s job.
-        for (int b = cta; b < B; b += P) {
+        // Zero rows of empty sequences; sequence b is CTA (b % grid)'s job.
+        for (int b = cta; b < B; b += gridDim.x) {
             if (s_len[b] == 0)
                 for (int idx = ctid; idx < Hq * D; idx += W * 32)
                     p.out[(int64_t)b * Hq * D + idx] = 0.0f;

@@ -172,7 +172,7 @@ def make_inputs(wl: Workload | str, lengths=None) -> Inputs:
     if wl.name == "tiny" and unique <= 16:
         num_blocks = 16
     else:
-        num_blocks = int(math.ceil(unique * (1.0 + wl.pool_slack)))
+        num_blocks = max(1, int(math.ceil(unique * (1.0 + wl.pool_slack))))
     perm = rng.permutation(num_blocks).astype(np.int32)
     max_blocks = int(nblk.max()) if B else 1
     tables = np.zeros((B, max(max_blocks, 1)), np.int32)

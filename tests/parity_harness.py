@@ -219,4 +219,11 @@ def run(inp: W.Inputs, steps=None, check_steps=None, seqs=None, device="cuda") -
     result["tol"] = TOL[wl.kv_dtype]
     result["error_word"] = pkv.pkv_check_error(case.pool)
     result["guards"] = case.guards_intact()
+    result["counters_zero"] = counters_zero(case)
     return result
+
+
+def counters_zero(case: Case) -> bool:
+    """Every call must leave the workspace's per-(sequence, KV head) counters at zero."""
+    n = case.wl.batch * case.wl.num_kv_heads
+    return not bool(case.workspace[:n * 4].view(torch.int32).any().item())

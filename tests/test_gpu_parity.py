@@ -24,6 +24,7 @@ def _assert_ok(res):
     assert res["max_err"] <= res["tol"], res
     assert res["error_word"] == pkv.PKV_OK
     assert res["guards"], "a canary around a device buffer was overwritten"
+    assert res["counters_zero"], "a split-merge counter was left non-zero"
 
 
 # ------------------------------------------------------------------ the five workloads
@@ -105,6 +106,15 @@ def test_one_long_sequence_split_over_all_ctas():
 
 def test_fewer_tiles_than_ctas():
     inp = _custom("few", 4, 2, 64, 16, W.F16, [3, 20], seed=47)
+    _assert_ok(run(inp))
+
+
+@pytest.mark.parametrize("lens", [[1, 15, 16, 17, 53, 777], [33], [16, 16, 16, 40],
+                                  [2000, 3, 70, 0, 129]])
+def test_split_sequences_with_idle_ctas(lens):
+    # fewer 16-token tiles than SMs, so some CTAs own no tile while
+    # multi-tile sequences are still split across several CTAs
+    inp = _custom("idle", 8, 2, 128, 16, W.BF16, lens, seed=len(lens))
     _assert_ok(run(inp))
 
 
