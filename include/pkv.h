@@ -252,6 +252,39 @@ int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtyp
                            pkv_stream_t stream);
 
 /*
+ * paged_decode_attention_noalloc — paged_decode_attention for callers that
+ * cannot allocate device memory.  The pages have no counterpart; this is a
+ * property of this library's interface, not of the method.
+ *
+ * Same arguments and result as paged_decode_attention, without the
+ * workspace: the scratch comes from a fixed 4 MiB array in the library's
+ * device image (every GPU that loads the library holds it until exit).  It
+ * suits code that may not call cudaMalloc at the point of the call: an
+ * allocator hook or host callback that would re-enter the allocator, a
+ * serving loop that must not allocate after start-up, or a process whose
+ * device memory is fully reserved by another runtime's pool.
+ *
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Each call clears the part of the array it uses (cudaMemsetAsync on
+ *    `stream`), then runs the same kernel as paged_decode_attention.  It
+ *    calls no cudaMalloc/cudaFree and no allocating library routine.
+ *  - All calls on a device share the array: calls that may overlap on the
+ *    GPU (different streams without ordering) race; order them.
+ *  - Returns PKV_ERR_UNSUPPORTED when the batch needs more scratch than the
+ *    array holds (paged_decode_workspace_bytes() > 4 MiB: on 152 SMs, more
+ *    than about 1,800 sequence x KV-head pairs at G = 4, d = 128, or about
+ *    850 at G = 8).
+ */
+int paged_decode_attention_noalloc(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
+                                   int num_q_heads, const void *k_cache, const void *v_cache,
+                                   const void *k_scales, const void *v_scales,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *seq_lens, int batch, int max_seq_len,
+                                   float scale, float *out, pkv_stream_t stream);
+
+/*
  * pkv_check_error — synchronise the stream, read and clear the pool's device
  * error word.  Returns PKV_OK, PKV_ERR_BAD_INDEX, PKV_ERR_TIMEOUT (a bounded
  * wait inside a kernel gave up; the kernel returned without finishing), or
