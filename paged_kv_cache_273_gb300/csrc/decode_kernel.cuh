@@ -18,7 +18,7 @@
 //    balanced to +-1 tile whatever the length mix).
 //  * In each CTA one producer warp issues bulk async copies (cp.async.bulk)
 //    of whole K and V tiles, located through the block table, into a ring of
-//    shared-memory stages guarded by mbarriers; eight consumer warps take
+//    shared-memory stages guarded by mbarriers; 15 (or 11) consumer warps take
 //    tiles round-robin, each keeping its own online-softmax state (the
 //    FlashAttention idea of never materialising the score row, from the
 //    guide's "Flash attention: don't build the giant matrix").
@@ -46,17 +46,25 @@ namespace kern {
 using namespace dev;
 
 constexpr int TILE = 16;        // tokens per pipeline stage
-constexpr int NWARP_C = 8;      // consumer warps per CTA
-constexpr int NTHREADS = (NWARP_C + 1) * 32;
 constexpr int MAX_STAGES = 32;
 // misc ints in shared memory: [0] abort flag, [1] "merge partials" flag,
-// [2] a constant zero, [8..8+NWARPS) scan scratch, [32..32+MAX_STAGES) last
-// issued round per stage (+1; 0 = never), [64..66) q copies issued per slot.
+// [2] a constant zero, [8..8+warps) scan scratch, [32..32+MAX_STAGES) last
+// issued round per stage (+1; 0 = never), [64..66) q copies issued per slot,
+// [66] number of q copies issued so far (they go out in piece order).
 constexpr int MISC_INTS = 72;
 constexpr int MISC_ISSUED = 32;
 constexpr int MISC_QISSUED = 64;
+constexpr int MISC_QCOUNT = 66;
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// Consumer warps per CTA.  The tile math of 16-bit K/V with G <= 4 (and int8
+// with G <= 2) fits in 128 registers, so 15 consumer warps + the producer
+// fill 16 warps per SM; larger groups need up to 168 registers: 11 + 1.
+__host__ __device__ constexpr int consumer_warps(int G, int KV)
+{
+    return ((KV == PKV_BF16 || KV == PKV_F16) && G <= 4) || (KV == PKV_I8 && G <= 2) ? 15 : 11;
+}
 
 template <int KV>
 struct KvBytes;
@@ -67,7 +75,8 @@ template <> struct KvBytes<PKV_I8> { static constexpr int v = 1; };
 
 template <int D, int G, int KV>
 struct Cfg {
-    static constexpr int W = NWARP_C;
+    static constexpr int W = consumer_warps(G, KV);
+    static constexpr int NTHREADS = (W + 1) * 32;
     static constexpr int EB = KvBytes<KV>::v;
     static constexpr int ROWB = D * EB;            // bytes of one cached row
     static constexpr int NCH = ROWB / 16;          // 16-byte chunks per row
@@ -83,7 +92,9 @@ struct Cfg {
     static constexpr int STAGE_BYTES = round_up(2 * KV_BYTES + 2 * SC_BYTES, 128);
     static constexpr int QSLOT = round_up(G * D * 4, 128);   // fits any q dtype
     static constexpr int MERGE_FLOATS = W * G * (D + 2);
-    static constexpr int PS_FLOATS = W * (TILE * G + G);
+    // per warp: {p, p} pairs of the tile ([TILE][G] float2) + G rescale factors
+    static constexpr int PSW = round_up(TILE * 2 * G + G, 4);
+    static constexpr int PS_FLOATS = W * PSW;
     static_assert(NCH >= 4 && (NCH % DS) == 0, "row must split into 16-byte chunks");
     static_assert(TPL * TQ == TILE, "tile split");
 };
@@ -128,7 +139,7 @@ __host__ __device__ inline Layout make_layout(int nst, int batch)
     int o = 0;
     L.stages = o; o += nst * C::STAGE_BYTES;
     L.qring = o; o += 2 * C::QSLOT;
-    L.merge = o; o += C::MERGE_FLOATS * 4;
+    L.merge = o; o += round_up(C::MERGE_FLOATS * 4, 16);
     L.ps = o; o += C::PS_FLOATS * 4;
     L.lens = o; o += batch * 4;
     L.tstart = o; o += (batch + 1) * 4;
@@ -347,13 +358,32 @@ __device__ __forceinline__ void load_v(float (&v)[D / 32], const unsigned char *
     }
 }
 
+// 2^x with the hardware approximation (relative error ~2^-22; -inf -> +0).
+__device__ __forceinline__ float exp2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// (a0, a1) += (b0, b1) * (c0, c1) as one packed fp32x2 FMA.
+__device__ __forceinline__ void fma2(float &a0, float &a1, float b0, float b1, float c0, float c1)
+{
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%0, %1};\n\t"
+        "fma.rn.f32x2 z, x, y, z;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // ---- the kernel ---------------------------------------------------------------
 
 template <int D, int G, int KV>
-__global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const Params p)
+__global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kernel(const Params p)
 {
     using C = Cfg<D, G, KV>;
     constexpr int W = C::W;
+    constexpr int NTHREADS = C::NTHREADS;
     extern __shared__ __align__(128) unsigned char smem[];
     const Layout lay = make_layout<D, G, KV>(p.nst, p.batch);
     unsigned char *stages = smem + lay.stages;
@@ -452,116 +482,139 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const Params 
 
     if (warp == W) {
         // ================= producer warp =================
-        int64_t seg_prev = -1;
-        int qn = 0;
+        // The warp issues tiles in groups of GRP = min(32, stages): lane j
+        // copies tile k0 + j into its own stage, so the lanes of a group wait
+        // for their stages and issue their copies in parallel (a stage is free
+        // again only after its tile of an earlier group was consumed).  The
+        // next group's block ids are fetched while this group is issued.
         const int n_local = (int)(R1 - R0);
         const int bs = p.block_size;
+        const int GRP = min(32, p.nst);
         const uint64_t policy = policy_evict_first();
-        for (int k0 = 0; k0 < n_local; k0 += 32) {
-            // Lane j describes tile R0 + k0 + j.
-            int b = 0, kvh = 0, ti = 0, nvalid = 0, nblk = 0;
-            int32_t id0 = -1, id1 = -1, id2 = -1, id3 = -1;
-            if (k0 + lane < n_local) {
+        struct Desc { int b, kvh, ti, nblk; int32_t id[4]; };
+        auto describe = [&](int k0) {
+            Desc d{0, 0, 0, 0, {-1, -1, -1, -1}};
+            if (lane < GRP && k0 + lane < n_local) {
                 const int64_t x = R0 + k0 + lane;
-                b = find_seq(s_tstart, B, x);
-                const int nt = (s_tstart[b + 1] - s_tstart[b]) / Hkv;
-                const int off = (int)(x - s_tstart[b]);
-                kvh = off / nt;
-                ti = off - kvh * nt;
-                nvalid = min(TILE, s_len[b] - TILE * ti);
-                const int32_t *row = p.block_tables + (int64_t)b * p.max_blocks_per_seq;
-                const int first = (TILE * ti) >> p.bs_log2;
-                if (bs >= TILE) {
-                    nblk = 1;
-                    id0 = __ldg(row + first);
-                } else {
-                    nblk = (nvalid + bs - 1) >> p.bs_log2;   // 1..4 (bs >= 4)
-                    id0 = __ldg(row + first);
-                    if (nblk > 1) id1 = __ldg(row + first + 1);
-                    if (nblk > 2) id2 = __ldg(row + first + 2);
-                    if (nblk > 3) id3 = __ldg(row + first + 3);
-                }
+                d.b = find_seq(s_tstart, B, x);
+                const int nt = (s_tstart[d.b + 1] - s_tstart[d.b]) / Hkv;
+                const int off = (int)(x - s_tstart[d.b]);
+                d.kvh = off / nt;
+                d.ti = off - d.kvh * nt;
+                const int nvalid = min(TILE, s_len[d.b] - TILE * d.ti);
+                const int32_t *row = p.block_tables + (int64_t)d.b * p.max_blocks_per_seq;
+                const int first = (TILE * d.ti) >> p.bs_log2;
+                d.nblk = bs >= TILE ? 1 : (nvalid + bs - 1) >> p.bs_log2;   // 1..4 (bs >= 4)
+                d.id[0] = __ldg(row + first);
+                if (d.nblk > 1) d.id[1] = __ldg(row + first + 1);
+                if (d.nblk > 2) d.id[2] = __ldg(row + first + 2);
+                if (d.nblk > 3) d.id[3] = __ldg(row + first + 3);
             }
-            const int cnt = min(32, n_local - k0);
-            for (int j = 0; j < cnt; ++j) {
-                const int bj = __shfl_sync(FULL_MASK, b, j);
-                const int kvhj = __shfl_sync(FULL_MASK, kvh, j);
-                const int tij = __shfl_sync(FULL_MASK, ti, j);
-                const int nbj = __shfl_sync(FULL_MASK, nblk, j);
-                int32_t ids[4];
-                ids[0] = __shfl_sync(FULL_MASK, id0, j);
-                ids[1] = __shfl_sync(FULL_MASK, id1, j);
-                ids[2] = __shfl_sync(FULL_MASK, id2, j);
-                ids[3] = __shfl_sync(FULL_MASK, id3, j);
-                if (lane == 0) {
-                    const int k = k0 + j;
-                    const int64_t seg = (int64_t)bj * Hkv + kvhj;
-                    if (seg != seg_prev) {
-                        const int slot = qn & 1;
-                        if (mbar_wait_bounded(&qempty[slot], ((qn >> 1) & 1) ^ 1, abort_flag)) {
-                            const uint32_t qbytes = (uint32_t)(G * D * p.q_bytes);
-                            mbar_arrive_expect_tx(&qfull[slot], qbytes);
-                            const unsigned char *qsrc = static_cast<const unsigned char *>(p.q) +
-                                                        ((int64_t)bj * Hq + kvhj * G) * D * p.q_bytes;
-                            bulk_g2s(qring + slot * C::QSLOT, qsrc, qbytes, &qfull[slot]);
-                            misc[MISC_QISSUED + slot] = (qn >> 1) + 1;
-                        } else if (!*abort_flag) {
-                            *abort_flag = 1;
-                            atomicOr(p.err, PKV_EBIT_TIMEOUT);
-                        }
-                        ++qn;
-                        seg_prev = seg;
-                    }
-                    const int st = k % p.nst;
-                    const uint32_t par = (uint32_t)((k / p.nst) & 1) ^ 1u;
-                    if (mbar_wait_bounded(&empty[st], par, abort_flag)) {
-                        unsigned char *sK = stages + st * C::STAGE_BYTES;
-                        unsigned char *sV = sK + C::KV_BYTES;
-                        unsigned char *sKS = sV + C::KV_BYTES;
-                        unsigned char *sVS = sKS + C::SC_BYTES;
-                        // Count bytes of the copies that will be issued.
-                        const int rows_per_copy = bs >= TILE ? TILE : bs;
-                        const uint32_t kv_copy = (uint32_t)(rows_per_copy * C::ROWB);
-                        const uint32_t sc_copy = (uint32_t)(rows_per_copy * 2);
-                        uint32_t total = 0;
-                        bool bad = false;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            if (u < nbj) {
-                                if (ids[u] >= 0 && ids[u] < p.num_blocks)
-                                    total += 2 * kv_copy + (KV == PKV_I8 ? 2 * sc_copy : 0);
-                                else
-                                    bad = true;
-                            }
-                        }
-                        if (bad)
-                            atomicOr(p.err, PKV_EBIT_BLOCK);
-                        mbar_arrive_expect_tx(&full[st], total);
-                        misc[MISC_ISSUED + st] = k / p.nst + 1;
-                        const int in_block = (TILE * tij) & (bs - 1);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            if (u < nbj && ids[u] >= 0 && ids[u] < p.num_blocks) {
-                                const int64_t row0 =
-                                    ((int64_t)ids[u] * Hkv + kvhj) * bs + (bs >= TILE ? in_block : 0);
-                                const int dst_row = u * rows_per_copy;
-                                bulk_g2s_hint(sK + dst_row * C::ROWB, p.k_cache + row0 * C::ROWB,
-                                              kv_copy, &full[st], policy);
-                                bulk_g2s_hint(sV + dst_row * C::ROWB, p.v_cache + row0 * C::ROWB,
-                                              kv_copy, &full[st], policy);
-                                if constexpr (KV == PKV_I8) {
-                                    bulk_g2s(sKS + dst_row * 2, p.k_scales + row0, sc_copy, &full[st]);
-                                    bulk_g2s(sVS + dst_row * 2, p.v_scales + row0, sc_copy, &full[st]);
-                                }
-                            }
-                        }
+            return d;
+        };
+        long long seg_last = -1;                // (sequence, KV head) of the previous tile
+        int qn_base = 0;                        // q copies issued before this group
+        int st_base = 0, rnd_base = 0;          // stage and ring round of tile k0
+        Desc cur = describe(0);
+        for (int k0 = 0; k0 < n_local; k0 += GRP) {
+            const Desc nxt = describe(k0 + GRP);
+            const int n = min(GRP, n_local - k0);
+            const bool active = lane < n;
+            const long long seg = active ? (long long)cur.b * Hkv + cur.kvh : -1;
+            long long prev = __shfl_up_sync(FULL_MASK, seg, 1);
+            if (lane == 0)
+                prev = seg_last;
+            const bool starts = active && seg != prev;      // first tile of a piece
+            const unsigned start_mask = __ballot_sync(FULL_MASK, starts);
+            const int qn = qn_base + __popc(start_mask & ((1u << lane) - 1u));
+            int st = st_base + lane, rnd = rnd_base;
+            if (st >= p.nst) {
+                st -= p.nst;
+                ++rnd;
+            }
+            if (active) {
+                if (starts) {
+                    // q copies leave in piece order: the q ring has two slots and
+                    // a parity wait only tells one phase from the next, so copy
+                    // qn may wait for its slot only after copy qn - 1 has gone
+                    // (which itself waited for the slot's previous use).
+                    volatile int *qcount = misc + MISC_QCOUNT;
+                    const int slot = qn & 1;
+                    // A lane that gives up raises the abort flag before passing
+                    // its turn on, so later lanes issue nothing out of order.
+                    bool ok = count_wait_bounded(qcount, qn, abort_flag) && !*abort_flag;
+                    if (ok)
+                        ok = mbar_wait_bounded(&qempty[slot], ((qn >> 1) & 1) ^ 1, abort_flag);
+                    if (ok) {
+                        const uint32_t qbytes = (uint32_t)(G * D * p.q_bytes);
+                        mbar_arrive_expect_tx(&qfull[slot], qbytes);
+                        const unsigned char *qsrc = static_cast<const unsigned char *>(p.q) +
+                                                    ((int64_t)cur.b * Hq + cur.kvh * G) * D * p.q_bytes;
+                        bulk_g2s(qring + slot * C::QSLOT, qsrc, qbytes, &qfull[slot]);
+                        atomicMax(&misc[MISC_QISSUED + slot], (qn >> 1) + 1);
                     } else if (!*abort_flag) {
                         *abort_flag = 1;
                         atomicOr(p.err, PKV_EBIT_TIMEOUT);
                     }
+                    __threadfence_block();
+                    *qcount = qn + 1;
                 }
-                __syncwarp();
+                if (mbar_wait_bounded(&empty[st], (uint32_t)(rnd & 1) ^ 1u, abort_flag)) {
+                    unsigned char *sK = stages + st * C::STAGE_BYTES;
+                    unsigned char *sV = sK + C::KV_BYTES;
+                    unsigned char *sKS = sV + C::KV_BYTES;
+                    unsigned char *sVS = sKS + C::SC_BYTES;
+                    const int rows_per_copy = bs >= TILE ? TILE : bs;
+                    const uint32_t kv_copy = (uint32_t)(rows_per_copy * C::ROWB);
+                    const uint32_t sc_copy = (uint32_t)(rows_per_copy * 2);
+                    // Count the bytes of the copies that will be issued.
+                    uint32_t total = 0;
+                    bool bad = false;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (u < cur.nblk) {
+                            if (cur.id[u] >= 0 && cur.id[u] < p.num_blocks)
+                                total += 2 * kv_copy + (KV == PKV_I8 ? 2 * sc_copy : 0);
+                            else
+                                bad = true;
+                        }
+                    }
+                    if (bad)
+                        atomicOr(p.err, PKV_EBIT_BLOCK);
+                    mbar_arrive_expect_tx(&full[st], total);
+                    // Tell the consumers that this round of the stage is armed.
+                    reinterpret_cast<volatile int *>(misc)[MISC_ISSUED + st] = rnd + 1;
+                    const int in_block = (TILE * cur.ti) & (bs - 1);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (u < cur.nblk && cur.id[u] >= 0 && cur.id[u] < p.num_blocks) {
+                            const int64_t row0 = ((int64_t)cur.id[u] * Hkv + cur.kvh) * bs +
+                                                 (bs >= TILE ? in_block : 0);
+                            const int dst_row = u * rows_per_copy;
+                            bulk_g2s_hint(sK + dst_row * C::ROWB, p.k_cache + row0 * C::ROWB,
+                                          kv_copy, &full[st], policy);
+                            bulk_g2s_hint(sV + dst_row * C::ROWB, p.v_cache + row0 * C::ROWB,
+                                          kv_copy, &full[st], policy);
+                            if constexpr (KV == PKV_I8) {
+                                bulk_g2s(sKS + dst_row * 2, p.k_scales + row0, sc_copy, &full[st]);
+                                bulk_g2s(sVS + dst_row * 2, p.v_scales + row0, sc_copy, &full[st]);
+                            }
+                        }
+                    }
+                } else if (!*abort_flag) {
+                    *abort_flag = 1;
+                    atomicOr(p.err, PKV_EBIT_TIMEOUT);
+                }
             }
+            __syncwarp();
+            seg_last = __shfl_sync(FULL_MASK, seg, n - 1);
+            qn_base += __popc(start_mask);
+            st_base += n;
+            if (st_base >= p.nst) {
+                st_base -= p.nst;
+                ++rnd_base;
+            }
+            cur = nxt;
         }
     } else {
         // ================= consumer warps =================
@@ -569,7 +622,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const Params 
         const int ds = lane % C::DS;
         const int tq = lane / C::DS;
         const int ctid = tid;                  // 0 .. W*32-1
-        float *ps = psbuf + w * (TILE * G + G);
+        float *ps = psbuf + w * C::PSW;
         float *mw = merge + w * G * (D + 2);
 
         // Zero rows of empty sequences; sequence b is CTA (b % grid)'s job.
@@ -623,11 +676,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const Params 
                     acc[g][e] = 0.0f;
 
             const int kfirst = k0 + (w - k0 % W + W) % W;
+            int st = kfirst % p.nst;                 // stage and ring round of tile kfirst
+            int rnd = kfirst / p.nst;
             for (int k = kfirst; k < k1; k += W) {
                 const int ti = ti0 + (k - k0);
                 const int nvalid = min(TILE, L - TILE * ti);
-                const int st = k % p.nst;
-                if (!mbar_wait_bounded(&full[st], (uint32_t)((k / p.nst) & 1), abort_flag) &&
+                // Warps take tiles round-robin and may drift apart, so this
+                // warp can reach tile k while the stage's previous tile
+                // (k - stages) is still landing; a parity wait alone would
+                // mistake that phase for an older completed one.  So first
+                // wait until the producer has armed this round of the stage
+                // (it records the round after arming the barrier), then the
+                // parity wait is unambiguous.
+                const bool armed =
+                    count_wait_bounded(misc + MISC_ISSUED + st, rnd + 1, abort_flag);
+                if (!(armed && mbar_wait_bounded(&full[st], (uint32_t)rnd & 1u, abort_flag)) &&
                     !*abort_flag) {
                     *abort_flag = 1;
                     atomicOr(p.err, PKV_EBIT_TIMEOUT);
@@ -651,82 +714,104 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const Params 
                 float kscale = p.scale_log2;
                 if constexpr (KV == PKV_I8)
                     kscale *= __half2float(sKS[t]);
+                bool above = false;
 #pragma unroll
-                for (int r = 0; r < C::NF; ++r)
+                for (int r = 0; r < C::NF; ++r) {
                     s[r] = t < nvalid ? part[r] * kscale : -INFINITY;
-                // Tile maximum per head over the lanes holding that head.
-                float mx[C::NF];
+                    above |= s[r] > m_run[r];
+                }
+                // The running maximum only needs to move when some score
+                // exceeds it (softmax is shift invariant, so any running value
+                // that is one of the scores seen is exact); most tiles skip
+                // the per-head maximum and the rescale.
+                const bool moved = __any_sync(FULL_MASK, above);
+                float corr[C::NF];
+                if (moved) {
+#pragma unroll
+                    for (int r = 0; r < C::NF; ++r) {
+                        float mx = s[r];
+#pragma unroll
+                        for (int mask = 2; mask < 32; mask <<= 1)
+                            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, mask));
+                        const float mnew = fmaxf(m_run[r], mx);   // finite: a valid token
+                        corr[r] = exp2_approx(m_run[r] - mnew);
+                        l_run[r] *= corr[r];
+                        m_run[r] = mnew;
+                    }
+                }
+                float pr[C::NF];
 #pragma unroll
                 for (int r = 0; r < C::NF; ++r) {
-                    mx[r] = s[r];
-#pragma unroll
-                    for (int mask = 2; mask < 32; mask <<= 1)
-                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(FULL_MASK, mx[r], mask));
+                    pr[r] = exp2_approx(s[r] - m_run[r]);
+                    l_run[r] += pr[r];
                 }
-                float corr[C::NF], pr[C::NF];
-#pragma unroll
-                for (int r = 0; r < C::NF; ++r) {
-                    const float mnew = fmaxf(m_run[r], mx[r]);   // finite: tile has a valid token
-                    corr[r] = exp2f(m_run[r] - mnew);
-                    pr[r] = exp2f(s[r] - mnew);
-                    l_run[r] = l_run[r] * corr[r] + pr[r];
-                    m_run[r] = mnew;
-                }
-                // Publish p (times the V scale for int8) and the rescale factors.
+                // Publish {p, p} pairs (p times the V scale for int8) and, when
+                // the maximum moved, the rescale factors.
                 if (G >= 2 || (ds & 1) == 0) {
                     float vsc = 1.0f;
                     if constexpr (KV == PKV_I8)
                         vsc = __half2float(sVS[t]);
+                    float2 *pp = reinterpret_cast<float2 *>(ps + t * 2 * G) + g0;
 #pragma unroll
-                    for (int r = 0; r < C::NF; ++r)
-                        ps[t * G + g0 + r] = pr[r] * vsc;
-                    if (tq == 0 && (ds >> 1) == 0) {
+                    for (int r = 0; r < C::NF; ++r) {
+                        const float v = pr[r] * vsc;
+                        pp[r] = make_float2(v, v);
+                    }
+                    if (moved && tq == 0 && (ds >> 1) == 0) {
 #pragma unroll
                         for (int r = 0; r < C::NF; ++r)
-                            ps[TILE * G + g0 + r] = corr[r];
+                            ps[TILE * 2 * G + g0 + r] = corr[r];
                     }
                 }
                 __syncwarp();
 
                 // ---- weighted V
-                float cg[G];
+                if (moved) {
 #pragma unroll
-                for (int g = 0; g < G; ++g)
-                    cg[g] = ps[TILE * G + g];
+                    for (int g = 0; g < G; ++g) {
+                        const float cg = ps[TILE * 2 * G + g];
 #pragma unroll
-                for (int g = 0; g < G; ++g)
+                        for (int e = 0; e < C::VE; ++e)
+                            acc[g][e] *= cg;
+                    }
+                }
+                auto pv_token = [&](int tt) {
+                    float v[C::VE];
+                    load_v<D, KV>(v, sV, tt, lane);
+                    const float *pt = ps + tt * 2 * G;
+                    if constexpr (G == 1) {
+                        const float2 w2 = *reinterpret_cast<const float2 *>(pt);
 #pragma unroll
-                    for (int e = 0; e < C::VE; ++e)
-                        acc[g][e] *= cg[g];
+                        for (int e = 0; e < C::VE; e += 2)
+                            fma2(acc[0][e], acc[0][e + 1], w2.x, w2.y, v[e], v[e + 1]);
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < G; g += 2) {
+                            const float4 w4 = *reinterpret_cast<const float4 *>(pt + 2 * g);
+#pragma unroll
+                            for (int e = 0; e < C::VE; e += 2) {
+                                fma2(acc[g][e], acc[g][e + 1], w4.x, w4.y, v[e], v[e + 1]);
+                                fma2(acc[g + 1][e], acc[g + 1][e + 1], w4.z, w4.w, v[e], v[e + 1]);
+                            }
+                        }
+                    }
+                };
                 if (nvalid == TILE) {
 #pragma unroll
-                    for (int tt = 0; tt < TILE; ++tt) {
-                        float v[C::VE];
-                        load_v<D, KV>(v, sV, tt, lane);
-#pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float pg = ps[tt * G + g];
-#pragma unroll
-                            for (int e = 0; e < C::VE; ++e)
-                                acc[g][e] = fmaf(pg, v[e], acc[g][e]);
-                        }
-                    }
+                    for (int tt = 0; tt < TILE; ++tt)
+                        pv_token(tt);
                 } else {
-                    for (int tt = 0; tt < nvalid; ++tt) {
-                        float v[C::VE];
-                        load_v<D, KV>(v, sV, tt, lane);
-#pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float pg = ps[tt * G + g];
-#pragma unroll
-                            for (int e = 0; e < C::VE; ++e)
-                                acc[g][e] = fmaf(pg, v[e], acc[g][e]);
-                        }
-                    }
+                    for (int tt = 0; tt < nvalid; ++tt)
+                        pv_token(tt);
                 }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&empty[st]);
+                st += W;
+                while (st >= p.nst) {
+                    st -= p.nst;
+                    ++rnd;
+                }
             }
 
             // ---- merge the W warp states of this piece
@@ -816,7 +901,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const Params 
     // Let every copy this CTA issued land before the CTA exits (only matters
     // after a timeout; otherwise the consumers already waited for all of them).
     __syncthreads();
-    if (*abort_flag && tid == NWARP_C * 32) {
+    if (*abort_flag && tid == W * 32) {
         for (int s = 0; s < p.nst; ++s)
             if (misc[MISC_ISSUED + s] > 0)
                 mbar_wait_bounded(&full[s], (uint32_t)((misc[MISC_ISSUED + s] - 1) & 1), misc + 2);
@@ -863,7 +948,7 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
         P = max_tiles;
     if (P < 1)
         P = 1;
-    paged_decode_kernel<D, G, KV><<<(int)P, NTHREADS, lay.total, stream>>>(prm);
+    paged_decode_kernel<D, G, KV><<<(int)P, C::NTHREADS, lay.total, stream>>>(prm);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

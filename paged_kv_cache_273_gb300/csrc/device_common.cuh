@@ -86,6 +86,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// Wait until the shared counter *c reaches target (another thread of the
+// CTA advances it).  Bounded like mbar_wait_bounded.
+__device__ __forceinline__ bool count_wait_bounded(volatile int *c, int target,
+                                                   volatile int *abort)
+{
+    if (*c >= target)
+        return true;
+    uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (*c >= target)
+            return true;
+        if ((it & 63u) == 0) {
+            if (*abort)
+                return false;
+            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS)
+                return false;
+        }
+    }
+}
+
 // Bulk (non-tensor) async copy global -> this CTA's shared memory; completion
 // is counted in bytes on the mbarrier.  dst, src 16-byte aligned; bytes a
 // multiple of 16.
