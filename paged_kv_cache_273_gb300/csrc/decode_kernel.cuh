@@ -37,6 +37,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "device_common.cuh"
 
@@ -58,12 +59,13 @@ constexpr int MISC_QCOUNT = 66;
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// Consumer warps per CTA.  The tile math of 16-bit K/V with G <= 4 (and int8
-// with G <= 2) fits in 128 registers, so 15 consumer warps + the producer
-// fill 16 warps per SM; larger groups need up to 168 registers: 11 + 1.
+// Consumer warps per CTA.  With G <= 2 the tile math of 16-bit or int8 K/V
+// (including the tile's V columns held in registers) fits in 128 registers,
+// so 15 consumer warps + the producer fill 16 warps per SM; larger groups
+// need up to 168 registers: 11 + 1.
 __host__ __device__ constexpr int consumer_warps(int G, int KV)
 {
-    return ((KV == PKV_BF16 || KV == PKV_F16) && G <= 4) || (KV == PKV_I8 && G <= 2) ? 15 : 11;
+    return (KV != PKV_F32 && G <= 2) ? 15 : 11;
 }
 
 template <int KV>
@@ -218,20 +220,32 @@ __device__ __forceinline__ void load_q(QRegs<D, G, KV> &qr, const unsigned char 
         }
 }
 
-// part[ii*G + g] += q[g] . K[token t_ii] over this lane's chunks.
+// This lane's K chunks of a tile: chunk ds + DS*c of token tq + TQ*ii.
+template <int D, int G, int KV>
+__device__ __forceinline__ void load_k(uint4 (&kr)[Cfg<D, G, KV>::TPL][Cfg<D, G, KV>::CPL],
+                                       const unsigned char *sK, int tq, int ds)
+{
+    using C = Cfg<D, G, KV>;
+#pragma unroll
+    for (int ii = 0; ii < C::TPL; ++ii)
+#pragma unroll
+        for (int c = 0; c < C::CPL; ++c)
+            kr[ii][c] = *reinterpret_cast<const uint4 *>(sK + (tq + C::TQ * ii) * C::ROWB +
+                                                         (ds + C::DS * c) * 16);
+}
+
+// part[ii*G + g] += q[g] . K[token t_ii] over this lane's chunks (held in kr).
 template <int D, int G, int KV>
 __device__ __forceinline__ void qk_tile(float (&part)[Cfg<D, G, KV>::NP],
-                                        const QRegs<D, G, KV> &qr, const unsigned char *sK,
-                                        int tq, int ds)
+                                        const QRegs<D, G, KV> &qr,
+                                        const uint4 (&kr)[Cfg<D, G, KV>::TPL][Cfg<D, G, KV>::CPL])
 {
     using C = Cfg<D, G, KV>;
 #pragma unroll
     for (int ii = 0; ii < C::TPL; ++ii) {
-        const int t = tq + C::TQ * ii;
 #pragma unroll
         for (int c = 0; c < C::CPL; ++c) {
-            const int chunk = ds + C::DS * c;
-            const uint4 kw = *reinterpret_cast<const uint4 *>(sK + t * C::ROWB + chunk * 16);
+            const uint4 kw = kr[ii][c];
             if constexpr (KV == PKV_BF16) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
@@ -353,6 +367,63 @@ __device__ __forceinline__ void load_v(float (&v)[D / 32], const unsigned char *
             v[2] = i8_to_float<2>(b); v[3] = i8_to_float<3>(b);
         } else {
             const uint32_t b = (uint32_t)(*reinterpret_cast<const uint16_t *>(p)) ^ 0x8080u;
+            v[0] = i8_to_float<0>(b); v[1] = i8_to_float<1>(b);
+        }
+    }
+}
+
+// Raw bytes of the lane's VE elements of one V row, when they fit in 8 bytes
+// (every case but fp32 with d = 128): a warp copies its V columns of the
+// whole tile into registers and releases the stage before the arithmetic.
+template <int D, int KV>
+struct VRaw {
+    static constexpr int BYTES = (D / 32) * KvBytes<KV>::v;
+    static constexpr bool IN_REGS = BYTES <= 8;
+    using type = typename std::conditional<(BYTES <= 4), uint32_t, uint2>::type;
+};
+
+template <int D, int KV>
+__device__ __forceinline__ typename VRaw<D, KV>::type load_v_raw(const unsigned char *sV, int t,
+                                                                 int lane)
+{
+    constexpr int BYTES = VRaw<D, KV>::BYTES;
+    const unsigned char *p = sV + t * D * KvBytes<KV>::v + lane * BYTES;
+    if constexpr (BYTES == 8)
+        return *reinterpret_cast<const uint2 *>(p);
+    else if constexpr (BYTES == 4)
+        return *reinterpret_cast<const uint32_t *>(p);
+    else
+        return (uint32_t)(*reinterpret_cast<const uint16_t *>(p));
+}
+
+template <int D, int KV>
+__device__ __forceinline__ void unpack_v(float (&v)[D / 32], typename VRaw<D, KV>::type raw)
+{
+    constexpr int VE = D / 32;
+    if constexpr (KV == PKV_BF16) {
+        if constexpr (VE == 4) {
+            v[0] = bf16lo(raw.x); v[1] = bf16hi(raw.x); v[2] = bf16lo(raw.y); v[3] = bf16hi(raw.y);
+        } else {
+            v[0] = bf16lo(raw); v[1] = bf16hi(raw);
+        }
+    } else if constexpr (KV == PKV_F16) {
+        if constexpr (VE == 4) {
+            const float2 a = half2_to_float2(raw.x), b = half2_to_float2(raw.y);
+            v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+        } else {
+            const float2 a = half2_to_float2(raw);
+            v[0] = a.x; v[1] = a.y;
+        }
+    } else if constexpr (KV == PKV_F32) {
+        static_assert(VE == 2, "fp32 rows of d = 128 are read from shared memory");
+        v[0] = __uint_as_float(raw.x); v[1] = __uint_as_float(raw.y);
+    } else {
+        if constexpr (VE == 4) {
+            const uint32_t b = raw ^ 0x80808080u;
+            v[0] = i8_to_float<0>(b); v[1] = i8_to_float<1>(b);
+            v[2] = i8_to_float<2>(b); v[3] = i8_to_float<3>(b);
+        } else {
+            const uint32_t b = raw ^ 0x8080u;
             v[0] = i8_to_float<0>(b); v[1] = i8_to_float<1>(b);
         }
     }
@@ -532,34 +603,34 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 st -= p.nst;
                 ++rnd;
             }
-            if (active) {
-                if (starts) {
-                    // q copies leave in piece order: the q ring has two slots and
-                    // a parity wait only tells one phase from the next, so copy
-                    // qn may wait for its slot only after copy qn - 1 has gone
-                    // (which itself waited for the slot's previous use).
-                    volatile int *qcount = misc + MISC_QCOUNT;
-                    const int slot = qn & 1;
-                    // A lane that gives up raises the abort flag before passing
-                    // its turn on, so later lanes issue nothing out of order.
-                    bool ok = count_wait_bounded(qcount, qn, abort_flag) && !*abort_flag;
-                    if (ok)
-                        ok = mbar_wait_bounded(&qempty[slot], ((qn >> 1) & 1) ^ 1, abort_flag);
-                    if (ok) {
+            {
+                // One convergent polling loop: each round every lane tests,
+                // without blocking, its q slot (if its tile starts a piece) and
+                // its stage, and issues the copies as soon as they are free; the
+                // warp leaves when all lanes are done.  (A blocking wait in a
+                // divergent lane would hold up lanes whose stages are already
+                // free.)  q copies leave in piece order: the q ring has two slots
+                // and a parity test only tells one phase from the next, so copy
+                // qn may test its slot only after copy qn - 1 has gone.
+                volatile int *qcount = misc + MISC_QCOUNT;
+                const int slot = qn & 1;
+                bool q_done = !starts;
+                bool t_done = !active;
+                uint64_t t0 = 0;
+                for (uint32_t it = 0;; ++it) {
+                    if (!q_done && *qcount == qn &&
+                        mbar_test_wait(&qempty[slot], ((qn >> 1) & 1) ^ 1)) {
                         const uint32_t qbytes = (uint32_t)(G * D * p.q_bytes);
                         mbar_arrive_expect_tx(&qfull[slot], qbytes);
                         const unsigned char *qsrc = static_cast<const unsigned char *>(p.q) +
                                                     ((int64_t)cur.b * Hq + cur.kvh * G) * D * p.q_bytes;
                         bulk_g2s(qring + slot * C::QSLOT, qsrc, qbytes, &qfull[slot]);
                         atomicMax(&misc[MISC_QISSUED + slot], (qn >> 1) + 1);
-                    } else if (!*abort_flag) {
-                        *abort_flag = 1;
-                        atomicOr(p.err, PKV_EBIT_TIMEOUT);
+                        __threadfence_block();
+                        *qcount = qn + 1;
+                        q_done = true;
                     }
-                    __threadfence_block();
-                    *qcount = qn + 1;
-                }
-                if (mbar_wait_bounded(&empty[st], (uint32_t)(rnd & 1) ^ 1u, abort_flag)) {
+                    if (!t_done && mbar_test_wait(&empty[st], (uint32_t)(rnd & 1) ^ 1u)) {
                     unsigned char *sK = stages + st * C::STAGE_BYTES;
                     unsigned char *sV = sK + C::KV_BYTES;
                     unsigned char *sKS = sV + C::KV_BYTES;
@@ -601,9 +672,29 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                             }
                         }
                     }
-                } else if (!*abort_flag) {
-                    *abort_flag = 1;
-                    atomicOr(p.err, PKV_EBIT_TIMEOUT);
+                        t_done = true;
+                    }
+                    if (__all_sync(FULL_MASK, q_done && t_done))
+                        break;
+                    if ((it & 63u) == 63u) {
+                        // bounded: give up after WAIT_LIMIT_NS (decided by lane 0
+                        // so that the whole warp leaves together)
+                        int stop = 0;
+                        if (lane == 0) {
+                            const uint64_t now = globaltimer_ns();
+                            if (it == 63u)
+                                t0 = now;
+                            else if (now - t0 > WAIT_LIMIT_NS || *abort_flag)
+                                stop = 1;
+                        }
+                        if (__shfl_sync(FULL_MASK, stop, 0)) {
+                            if (lane == 0 && !*abort_flag) {
+                                *abort_flag = 1;
+                                atomicOr(p.err, PKV_EBIT_TIMEOUT);
+                            }
+                            break;
+                        }
+                    }
                 }
             }
             __syncwarp();
@@ -699,21 +790,44 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 const unsigned char *sV = sK + C::KV_BYTES;
                 const __half *sKS = reinterpret_cast<const __half *>(sV + C::KV_BYTES);
                 const __half *sVS = sKS + TILE;
+                // After the reduction below the lane holds token t, heads g0 + r.
+                const int t = tq + C::TQ * (ds >> 1);
+                const int g0 = G >= 2 ? (G / 2) * (ds & 1) : 0;
+
+                // ---- take this lane's part of the tile into registers and hand
+                // the stage back at once, so that the next copy into it starts
+                // while this warp computes
+                uint4 kr[C::TPL][C::CPL];
+                load_k<D, G, KV>(kr, sK, tq, ds);
+                float ks_t = 1.0f, vs_t = 1.0f;
+                if constexpr (KV == PKV_I8) {
+                    ks_t = __half2float(sKS[t]);
+                    vs_t = __half2float(sVS[t]);
+                }
+                // (with G = 8 the heads' accumulators need the registers; V is
+                // then read from the stage, which is released after P.V)
+                constexpr bool VREG = VRaw<D, KV>::IN_REGS && G <= 4;
+                typename VRaw<D, KV>::type vr[TILE];
+                if constexpr (VREG) {
+#pragma unroll
+                    for (int tt = 0; tt < TILE; ++tt)
+                        vr[tt] = load_v_raw<D, KV>(sV, tt, lane);
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&empty[st]);
+                }
 
                 // ---- scores: partial dots, then reduce-scatter over the DS lanes
                 float part[C::NP];
 #pragma unroll
                 for (int j = 0; j < C::NP; ++j)
                     part[j] = 0.0f;
-                qk_tile<D, G, KV>(part, qr, sK, tq, ds);
+                qk_tile<D, G, KV>(part, qr, kr);
                 reduce_scatter<C::NP, C::DS / 2>(part, ds);
-                // Lane holds token t, heads g0 + r (r < NF).
-                const int t = tq + C::TQ * (ds >> 1);
-                const int g0 = G >= 2 ? (G / 2) * (ds & 1) : 0;
                 float s[C::NF];
                 float kscale = p.scale_log2;
                 if constexpr (KV == PKV_I8)
-                    kscale *= __half2float(sKS[t]);
+                    kscale *= ks_t;
                 bool above = false;
 #pragma unroll
                 for (int r = 0; r < C::NF; ++r) {
@@ -748,9 +862,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 // Publish {p, p} pairs (p times the V scale for int8) and, when
                 // the maximum moved, the rescale factors.
                 if (G >= 2 || (ds & 1) == 0) {
-                    float vsc = 1.0f;
-                    if constexpr (KV == PKV_I8)
-                        vsc = __half2float(sVS[t]);
+                    const float vsc = vs_t;
                     float2 *pp = reinterpret_cast<float2 *>(ps + t * 2 * G) + g0;
 #pragma unroll
                     for (int r = 0; r < C::NF; ++r) {
@@ -777,7 +889,10 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 }
                 auto pv_token = [&](int tt) {
                     float v[C::VE];
-                    load_v<D, KV>(v, sV, tt, lane);
+                    if constexpr (VREG)
+                        unpack_v<D, KV>(v, vr[tt]);
+                    else
+                        load_v<D, KV>(v, sV, tt, lane);
                     const float *pt = ps + tt * 2 * G;
                     if constexpr (G == 1) {
                         const float2 w2 = *reinterpret_cast<const float2 *>(pt);
@@ -801,12 +916,16 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     for (int tt = 0; tt < TILE; ++tt)
                         pv_token(tt);
                 } else {
-                    for (int tt = 0; tt < nvalid; ++tt)
-                        pv_token(tt);
+#pragma unroll
+                    for (int tt = 0; tt < TILE; ++tt)
+                        if (tt < nvalid)
+                            pv_token(tt);
                 }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&empty[st]);
+                if constexpr (!VREG) {
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&empty[st]);
+                }
                 st += W;
                 while (st >= p.nst) {
                     st -= p.nst;
