@@ -48,8 +48,8 @@ using namespace dev;
 
 constexpr int TILE = 16;        // tokens per pipeline stage
 constexpr int MAX_STAGES = 32;
-// misc ints in shared memory: [0] abort flag, [1] "merge partials" flag,
-// [2] a constant zero, [8..8+warps) scan scratch, [32..32+MAX_STAGES) last
+// misc ints in shared memory: [0] abort flag, [2] a constant zero, [4..6)
+// "merge the partials of the first / last piece" flags, [8..8+warps) scan scratch, [32..32+MAX_STAGES) last
 // issued round per stage (+1; 0 = never), [64..66) q copies issued per slot,
 // [66] number of q copies issued so far (they go out in piece order).
 constexpr int MISC_INTS = 72;
@@ -469,7 +469,8 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     uint64_t *qempty = qfull + 2;
     int *misc = reinterpret_cast<int *>(smem + lay.misc);
     volatile int *abort_flag = misc + 0;  // set on any timeout
-    // misc[1]: "this CTA merges the partials"; misc[2]: zero word; misc[8..]: scan scratch
+    // misc[2]: zero word; misc[4..6): "this CTA merges the partials of its
+    // first / last piece"; misc[8..]: scan scratch
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -723,6 +724,50 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     p.out[(int64_t)b * Hq * D + idx] = 0.0f;
         }
 
+        const int stride = G * (D + 2);   // floats of one partial
+        // Tiles [seg_begin, seg_end) of a (sequence, KV head) and the CTAs
+        // that own its first and last tile.
+        struct SegSpan { int c_first, c_last; };
+        auto seg_span = [&](int seg) {
+            const int bq = seg / Hkv, kq = seg - (seg / Hkv) * Hkv;
+            const int nt = (s_tstart[bq + 1] - s_tstart[bq]) / Hkv;
+            const int64_t sb = (int64_t)s_tstart[bq] + (int64_t)kq * nt;
+            return SegSpan{owner_of(sb, T, P), owner_of(sb + nt - 1, T, P)};
+        };
+        // Fold the stored partials of CTAs [c0, c1] (skipping CTA `skip`)
+        // of piece `seg` into the running (m, num, den) of output idx.
+        auto fold_partials = [&](int seg, int c0, int c1, int skip, int idx, float &m,
+                                 float &num, float &den) {
+            const int g = idx / D;
+            const float *base = p.partials + (int64_t)seg * stride;
+#pragma unroll 4
+            for (int pc = c0; pc <= c1; ++pc) {
+                if (pc == skip)
+                    continue;
+                const float *part = base + (int64_t)pc * stride;
+                const float mp = __ldcg(part + G * D + g);
+                const float np = __ldcg(part + idx);
+                const float lp = __ldcg(part + G * D + G + g);
+                const float mn = fmaxf(m, mp);
+                const float fo = exp2_approx(m - mn), fp = exp2_approx(mp - mn);
+                num = fmaf(num, fo, np * fp);
+                den = fmaf(den, fo, lp * fp);
+                m = mn;
+            }
+        };
+        // Merge every partial of piece `seg` (this CTA was the last to
+        // publish one) and write the output rows; reset the piece's counter.
+        auto final_merge = [&](int seg) {
+            const SegSpan sp = seg_span(seg);
+            const int bq = seg / Hkv, kq = seg - (seg / Hkv) * Hkv;
+            for (int idx = ctid; idx < G * D; idx += W * 32) {
+                float m = -INFINITY, num = 0.0f, den = 0.0f;
+                fold_partials(seg, sp.c_first, sp.c_last, -1, idx, m, num, den);
+                p.out[((int64_t)bq * Hq + kq * G) * D + idx] = num / den;
+            }
+            if (ctid == 0)
+                p.counters[seg] = 0;
+        };
         int qn = 0;
         int64_t x = R0;
         while (x < R1) {
@@ -957,64 +1002,112 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             const int c_first = owner_of(seg_begin, T, P);
             const int c_last = owner_of(seg_end - 1, T, P);
             const bool whole = c_first == c_last;
+            const bool last_piece = xe == R1;
             const int seg = b * Hkv + kvh;
-            const int stride = G * (D + 2);
-            float *part_out = p.partials + (int64_t)(cta + seg) * stride;
-            for (int idx = ctid; idx < G * D; idx += W * 32) {
-                const int g = idx / D;
-                float M = -INFINITY;
+            // The CTA's last piece, if split: look (without waiting) whether
+            // every other CTA holding a part of it has already published;
+            // then this CTA merges at once instead of publishing its own.
+            int published = -1;
+            if (!whole && last_piece && ctid == 0)
+                published = ld_relaxed_gpu(p.counters + seg);
+            // Merge the W warp states of each output this thread owns.
+            constexpr int MO = (G * D + W * 32 - 1) / (W * 32);
+            float o_m[MO], o_num[MO], o_den[MO];
 #pragma unroll
-                for (int ww = 0; ww < W; ++ww)
-                    M = fmaxf(M, merge[ww * stride + G * D + g]);
-                float num = 0.0f, den = 0.0f;
+            for (int j = 0; j < MO; ++j) {
+                const int idx = ctid + j * W * 32;
+                o_m[j] = -INFINITY;
+                o_num[j] = 0.0f;
+                o_den[j] = 0.0f;
+                if (idx < G * D) {
+                    const int g = idx / D;
+                    float M = -INFINITY;
 #pragma unroll
-                for (int ww = 0; ww < W; ++ww) {
-                    const float f = exp2f(merge[ww * stride + G * D + g] - M);
-                    num = fmaf(f, merge[ww * stride + idx], num);
-                    den = fmaf(f, merge[ww * stride + G * D + G + g], den);
-                }
-                if (whole) {
-                    p.out[((int64_t)b * Hq + kvh * G) * D + idx] = num / den;
-                } else {
-                    part_out[idx] = num;
-                    if ((idx % D) == 0) {
-                        part_out[G * D + g] = M;
-                        part_out[G * D + G + g] = den;
+                    for (int ww = 0; ww < W; ++ww)
+                        M = fmaxf(M, merge[ww * stride + G * D + g]);
+                    float num = 0.0f, den = 0.0f;
+#pragma unroll
+                    for (int ww = 0; ww < W; ++ww) {
+                        const float f = exp2_approx(merge[ww * stride + G * D + g] - M);
+                        num = fmaf(f, merge[ww * stride + idx], num);
+                        den = fmaf(f, merge[ww * stride + G * D + G + g], den);
                     }
+                    o_m[j] = M;
+                    o_num[j] = num;
+                    o_den[j] = den;
                 }
             }
-            if (!whole) {
-                __threadfence();
-                named_bar_sync(1, W * 32);
-                if (ctid == 0) {
-                    const int old = atomicAdd(p.counters + seg, 1);
-                    misc[1] = (old == c_last - c_first) ? 1 : 0;
+            float *orow = p.out + ((int64_t)b * Hq + kvh * G) * D;
+            if (whole) {
+#pragma unroll
+                for (int j = 0; j < MO; ++j) {
+                    const int idx = ctid + j * W * 32;
+                    if (idx < G * D)
+                        orow[idx] = o_num[j] / o_den[j];
                 }
-                named_bar_sync(1, W * 32);
-                if (misc[1]) {
-                    __threadfence();
-                    const float *base = p.partials + (int64_t)(c_first + seg) * stride;
-                    const int npieces = c_last - c_first + 1;
-                    for (int idx = ctid; idx < G * D; idx += W * 32) {
-                        const int g = idx / D;
-                        float M = -INFINITY;
-                        for (int pc = 0; pc < npieces; ++pc)
-                            M = fmaxf(M, __ldcg(base + pc * stride + G * D + g));
-                        float num = 0.0f, den = 0.0f;
-                        for (int pc = 0; pc < npieces; ++pc) {
-                            const float f = exp2f(__ldcg(base + pc * stride + G * D + g) - M);
-                            num = fmaf(f, __ldcg(base + pc * stride + idx), num);
-                            den = fmaf(f, __ldcg(base + pc * stride + G * D + G + g), den);
+                named_bar_sync(1, W * 32);   // the merge buffer is free again
+            } else {
+                int merge_now = 0;
+                if (last_piece) {
+                    if (ctid == 0) {
+                        merge_now = published == c_last - c_first;
+                        if (merge_now)
+                            __threadfence();   // acquire: their partials are visible
+                        misc[4] = merge_now;
+                    }
+                    named_bar_sync(1, W * 32);
+                    merge_now = misc[4];
+                }
+                if (merge_now) {
+#pragma unroll
+                    for (int j = 0; j < MO; ++j) {
+                        const int idx = ctid + j * W * 32;
+                        if (idx < G * D) {
+                            fold_partials(seg, c_first, c_last, cta, idx, o_m[j], o_num[j],
+                                          o_den[j]);
+                            orow[idx] = o_num[j] / o_den[j];
                         }
-                        p.out[((int64_t)b * Hq + kvh * G) * D + idx] = num / den;
                     }
                     if (ctid == 0)
                         p.counters[seg] = 0;
+                } else {
+                    float *part_out = p.partials + (int64_t)(cta + seg) * stride;
+#pragma unroll
+                    for (int j = 0; j < MO; ++j) {
+                        const int idx = ctid + j * W * 32;
+                        if (idx < G * D) {
+                            part_out[idx] = o_num[j];
+                            if ((idx % D) == 0) {
+                                part_out[G * D + idx / D] = o_m[j];
+                                part_out[G * D + G + idx / D] = o_den[j];
+                            }
+                        }
+                    }
+                    // Publish: one thread fences for the CTA after the barrier
+                    // (which orders every thread's partial stores before it),
+                    // then counts this CTA in.  Mid-stream only that thread's
+                    // warp waits for the round trip; a CTA that turns out to
+                    // be the last one merges at its end.
+                    named_bar_sync(1, W * 32);
+                    if (ctid == 0) {
+                        __threadfence();
+                        const int old = atomicAdd(p.counters + seg, 1);
+                        if (old == c_last - c_first) {
+                            __threadfence();
+                            misc[last_piece ? 5 : 6] = seg + 1;
+                        }
+                    }
                 }
             }
-            named_bar_sync(1, W * 32);
             x = xe;
         }
+
+        // Pieces whose partials this CTA was the last to publish.
+        named_bar_sync(1, W * 32);
+        if (misc[6])
+            final_merge(misc[6] - 1);
+        if (misc[5])
+            final_merge(misc[5] - 1);
     }
 
     // Let every copy this CTA issued land before the CTA exits (only matters

@@ -120,6 +120,14 @@ __device__ __forceinline__ bool count_wait_bounded(volatile int *c, int target,
     }
 }
 
+// Relaxed load at GPU scope (no ordering; pair with a fence to acquire).
+__device__ __forceinline__ int ld_relaxed_gpu(const int *ptr)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 // Bulk (non-tensor) async copy global -> this CTA's shared memory; completion
 // is counted in bytes on the mbarrier.  dst, src 16-byte aligned; bytes a
 // multiple of 16.
