@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) append_copy_kernel(
     int num_kv_heads, int block_size, int64_t num_slots, uint4 *__restrict__ k_cache,
     uint4 *__restrict__ v_cache, unsigned int *__restrict__ err)
 {
+    grid_dependency_wait();
+    grid_dependents_launch();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < total_chunks;
          c += stride) {
@@ -69,6 +71,8 @@ __global__ void __launch_bounds__(256) append_q8_kernel(
     __half *__restrict__ k_scales, __half *__restrict__ v_scales, unsigned int *__restrict__ err)
 {
     constexpr int D = 32 * E;
+    grid_dependency_wait();
+    grid_dependents_launch();
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -148,10 +152,11 @@ int launch_append(const pkv_pool *pool, const void *k_new, const void *v_new, pk
         const int chunks_per_row = D * dtype_bytes(pool->kv_dtype) / 16;
         const int64_t total = (int64_t)num_tokens * H * chunks_per_row;
         const int threads = 256;
-        append_copy_kernel<<<grid_for(total, threads, pool->num_sms), threads, 0, s>>>(
-            static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
-            total, chunks_per_row, H, bs, num_slots, static_cast<uint4 *>(k_cache),
-            static_cast<uint4 *>(v_cache), pool->d_err);
+        launch_pdl(append_copy_kernel, dim3(grid_for(total, threads, pool->num_sms)),
+                   dim3(threads), 0, s, static_cast<const uint4 *>(k_new),
+                   static_cast<const uint4 *>(v_new), slot_mapping, total, chunks_per_row, H, bs,
+                   num_slots, static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+                   pool->d_err);
     } else {
         const int64_t rows = (int64_t)num_tokens * H;
         const int threads = 256;
@@ -161,10 +166,9 @@ int launch_append(const pkv_pool *pool, const void *k_new, const void *v_new, pk
         __half *ks = static_cast<__half *>(k_scales);
         __half *vs = static_cast<__half *>(v_scales);
 #define PKV_Q8(T, E)                                                                        \
-    append_q8_kernel<T, E><<<grid, threads, 0, s>>>(static_cast<const T *>(k_new),          \
-                                                    static_cast<const T *>(v_new),          \
-                                                    slot_mapping, rows, H, bs, num_slots, kc, \
-                                                    vc, ks, vs, pool->d_err)
+    launch_pdl(append_q8_kernel<T, E>, dim3(grid), dim3(threads), 0, s,                      \
+               static_cast<const T *>(k_new), static_cast<const T *>(v_new), slot_mapping,   \
+               rows, H, bs, num_slots, kc, vc, ks, vs, pool->d_err)
         if (D == 128) {
             if (in_dtype == PKV_F16) PKV_Q8(__half, 4);
             else if (in_dtype == PKV_BF16) PKV_Q8(__nv_bfloat16, 4);

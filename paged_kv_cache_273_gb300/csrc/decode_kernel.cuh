@@ -492,6 +492,11 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         mbar_fence_init();
     }
 
+    // Everything above touched shared memory only; global inputs may come
+    // from the previous kernel in the stream.
+    grid_dependency_wait();
+    grid_dependents_launch();
+
     // Sequence lengths (validated) and the exclusive prefix of tiles.
     for (int b = tid; b < B; b += NTHREADS) {
         int L = __ldg(p.seq_lens + b);
@@ -1160,7 +1165,9 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
         P = max_tiles;
     if (P < 1)
         P = 1;
-    paged_decode_kernel<D, G, KV><<<(int)P, C::NTHREADS, lay.total, stream>>>(prm);
+    if (launch_pdl(paged_decode_kernel<D, G, KV>, dim3((unsigned)P), dim3(C::NTHREADS),
+                   (size_t)lay.total, stream, prm) != cudaSuccess)
+        return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

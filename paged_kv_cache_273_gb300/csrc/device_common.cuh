@@ -4,7 +4,9 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 #include "pkv_internal.h"
 
@@ -118,6 +120,43 @@ __device__ __forceinline__ bool count_wait_bounded(volatile int *c, int target,
                 return false;
         }
     }
+}
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel of its stream is still
+// running; grid_dependency_wait() blocks until that kernel has completed and
+// its memory is visible, so it must come before the first global access.
+// grid_dependents_launch() lets the next such kernel start early (it still
+// waits for this one to finish before touching memory).  Both are no-ops for
+// a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Host: launch kernel<<<grid, block, smem, stream>>>(args...) with
+// programmatic stream serialization allowed, so that its launch and prologue
+// overlap the tail of the previous kernel in the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Relaxed load at GPU scope (no ordering; pair with a fence to acquire).
