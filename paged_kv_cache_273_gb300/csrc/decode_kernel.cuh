@@ -739,20 +739,24 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             const int64_t sb = (int64_t)s_tstart[bq] + (int64_t)kq * nt;
             return SegSpan{owner_of(sb, T, P), owner_of(sb + nt - 1, T, P)};
         };
-        // Fold the stored partials of CTAs [c0, c1] (skipping CTA `skip`)
-        // of piece `seg` into the running (m, num, den) of output idx.
-        auto fold_partials = [&](int seg, int c0, int c1, int skip, int idx, float &m,
-                                 float &num, float &den) {
+        // Merge the partials of CTAs c0..c1 of piece `seg`, in CTA order, for
+        // output idx; CTA `own` (if any) contributes (own_m, own_num, own_den)
+        // from registers instead of its stored partial.  The order, and so the
+        // rounding, is the same whichever CTA merges.
+        auto fold_partials = [&](int seg, int c0, int c1, int own, float own_m, float own_num,
+                                 float own_den, int idx, float &m, float &num, float &den) {
             const int g = idx / D;
             const float *base = p.partials + (int64_t)seg * stride;
+            m = -INFINITY;
+            num = 0.0f;
+            den = 0.0f;
 #pragma unroll 4
             for (int pc = c0; pc <= c1; ++pc) {
-                if (pc == skip)
-                    continue;
                 const float *part = base + (int64_t)pc * stride;
-                const float mp = __ldcg(part + G * D + g);
-                const float np = __ldcg(part + idx);
-                const float lp = __ldcg(part + G * D + G + g);
+                const bool mine = pc == own;
+                const float mp = mine ? own_m : __ldcg(part + G * D + g);
+                const float np = mine ? own_num : __ldcg(part + idx);
+                const float lp = mine ? own_den : __ldcg(part + G * D + G + g);
                 const float mn = fmaxf(m, mp);
                 const float fo = exp2_approx(m - mn), fp = exp2_approx(mp - mn);
                 num = fmaf(num, fo, np * fp);
@@ -766,8 +770,8 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             const SegSpan sp = seg_span(seg);
             const int bq = seg / Hkv, kq = seg - (seg / Hkv) * Hkv;
             for (int idx = ctid; idx < G * D; idx += W * 32) {
-                float m = -INFINITY, num = 0.0f, den = 0.0f;
-                fold_partials(seg, sp.c_first, sp.c_last, -1, idx, m, num, den);
+                float m, num, den;
+                fold_partials(seg, sp.c_first, sp.c_last, -1, 0.0f, 0.0f, 0.0f, idx, m, num, den);
                 p.out[((int64_t)bq * Hq + kq * G) * D + idx] = num / den;
             }
             if (ctid == 0)
@@ -1068,9 +1072,10 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     for (int j = 0; j < MO; ++j) {
                         const int idx = ctid + j * W * 32;
                         if (idx < G * D) {
-                            fold_partials(seg, c_first, c_last, cta, idx, o_m[j], o_num[j],
-                                          o_den[j]);
-                            orow[idx] = o_num[j] / o_den[j];
+                            float m, num, den;
+                            fold_partials(seg, c_first, c_last, cta, o_m[j], o_num[j], o_den[j],
+                                          idx, m, num, den);
+                            orow[idx] = num / den;
                         }
                     }
                     if (ctid == 0)
