@@ -354,6 +354,29 @@ def run_gpu(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_val = e2e_bytes * world / float(tt.item()) / 1e9
 
+    # ---- copy-on-write block copy (kv_block_copy) on a pool of the same shape:
+    # 4096 block pairs per launch, 268 MB read + 268 MB written (twice L2)
+    cow_blocks = 8192
+    cow_pool = pkv.kv_block_pool_init(cow_blocks, bs, Hkv, D, wl.kv_dtype)
+    ck, cv, _, _ = cow_pool.alloc_cache(dev)
+    perm = np.random.default_rng(5).permutation(cow_blocks).astype(np.int32)
+    c_src = torch.from_numpy(perm[:cow_blocks // 2].copy()).to(dev)
+    c_dst = torch.from_numpy(perm[cow_blocks // 2:].copy()).to(dev)
+    cow_bytes = (cow_blocks // 2) * Hkv * bs * D * eb(wl.kv_dtype) * 2 * 2   # K+V, read+write
+    for _ in range(3):
+        pkv.kv_block_copy(cow_pool, c_src, c_dst, ck, cv, stream=stream)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cow_reps = 50
+    c0.record(stream)
+    for _ in range(cow_reps):
+        pkv.kv_block_copy(cow_pool, c_src, c_dst, ck, cv, stream=stream)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    cow_ms = c0.elapsed_time(c1) / cow_reps
+    if pkv.pkv_check_error(cow_pool) != pkv.PKV_OK:
+        raise RuntimeError("device error in the block-copy measurement")
+    del ck, cv
+
     # ---- peaks, traffic and the CPU baseline (rank 0)
     peaks = {}
     try:
@@ -403,6 +426,13 @@ def run_gpu(args):
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": 2 * args.steps,
+            "extra_kernels": {
+                "kv_block_copy": {"value": cow_bytes / (cow_ms / 1e3) / 1e9, "unit": "GB/s",
+                                  "frac": cow_bytes / (cow_ms / 1e3) / 1e9 / peak,
+                                  "launch_us": cow_ms * 1e3, "bytes_per_launch": cow_bytes,
+                                  "pairs": cow_blocks // 2,
+                                  "note": "copy-on-write block copy, bf16 blocks of the "
+                                          "same shape, read + write bytes"}},
             "clocks": clk,
         }
         print(json.dumps(line))

@@ -164,6 +164,31 @@ int kv_reserve_slots(pkv_pool *pool, int batch, const int32_t *seq_lens, const i
                      int32_t *block_tables, int max_blocks_per_seq, int32_t *slot_mapping);
 
 /*
+ * kv_reserve_slots_cow — kv_reserve_slots for tables that may point at shared
+ * blocks.  [VIS] "PagedAttention: the cache in blocks": requests with the same
+ * prefix point at the same blocks, and a block is copied only when one of
+ * them writes to it.  The only existing block an append step writes into is a
+ * sequence's last, partly filled one (at position seq_lens[b] when
+ * seq_lens[b] % bs != 0 and num_new[b] > 0); if its reference count is above
+ * one, the sequence gets a private copy first: a fresh block is allocated,
+ * the pair (old id, new id) is written to copy_src[i], copy_dst[i], one
+ * reference of the old block is dropped and the table entry is replaced.
+ * Sequences are handled in order, so when every holder of a shared block
+ * appends in one step, all but the last one to be handled get copies and
+ * that last one writes in place.  At most `batch` pairs; *num_copies
+ * receives their number.  The caller must run kv_block_copy on the pairs
+ * before the kv_append of this step.  Slots and new blocks are then handled
+ * as in kv_reserve_slots.
+ * All-or-nothing: PKV_ERR_NO_BLOCKS if the pool cannot cover the new blocks
+ * and the copies; PKV_ERR_INVALID for a table row that would overflow or a
+ * written entry that is out of range or free.
+ */
+int kv_reserve_slots_cow(pkv_pool *pool, int batch, const int32_t *seq_lens,
+                         const int32_t *num_new, int32_t *block_tables, int max_blocks_per_seq,
+                         int32_t *slot_mapping, int32_t *copy_src, int32_t *copy_dst,
+                         int *num_copies);
+
+/*
  * kv_slot_mapping — pure host computation of slots from existing block
  * tables: token j of sequence b sits at position start[b] + j, in logical
  * block p / bs at offset p % bs, so its slot is
@@ -202,6 +227,25 @@ int kv_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq, int blo
 int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
               const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,
               void *k_scales, void *v_scales, pkv_stream_t stream);
+
+/*
+ * kv_block_copy — the copy half of copy-on-write ([VIS] "PagedAttention: the
+ * cache in blocks"): for i < n, every cached K and V row of block src[i] (all
+ * KV heads; and the fp16 scales for int8 pools) is copied bit for bit to
+ * block dst[i].
+ *
+ *   src, dst   device int32 [n] block ids (as kv_reserve_slots_cow writes
+ *              them).  The dst blocks must be distinct and none may be a src
+ *              block of the same call (overlapping pairs give an undefined
+ *              result).
+ *   k_cache, v_cache, k_scales, v_scales  as for kv_append.
+ *
+ * An id outside [0, NB) sets PKV_ERR_BAD_INDEX in the error word and that
+ * pair is skipped.  n == 0 is a no-op.
+ */
+int kv_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, int n,
+                  void *k_cache, void *v_cache, void *k_scales, void *v_scales,
+                  pkv_stream_t stream);
 
 /*
  * paged_decode_workspace_bytes — size of the scratch buffer that

@@ -198,6 +198,31 @@ void orc_append(const void *k_new, const void *v_new, int dtype, const int32_t *
 }
 
 /* ------------------------------------------------------------------ */
+/* Copy-on-write: [VIS] "PagedAttention: the cache in blocks".  Requests */
+/* with the same prefix point at the same blocks, and a block is copied  */
+/* only when one of them writes to it; the writer then holds a private   */
+/* block with the same rows.  So every element (head, offset, i) of      */
+/* block src[j] is copied to the same place in block dst[j].  One call   */
+/* handles one array: a K or V cache (row = head_dim elements), or the   */
+/* int8 scales (row = 1 element of 2 bytes).                             */
+/* ------------------------------------------------------------------ */
+void orc_block_copy(void *cache, int elem_size, int num_kv_heads, int block_size, int row_len,
+                    const int32_t *src, const int32_t *dst, int n)
+{
+    for (int j = 0; j < n; ++j)
+        for (int h = 0; h < num_kv_heads; ++h)
+            for (int off = 0; off < block_size; ++off)
+                for (int i = 0; i < row_len; ++i) {
+                    int64_t from = cache_index((int64_t)src[j] * block_size + off, h, i,
+                                               block_size, num_kv_heads, row_len);
+                    int64_t to = cache_index((int64_t)dst[j] * block_size + off, h, i,
+                                             block_size, num_kv_heads, row_len);
+                    memcpy((char *)cache + to * elem_size, (const char *)cache + from * elem_size,
+                           (size_t)elem_size);
+                }
+}
+
+/* ------------------------------------------------------------------ */
 /* int8 quantization of one (token, head) row.                          */
 /* [NOTES] "How serving systems tame the cost", "Quantized KV cache":   */
 /* store cached K and V at lower precision, e.g. FP16 to INT8.  The      */

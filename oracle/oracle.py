@@ -65,6 +65,8 @@ def _load():
         lib.orc_slot_mapping.restype = None
         lib.orc_append.argtypes = [P, P, I, P, I, I, I, I, P, P]
         lib.orc_append.restype = None
+        lib.orc_block_copy.argtypes = [P, I, I, I, I, P, P, I]
+        lib.orc_block_copy.restype = None
         lib.orc_quantize_row_q8.argtypes = [P, I, P, P]
         lib.orc_quantize_row_q8.restype = None
         lib.orc_append_q8.argtypes = [P, P, I, P, I, I, I, I, P, P, P, P]
@@ -150,6 +152,22 @@ def append(k_new, v_new, dtype, slots, block_size, k_cache, v_cache):
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
     _load().orc_append(_ptr(k_new), _ptr(v_new), dtype, _ptr(slots), T, H, D, block_size,
                        _ptr(k_cache), _ptr(v_cache))
+
+
+def block_copy(src, dst, block_size, k_cache, v_cache, k_scales=None, v_scales=None):
+    """Copy-on-write copy of blocks src[j] -> dst[j] in numpy caches (in place)."""
+    src = _c(src, np.int32)
+    dst = _c(dst, np.int32)
+    NB, H, bs, D = k_cache.shape
+    assert bs == block_size
+    for a in (k_cache, v_cache):
+        assert a.flags.c_contiguous
+        _load().orc_block_copy(_ptr(a), a.dtype.itemsize, H, bs, D, _ptr(src), _ptr(dst), src.size)
+    for a in (k_scales, v_scales):
+        if a is not None:
+            assert a.flags.c_contiguous and a.shape == (NB, H, bs)
+            _load().orc_block_copy(_ptr(a), a.dtype.itemsize, H, bs, 1, _ptr(src), _ptr(dst),
+                                   src.size)
 
 
 def quantize_row_q8(x):

@@ -8,6 +8,10 @@
 // fp caches: a bit copy, 16 bytes per thread.  int8 caches ("Quantized KV
 // cache" on the same page): one warp per (token, head, K-or-V) row computes the
 // row's absolute maximum, an fp16 scale amax/127 and round-half-even codes.
+//
+// kv_block_copy: the copy half of copy-on-write (KV cache visualization page,
+// "PagedAttention: the cache in blocks": a shared block is copied only when a
+// request writes to it), a bit copy of whole blocks.
 
 #include <cuda_runtime.h>
 
@@ -128,6 +132,44 @@ __global__ void __launch_bounds__(256) append_q8_kernel(
     }
 }
 
+// Copy whole blocks (copy-on-write): K and V of block src[i] -> dst[i], one
+// thread per 16-byte chunk; a block-head tile row is a multiple of 16 bytes.
+// int8 scales ([NB][Hkv][bs] fp16) follow as 2-byte elements.
+__global__ void __launch_bounds__(256) block_copy_kernel(
+    const int32_t *__restrict__ src, const int32_t *__restrict__ dst, int n,
+    int64_t chunks_per_block, int64_t scales_per_block, int num_blocks,
+    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, __half *__restrict__ k_scales,
+    __half *__restrict__ v_scales, unsigned int *__restrict__ err)
+{
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t per_pair = 2 * chunks_per_block + 2 * scales_per_block;
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < (int64_t)n * per_pair;
+         c += stride) {
+        const int i = (int)(c / per_pair);
+        int64_t r = c - (int64_t)i * per_pair;
+        const int32_t s = __ldg(src + i), d = __ldg(dst + i);
+        if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+            if (r == 0)
+                atomicOr(err, PKV_EBIT_BLOCK);
+            continue;
+        }
+        if (r < 2 * chunks_per_block) {
+            uint4 *cache = r < chunks_per_block ? k_cache : v_cache;
+            if (r >= chunks_per_block)
+                r -= chunks_per_block;
+            cache[(int64_t)d * chunks_per_block + r] = cache[(int64_t)s * chunks_per_block + r];
+        } else {
+            r -= 2 * chunks_per_block;
+            __half *sc = r < scales_per_block ? k_scales : v_scales;
+            if (r >= scales_per_block)
+                r -= scales_per_block;
+            sc[(int64_t)d * scales_per_block + r] = sc[(int64_t)s * scales_per_block + r];
+        }
+    }
+}
+
 int grid_for(int64_t work_items, int threads, int num_sms)
 {
     int64_t blocks = (work_items + threads - 1) / threads;
@@ -140,6 +182,23 @@ int grid_for(int64_t work_items, int threads, int num_sms)
 }
 
 }  // namespace
+
+int launch_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, int n,
+                      void *k_cache, void *v_cache, void *k_scales, void *v_scales,
+                      pkv_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t rows = (int64_t)pool->num_kv_heads * pool->block_size;
+    const int64_t chunks = rows * pool->head_dim * dtype_bytes(pool->kv_dtype) / 16;
+    const int64_t scales = pool->kv_dtype == PKV_I8 ? rows : 0;
+    const int threads = 256;
+    const int64_t total = (int64_t)n * (2 * chunks + 2 * scales);
+    launch_pdl(block_copy_kernel, dim3(grid_for(total, threads, pool->num_sms)), dim3(threads), 0,
+               s, src, dst, n, chunks, scales, pool->num_blocks, static_cast<uint4 *>(k_cache),
+               static_cast<uint4 *>(v_cache), static_cast<__half *>(k_scales),
+               static_cast<__half *>(v_scales), pool->d_err);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 int launch_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
                   const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,

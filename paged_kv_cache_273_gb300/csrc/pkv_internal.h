@@ -11,7 +11,7 @@
 // Bits of the device error word.
 enum : unsigned int {
     PKV_EBIT_SLOT = 1u,      // kv_append: slot outside [0, NB*bs)
-    PKV_EBIT_BLOCK = 2u,     // attention: block id outside [0, NB)
+    PKV_EBIT_BLOCK = 2u,     // attention, block copy: block id outside [0, NB)
     PKV_EBIT_SEQLEN = 4u,    // attention: seq_len < 0 or beyond its block table row
     PKV_EBIT_TIMEOUT = 8u,   // a bounded mbarrier wait gave up
 };
@@ -49,6 +49,9 @@ inline int dtype_bytes(pkv_dtype t)
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launchers (defined in the .cu files).  They assume validated arguments.
+int launch_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, int n,
+                      void *k_cache, void *v_cache, void *k_scales, void *v_scales,
+                      pkv_stream_t stream);
 int launch_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
                   const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,
                   void *k_scales, void *v_scales, pkv_stream_t stream);

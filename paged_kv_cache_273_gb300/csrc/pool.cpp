@@ -239,7 +239,99 @@ int kv_reserve_slots(pkv_pool *pool, int batch, const int32_t *seq_lens, const i
     return PKV_OK;
 }
 
+int kv_reserve_slots_cow(pkv_pool *pool, int batch, const int32_t *seq_lens,
+                         const int32_t *num_new, int32_t *block_tables, int max_blocks_per_seq,
+                         int32_t *slot_mapping, int32_t *copy_src, int32_t *copy_dst,
+                         int *num_copies)
+{
+    if (!pool || batch < 0 || max_blocks_per_seq < 0 || !num_copies ||
+        (batch > 0 && (!seq_lens || !block_tables || !copy_src || !copy_dst)))
+        return PKV_ERR_INVALID;
+    const int bs = pool->block_size;
+    // First pass: validate and count the blocks the step needs, playing the
+    // reference drops of earlier copies forward so that the count is exact.
+    std::unordered_map<int32_t, int> dropped;
+    int64_t need = 0, total_new = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int n = num_new ? num_new[b] : 1;
+        if (seq_lens[b] < 0 || n < 0)
+            return PKV_ERR_INVALID;
+        const int64_t before = ceil_div(seq_lens[b], bs);
+        const int64_t after = ceil_div((int64_t)seq_lens[b] + n, bs);
+        if (after > max_blocks_per_seq)
+            return PKV_ERR_INVALID;
+        need += after - before;
+        total_new += n;
+        if (n > 0 && seq_lens[b] % bs != 0) {      // writes into its last block
+            const int32_t id = block_tables[(int64_t)b * max_blocks_per_seq + seq_lens[b] / bs];
+            if (id < 0 || id >= pool->num_blocks || pool->refcount[id] <= 0)
+                return PKV_ERR_INVALID;
+            int &d = dropped[id];
+            if (pool->refcount[id] - d > 1) {
+                ++need;
+                ++d;
+            }
+        }
+    }
+    if (total_new > 0 && !slot_mapping)
+        return PKV_ERR_INVALID;
+    if (need > (int64_t)pool->free_stack.size())
+        return PKV_ERR_NO_BLOCKS;
+    // Second pass: copies, new blocks and slots.
+    int copies = 0;
+    int64_t k = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int n = num_new ? num_new[b] : 1;
+        int32_t *row = block_tables + (int64_t)b * max_blocks_per_seq;
+        if (n > 0 && seq_lens[b] % bs != 0) {
+            int32_t &entry = row[seq_lens[b] / bs];
+            if (pool->refcount[entry] > 1) {
+                int32_t fresh;
+                kv_block_alloc(pool, 1, &fresh);    // cannot fail: counted above
+                copy_src[copies] = entry;
+                copy_dst[copies] = fresh;
+                ++copies;
+                --pool->refcount[entry];            // still held by the others
+                entry = fresh;
+            }
+        }
+        for (int j = 0; j < n; ++j) {
+            const int64_t pos = (int64_t)seq_lens[b] + j;
+            if (pos % bs == 0) {
+                int32_t id;
+                kv_block_alloc(pool, 1, &id);       // cannot fail: counted above
+                row[pos / bs] = id;
+            }
+            slot_mapping[k++] = (int32_t)((int64_t)row[pos / bs] * bs + pos % bs);
+        }
+    }
+    *num_copies = copies;
+    return PKV_OK;
+}
+
 // ---------------------------------------------------------------- device calls
+
+int kv_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, int n,
+                  void *k_cache, void *v_cache, void *k_scales, void *v_scales,
+                  pkv_stream_t stream)
+{
+    if (!pool || n < 0)
+        return PKV_ERR_INVALID;
+    if (n == 0)
+        return PKV_OK;
+    if (!src || !dst || !k_cache || !v_cache || (reinterpret_cast<uintptr_t>(src) & 3u) ||
+        (reinterpret_cast<uintptr_t>(dst) & 3u) || !pkv::aligned16(k_cache) ||
+        !pkv::aligned16(v_cache))
+        return PKV_ERR_INVALID;
+    if (pool->kv_dtype == PKV_I8 && (!k_scales || !v_scales ||
+                                     (reinterpret_cast<uintptr_t>(k_scales) & 1u) ||
+                                     (reinterpret_cast<uintptr_t>(v_scales) & 1u)))
+        return PKV_ERR_INVALID;
+    if (!pool->has_device)
+        return PKV_ERR_CUDA;
+    return pkv::launch_block_copy(pool, src, dst, n, k_cache, v_cache, k_scales, v_scales,
+                                  stream);
+}
 
 int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
               const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,

@@ -39,8 +39,8 @@ PKV_DTYPE = {v: k for k, v in TORCH_DTYPE.items()}
 # Every symbol the header declares (checked by the tests).
 SYMBOLS = ("pkv_status_string", "kv_block_pool_init", "kv_block_pool_destroy", "kv_cache_bytes",
            "kv_scales_bytes", "kv_num_free_blocks", "kv_block_refcount", "kv_block_alloc",
-           "kv_block_share", "kv_block_free", "kv_reserve_slots", "kv_slot_mapping", "kv_append",
-           "paged_decode_workspace_bytes", "paged_decode_attention",
+           "kv_block_share", "kv_block_free", "kv_reserve_slots", "kv_reserve_slots_cow",
+           "kv_slot_mapping", "kv_append", "kv_block_copy", "paged_decode_workspace_bytes", "paged_decode_attention",
            "paged_decode_attention_noalloc", "pkv_check_error")
 
 
@@ -88,6 +88,11 @@ def load() -> ctypes.CDLL:
         lib.kv_block_free.restype = I
         lib.kv_reserve_slots.argtypes = [P, I, I32P, I32P, I32P, I, I32P]
         lib.kv_reserve_slots.restype = I
+        lib.kv_reserve_slots_cow.argtypes = [P, I, I32P, I32P, I32P, I, I32P, I32P, I32P,
+                                             ctypes.POINTER(I)]
+        lib.kv_reserve_slots_cow.restype = I
+        lib.kv_block_copy.argtypes = [P, P, P, I, P, P, P, P, P]
+        lib.kv_block_copy.restype = I
         lib.kv_slot_mapping.argtypes = [I32P, I, I, I, I32P, I32P, I32P]
         lib.kv_slot_mapping.restype = I
         lib.kv_append.argtypes = [P, P, P, I, P, I, P, P, P, P, P]
@@ -238,6 +243,26 @@ def kv_reserve_slots(pool: Pool, seq_lens, block_tables: np.ndarray, num_new=Non
     return slots[:total]
 
 
+def kv_reserve_slots_cow(pool: Pool, seq_lens, block_tables: np.ndarray, num_new=None):
+    """kv_reserve_slots for tables that may share blocks.  Returns (slots, copy_src,
+    copy_dst): the pairs of blocks to copy with kv_block_copy before the append."""
+    if block_tables.dtype != np.int32 or not block_tables.flags.c_contiguous:
+        raise ValueError("block_tables must be a C-contiguous int32 array")
+    sl = _i32(seq_lens)
+    nn = None if num_new is None else _i32(num_new)
+    total = sl.size if nn is None else int(nn.sum())
+    slots = np.zeros(max(total, 1), np.int32)
+    src = np.zeros(max(sl.size, 1), np.int32)
+    dst = np.zeros(max(sl.size, 1), np.int32)
+    ncopy = ctypes.c_int(0)
+    _check(load().kv_reserve_slots_cow(pool.handle, sl.size, _i32p(sl), _i32p(nn),
+                                       _i32p(block_tables), block_tables.shape[1], _i32p(slots),
+                                       _i32p(src), _i32p(dst), ctypes.byref(ncopy)),
+           "kv_reserve_slots_cow")
+    n = ncopy.value
+    return slots[:total], src[:n].copy(), dst[:n].copy()
+
+
 def kv_slot_mapping(block_tables, block_size: int, start, num_new=None) -> np.ndarray:
     bt = _i32(block_tables)
     st = _i32(start)
@@ -260,6 +285,16 @@ def kv_append(pool: Pool, k_new, v_new, slot_mapping, k_cache, v_cache, k_scales
     _check(load().kv_append(pool.handle, _dptr(k_new), _dptr(v_new), PKV_DTYPE[k_new.dtype],
                             _dptr(slot_mapping), T, _dptr(k_cache), _dptr(v_cache),
                             _dptr(k_scales), _dptr(v_scales), _stream(stream)), "kv_append")
+
+
+def kv_block_copy(pool: Pool, src, dst, k_cache, v_cache, k_scales=None, v_scales=None,
+                  stream=None) -> None:
+    """Copy blocks src[i] -> dst[i] (device int32 tensors) in the caches."""
+    if src.dtype != torch.int32 or dst.dtype != torch.int32 or src.numel() != dst.numel():
+        raise ValueError("src and dst must be int32 tensors of equal length")
+    _check(load().kv_block_copy(pool.handle, _dptr(src), _dptr(dst), src.numel(),
+                                _dptr(k_cache), _dptr(v_cache), _dptr(k_scales),
+                                _dptr(v_scales), _stream(stream)), "kv_block_copy")
 
 
 def paged_decode_workspace_bytes(pool: Pool, batch: int, num_q_heads: int) -> int:
