@@ -65,6 +65,21 @@ def attention_bytes(wl: W.Workload, lens: np.ndarray) -> int:
     return kv + q + out + table + wl.batch * 4
 
 
+def attention_bytes_window(wl: W.Workload, lens: np.ndarray, window: int) -> int:
+    """attention_bytes for a sliding window: the last min(L, window) rows of each
+    sequence and the table entries of the blocks that hold them."""
+    L = lens.astype(np.int64)
+    lo = np.maximum(L - window, 0)
+    rows = int((L - lo).sum())
+    kv = rows * wl.num_kv_heads * wl.head_dim * eb(wl.kv_dtype) * 2
+    if wl.kv_dtype == W.I8:
+        kv += rows * wl.num_kv_heads * 2 * 2
+    q = wl.batch * wl.num_q_heads * wl.head_dim * eb(wl.q_dtype)
+    out = wl.batch * wl.num_q_heads * wl.head_dim * 4
+    table = int((-(-L // wl.block_size) - lo // wl.block_size).sum()) * 4
+    return kv + q + out + table + wl.batch * 4
+
+
 def append_bytes(wl: W.Workload, ntok: int) -> int:
     """New K/V rows read and written once, plus the slot mapping."""
     row = wl.num_kv_heads * wl.head_dim
@@ -377,6 +392,32 @@ def run_gpu(args):
         raise RuntimeError("device error in the block-copy measurement")
     del ck, cv
 
+    # ---- sliding-window attention (window 1024) on the same caches.  The
+    # window's 67 MB fit in L2, so L2 is flushed (a 256 MB write) before every
+    # timed call and each call has its own events.
+    win = 1024
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    win_bytes = attention_bytes_window(wl, lens_h[0], win)
+
+    def win_call():
+        pkv.paged_decode_attention_window(pool, d_q[0], kc, vc, tables, d_lens[0], scale, out, ws,
+                                          max_len, win, stream=stream)
+
+    for _ in range(3):
+        win_call()
+    win_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(50)]
+    for e0, e1 in win_ev:
+        flush.zero_()
+        e0.record(stream)
+        win_call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    win_ms = sorted(e0.elapsed_time(e1) for e0, e1 in win_ev)[len(win_ev) // 2]
+    if pkv.pkv_check_error(pool) != pkv.PKV_OK:
+        raise RuntimeError("device error in the sliding-window measurement")
+    del flush
+
     # ---- peaks, traffic and the CPU baseline (rank 0)
     peaks = {}
     try:
@@ -432,7 +473,13 @@ def run_gpu(args):
                                   "launch_us": cow_ms * 1e3, "bytes_per_launch": cow_bytes,
                                   "pairs": cow_blocks // 2,
                                   "note": "copy-on-write block copy, bf16 blocks of the "
-                                          "same shape, read + write bytes"}},
+                                          "same shape, read + write bytes"},
+                "paged_decode_attention_window": {
+                    "value": win_bytes / (win_ms / 1e3) / 1e9, "unit": "GB/s",
+                    "frac": win_bytes / (win_ms / 1e3) / 1e9 / peak, "launch_us": win_ms * 1e3,
+                    "bytes_per_launch": win_bytes, "window": win,
+                    "note": "same workload, last 1024 rows of each sequence; L2 flushed "
+                            "before each call; median of 50"}},
             "clocks": clk,
         }
         print(json.dumps(line))

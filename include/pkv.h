@@ -296,6 +296,27 @@ int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtyp
                            pkv_stream_t stream);
 
 /*
+ * paged_decode_attention_window — paged_decode_attention restricted to a
+ * sliding window: sequence b attends over its last min(window,
+ * seq_lens[b]) cached rows only, positions [seq_lens[b] - window,
+ * seq_lens[b]).  [VIS] "What the page leaves out" names sliding-window
+ * attention as a variant it does not show; this is the plain reading: the
+ * softmax of [NOTES] "Concept" taken over the window's rows.  Rows before the
+ * window are not read (their table entries are not looked at either), so a
+ * caller may already have freed those blocks.  window == 0 is full attention
+ * (identical to paged_decode_attention); window < 0 is PKV_ERR_INVALID.  All
+ * other arguments, the workspace and the error behaviour are those of
+ * paged_decode_attention.
+ */
+int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
+                                  int num_q_heads, const void *k_cache, const void *v_cache,
+                                  const void *k_scales, const void *v_scales,
+                                  const int32_t *block_tables, int max_blocks_per_seq,
+                                  const int32_t *seq_lens, int batch, int max_seq_len,
+                                  int window, float scale, float *out, void *workspace,
+                                  size_t workspace_bytes, pkv_stream_t stream);
+
+/*
  * paged_decode_attention_noalloc — paged_decode_attention for callers that
  * cannot allocate device memory.  The pages have no counterpart; this is a
  * property of this library's interface, not of the method.

@@ -314,18 +314,27 @@ void orc_append_q8(const void *k_new, const void *v_new, int in_dtype, const int
 /* dequantized as code * scale.  [VIS] "PagedAttention: the cache in     */
 /* blocks" (block table maps logical to physical blocks).                */
 /* ------------------------------------------------------------------ */
-void orc_gather(const void *cache, const uint16_t *scales, int dtype, const int32_t *block_table_row,
-                int seq_len, int head, int num_kv_heads, int head_dim, int block_size, double *rows)
+/* Rows of positions first .. last-1 (rows[0] is position first). */
+void orc_gather_range(const void *cache, const uint16_t *scales, int dtype,
+                      const int32_t *block_table_row, int first, int last, int head,
+                      int num_kv_heads, int head_dim, int block_size, double *rows)
 {
-    for (int t = 0; t < seq_len; ++t) {
+    for (int t = first; t < last; ++t) {
         int64_t slot = orc_slot_of(block_table_row, block_size, t);
         int64_t base = cache_index(slot, head, 0, block_size, num_kv_heads, head_dim);
         double sc = 1.0;
         if (dtype == ORC_I8)
             sc = orc_half_to_double(scales[base / head_dim]);
         for (int i = 0; i < head_dim; ++i)
-            rows[(int64_t)t * head_dim + i] = load_elem(cache, dtype, base + i) * sc;
+            rows[(int64_t)(t - first) * head_dim + i] = load_elem(cache, dtype, base + i) * sc;
     }
+}
+
+void orc_gather(const void *cache, const uint16_t *scales, int dtype, const int32_t *block_table_row,
+                int seq_len, int head, int num_kv_heads, int head_dim, int block_size, double *rows)
+{
+    orc_gather_range(cache, scales, dtype, block_table_row, 0, seq_len, head, num_kv_heads,
+                     head_dim, block_size, rows);
 }
 
 /* ------------------------------------------------------------------ */
@@ -374,22 +383,32 @@ void orc_attend_rows(const double *q, const double *krows, const double *vrows, 
 /* Returns 0, or -1 when a table entry or length is out of range.       */
 /* nthreads <= 0 uses the OpenMP default.                               */
 /* ------------------------------------------------------------------ */
-int orc_paged_decode_attention(const void *q, int q_dtype, int num_q_heads, const void *k_cache,
-                               const void *v_cache, const uint16_t *k_scales,
-                               const uint16_t *v_scales, int kv_dtype, int num_blocks,
-                               int num_kv_heads, int head_dim, int block_size,
-                               const int32_t *block_tables, int max_blocks_per_seq,
-                               const int32_t *seq_lens, int batch, double scale, double *out,
-                               int nthreads)
+/* Sliding window (a variant [VIS] "What the page leaves out" names): with
+ * window > 0 a sequence attends over its last min(window, L) rows only,
+ * positions L - window .. L-1; the same softmax over fewer rows.  Rows
+ * before the window are neither gathered nor looked up.  window == 0 is
+ * full attention. */
+static int window_start(int L, int window)
 {
-    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return (window > 0 && L > window) ? L - window : 0;
+}
+
+int orc_paged_decode_attention_window(const void *q, int q_dtype, int num_q_heads,
+                                      const void *k_cache, const void *v_cache,
+                                      const uint16_t *k_scales, const uint16_t *v_scales,
+                                      int kv_dtype, int num_blocks, int num_kv_heads,
+                                      int head_dim, int block_size, const int32_t *block_tables,
+                                      int max_blocks_per_seq, const int32_t *seq_lens, int batch,
+                                      int window, double scale, double *out, int nthreads)
+{
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || window < 0)
         return -1;
     int group = num_q_heads / num_kv_heads;
     for (int b = 0; b < batch; ++b) {
         if (seq_lens[b] < 0 || seq_lens[b] > (int64_t)max_blocks_per_seq * block_size)
             return -1;
         int nb = (seq_lens[b] + block_size - 1) / block_size;
-        for (int j = 0; j < nb; ++j) {
+        for (int j = window_start(seq_lens[b], window) / block_size; j < nb; ++j) {
             int32_t id = block_tables[(int64_t)b * max_blocks_per_seq + j];
             if (id < 0 || id >= num_blocks)
                 return -1;
@@ -408,19 +427,23 @@ int orc_paged_decode_attention(const void *q, int q_dtype, int num_q_heads, cons
         int b = (int)(item / num_kv_heads);
         int kvh = (int)(item % num_kv_heads);
         int L = seq_lens[b];
+        int lo = window_start(L, window);
+        int n = L - lo;
         const int32_t *row = block_tables + (int64_t)b * max_blocks_per_seq;
-        double *kr = (double *)malloc(sizeof(double) * ((size_t)L * head_dim + 1));
-        double *vr = (double *)malloc(sizeof(double) * ((size_t)L * head_dim + 1));
-        double *sc = (double *)malloc(sizeof(double) * ((size_t)L + 1));
+        double *kr = (double *)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double *vr = (double *)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double *sc = (double *)malloc(sizeof(double) * ((size_t)n + 1));
         double *qd = (double *)malloc(sizeof(double) * head_dim);
-        orc_gather(k_cache, k_scales, kv_dtype, row, L, kvh, num_kv_heads, head_dim, block_size, kr);
-        orc_gather(v_cache, v_scales, kv_dtype, row, L, kvh, num_kv_heads, head_dim, block_size, vr);
+        orc_gather_range(k_cache, k_scales, kv_dtype, row, lo, L, kvh, num_kv_heads, head_dim,
+                         block_size, kr);
+        orc_gather_range(v_cache, v_scales, kv_dtype, row, lo, L, kvh, num_kv_heads, head_dim,
+                         block_size, vr);
         for (int g = 0; g < group; ++g) {
             int h = kvh * group + g;
             int64_t qb = ((int64_t)b * num_q_heads + h) * head_dim;
             for (int i = 0; i < head_dim; ++i)
                 qd[i] = load_elem(q, q_dtype, qb + i);
-            orc_attend_rows(qd, kr, vr, L, head_dim, scale, out + qb, sc);
+            orc_attend_rows(qd, kr, vr, n, head_dim, scale, out + qb, sc);
         }
         free(kr);
         free(vr);
@@ -428,6 +451,21 @@ int orc_paged_decode_attention(const void *q, int q_dtype, int num_q_heads, cons
         free(qd);
     }
     return 0;
+}
+
+int orc_paged_decode_attention(const void *q, int q_dtype, int num_q_heads, const void *k_cache,
+                               const void *v_cache, const uint16_t *k_scales,
+                               const uint16_t *v_scales, int kv_dtype, int num_blocks,
+                               int num_kv_heads, int head_dim, int block_size,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *seq_lens, int batch, double scale, double *out,
+                               int nthreads)
+{
+    return orc_paged_decode_attention_window(q, q_dtype, num_q_heads, k_cache, v_cache, k_scales,
+                                             v_scales, kv_dtype, num_blocks, num_kv_heads,
+                                             head_dim, block_size, block_tables,
+                                             max_blocks_per_seq, seq_lens, batch, 0, scale, out,
+                                             nthreads);
 }
 
 int orc_max_threads(void)

@@ -78,6 +78,9 @@ def _load():
         lib.orc_paged_decode_attention.argtypes = [P, I, I, P, P, P, P, I, I, I, I, I, P, I, P,
                                                    I, D, P, I]
         lib.orc_paged_decode_attention.restype = I
+        lib.orc_paged_decode_attention_window.argtypes = [P, I, I, P, P, P, P, I, I, I, I, I, P,
+                                                          I, P, I, I, D, P, I]
+        lib.orc_paged_decode_attention_window.restype = I
         lib.orc_max_threads.argtypes = []
         lib.orc_max_threads.restype = I
         lib.orc_kv_bytes_per_token.argtypes = [I64, I64, I64, I64]
@@ -215,8 +218,9 @@ def attend_rows(q, krows, vrows, scale):
 
 
 def paged_decode_attention(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens, scale,
-                           k_scales=None, v_scales=None, nthreads=0):
-    """fp64 attention of every (sequence, query head) against its cached rows.
+                           k_scales=None, v_scales=None, nthreads=0, window=0):
+    """fp64 attention of every (sequence, query head) against its cached rows
+    (with window > 0: against its last min(window, L) rows only).
 
     q: [B, Hq, D] raw (fp32 or uint16 bits); caches [NB, Hkv, bs, D] raw;
     returns out [B, Hq, D] float64.
@@ -232,10 +236,16 @@ def paged_decode_attention(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
     ks = None if k_scales is None else _c(k_scales, np.uint16)
     vs = None if v_scales is None else _c(v_scales, np.uint16)
     out = np.zeros((B, Hq, D), np.float64)
-    rc = _load().orc_paged_decode_attention(_ptr(q), q_dtype, Hq, _ptr(k_cache), _ptr(v_cache),
-                                            _ptr(ks), _ptr(vs), kv_dtype, NB, Hkv, D, bs, _ptr(bt),
-                                            bt.shape[1], _ptr(sl), B, float(scale), _ptr(out),
-                                            int(nthreads))
+    if window:
+        rc = _load().orc_paged_decode_attention_window(
+            _ptr(q), q_dtype, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs), kv_dtype, NB,
+            Hkv, D, bs, _ptr(bt), bt.shape[1], _ptr(sl), B, int(window), float(scale), _ptr(out),
+            int(nthreads))
+    else:
+        rc = _load().orc_paged_decode_attention(_ptr(q), q_dtype, Hq, _ptr(k_cache),
+                                                _ptr(v_cache), _ptr(ks), _ptr(vs), kv_dtype, NB,
+                                                Hkv, D, bs, _ptr(bt), bt.shape[1], _ptr(sl), B,
+                                                float(scale), _ptr(out), int(nthreads))
     if rc != 0:
         raise ValueError("oracle: block table entry or sequence length out of range")
     return out

@@ -39,7 +39,8 @@ size_t decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads)
 int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
                   const void *k_cache, const void *v_cache, const void *k_scales,
                   const void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
-                  const int32_t *seq_lens, int batch, int max_seq_len, float scale, float *out,
+                  const int32_t *seq_lens, int batch, int max_seq_len, int window, float scale,
+                  float *out,
                   void *workspace, size_t workspace_bytes, pkv_stream_t stream)
 {
     (void)workspace_bytes;
@@ -74,6 +75,7 @@ int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int nu
     prm.max_seq_len = max_seq_len;
     const int64_t table_cap = (int64_t)max_blocks_per_seq * pool->block_size;
     prm.len_cap = (int)std::min<int64_t>(max_seq_len, table_cap);
+    prm.window = window > 0 ? window : 0;
     prm.num_blocks = pool->num_blocks;
     prm.q_dtype = q_dtype;
     prm.q_bytes = dtype_bytes(q_dtype);

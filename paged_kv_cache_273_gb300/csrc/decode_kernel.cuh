@@ -121,6 +121,7 @@ struct Params {
     int max_blocks_per_seq;
     int max_seq_len;
     int len_cap;        // min(max_seq_len, max_blocks_per_seq * block_size)
+    int window;         // > 0: attend over the last `window` rows only
     int num_blocks;
     int q_dtype;
     int q_bytes;
@@ -143,7 +144,7 @@ __host__ __device__ inline Layout make_layout(int nst, int batch)
     L.qring = o; o += 2 * C::QSLOT;
     L.merge = o; o += round_up(C::MERGE_FLOATS * 4, 16);
     L.ps = o; o += C::PS_FLOATS * 4;
-    L.lens = o; o += batch * 4;
+    L.lens = o; o += 2 * batch * 4;        // lengths, then window starts
     L.tstart = o; o += (batch + 1) * 4;
     o = round_up(o, 8);
     L.bars = o; o += (2 * nst + 4) * 8;
@@ -462,6 +463,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     float *merge = reinterpret_cast<float *>(smem + lay.merge);
     float *psbuf = reinterpret_cast<float *>(smem + lay.ps);
     int *s_len = reinterpret_cast<int *>(smem + lay.lens);
+    int *s_lo = s_len + p.batch;   // first attended position (sliding window)
     int *s_tstart = reinterpret_cast<int *>(smem + lay.tstart);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
     uint64_t *empty = full + p.nst;
@@ -506,14 +508,18 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             L = 0;
         }
         s_len[b] = L;
+        s_lo[b] = (p.window > 0 && L > p.window) ? L - p.window : 0;
     }
     __syncthreads();
+    // Tiles of sequence b: from the one holding its first attended row to the
+    // one holding its last.
+    auto seq_tiles = [&](int b) { return (s_len[b] + TILE - 1) / TILE - s_lo[b] / TILE; };
     {
         const int per = (B + NTHREADS - 1) / NTHREADS;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         int sum = 0;
         for (int b = b0; b < b1; ++b)
-            sum += ((s_len[b] + TILE - 1) / TILE) * Hkv;
+            sum += seq_tiles(b) * Hkv;
         int incl = sum;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -540,7 +546,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         int base = (warp > 0 ? wsum[warp - 1] : 0) + incl - sum;
         for (int b = b0; b < b1; ++b) {
             s_tstart[b] = base;
-            base += ((s_len[b] + TILE - 1) / TILE) * Hkv;
+            base += seq_tiles(b) * Hkv;
         }
         if (tid == 0)
             s_tstart[B] = wsum[NTHREADS / 32 - 1];
@@ -577,7 +583,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 const int nt = (s_tstart[d.b + 1] - s_tstart[d.b]) / Hkv;
                 const int off = (int)(x - s_tstart[d.b]);
                 d.kvh = off / nt;
-                d.ti = off - d.kvh * nt;
+                d.ti = off - d.kvh * nt + s_lo[d.b] / TILE;
                 const int nvalid = min(TILE, s_len[d.b] - TILE * d.ti);
                 const int32_t *row = p.block_tables + (int64_t)d.b * p.max_blocks_per_seq;
                 const int first = (TILE * d.ti) >> p.bs_log2;
@@ -784,13 +790,14 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             const int nt = (s_tstart[b + 1] - s_tstart[b]) / Hkv;
             const int off = (int)(x - s_tstart[b]);
             const int kvh = off / nt;
-            const int ti0 = off - kvh * nt;
+            const int ti0 = off - kvh * nt + s_lo[b] / TILE;   // tile index in the sequence
             const int64_t seg_begin = (int64_t)s_tstart[b] + (int64_t)kvh * nt;
             const int64_t seg_end = seg_begin + nt;
             const int64_t xe = min(seg_end, R1);
             const int k0 = (int)(x - R0);
             const int k1 = (int)(xe - R0);
             const int L = s_len[b];
+            const int lo = s_lo[b];
 
             // q of this (sequence, KV head) group.
             QRegs<D, G, KV> qr;
@@ -826,6 +833,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             for (int k = kfirst; k < k1; k += W) {
                 const int ti = ti0 + (k - k0);
                 const int nvalid = min(TILE, L - TILE * ti);
+                const int tlo = lo - TILE * ti;          // > 0 only in the window's first tile
                 // Warps take tiles round-robin and may drift apart, so this
                 // warp can reach tile k while the stage's previous tile
                 // (k - stages) is still landing; a parity wait alone would
@@ -885,7 +893,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 bool above = false;
 #pragma unroll
                 for (int r = 0; r < C::NF; ++r) {
-                    s[r] = t < nvalid ? part[r] * kscale : -INFINITY;
+                    s[r] = (t < nvalid && t >= tlo) ? part[r] * kscale : -INFINITY;
                     above |= s[r] > m_run[r];
                 }
                 // The running maximum only needs to move when some score

@@ -61,7 +61,8 @@ size_t decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads);
 int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
                   const void *k_cache, const void *v_cache, const void *k_scales,
                   const void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
-                  const int32_t *seq_lens, int batch, int max_seq_len, float scale, float *out,
+                  const int32_t *seq_lens, int batch, int max_seq_len, int window, float scale,
+                  float *out,
                   void *workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 }  // namespace pkv

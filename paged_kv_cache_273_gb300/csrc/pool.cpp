@@ -368,14 +368,16 @@ size_t paged_decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_h
     return pkv::decode_workspace_bytes(pool, batch, num_q_heads);
 }
 
-int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
-                           int num_q_heads, const void *k_cache, const void *v_cache,
-                           const void *k_scales, const void *v_scales,
-                           const int32_t *block_tables, int max_blocks_per_seq,
-                           const int32_t *seq_lens, int batch, int max_seq_len, float scale,
-                           float *out, void *workspace, size_t workspace_bytes,
-                           pkv_stream_t stream)
+namespace {
+
+int decode_call(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
+                const void *k_cache, const void *v_cache, const void *k_scales,
+                const void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
+                const int32_t *seq_lens, int batch, int max_seq_len, int window, float scale,
+                float *out, void *workspace, size_t workspace_bytes, pkv_stream_t stream)
 {
+    if (window < 0)
+        return PKV_ERR_INVALID;
     if (!pool || batch < 0 || max_blocks_per_seq < 0 || max_seq_len < 0 || num_q_heads < 1)
         return PKV_ERR_INVALID;
     if (num_q_heads % pool->num_kv_heads != 0)
@@ -409,7 +411,35 @@ int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtyp
         return PKV_ERR_INVALID;
     return pkv::launch_decode(pool, q, q_dtype, num_q_heads, k_cache, v_cache, k_scales, v_scales,
                               block_tables, max_blocks_per_seq, seq_lens, batch, max_seq_len,
-                              scale, out, workspace, workspace_bytes, stream);
+                              window, scale, out, workspace, workspace_bytes, stream);
+}
+
+}  // namespace
+
+int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
+                           int num_q_heads, const void *k_cache, const void *v_cache,
+                           const void *k_scales, const void *v_scales,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, int batch, int max_seq_len, float scale,
+                           float *out, void *workspace, size_t workspace_bytes,
+                           pkv_stream_t stream)
+{
+    return decode_call(pool, q, q_dtype, num_q_heads, k_cache, v_cache, k_scales, v_scales,
+                       block_tables, max_blocks_per_seq, seq_lens, batch, max_seq_len, 0, scale,
+                       out, workspace, workspace_bytes, stream);
+}
+
+int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
+                                  int num_q_heads, const void *k_cache, const void *v_cache,
+                                  const void *k_scales, const void *v_scales,
+                                  const int32_t *block_tables, int max_blocks_per_seq,
+                                  const int32_t *seq_lens, int batch, int max_seq_len,
+                                  int window, float scale, float *out, void *workspace,
+                                  size_t workspace_bytes, pkv_stream_t stream)
+{
+    return decode_call(pool, q, q_dtype, num_q_heads, k_cache, v_cache, k_scales, v_scales,
+                       block_tables, max_blocks_per_seq, seq_lens, batch, max_seq_len, window,
+                       scale, out, workspace, workspace_bytes, stream);
 }
 
 int pkv_check_error(const pkv_pool *pool, pkv_stream_t stream)

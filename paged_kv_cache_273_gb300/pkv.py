@@ -41,7 +41,7 @@ SYMBOLS = ("pkv_status_string", "kv_block_pool_init", "kv_block_pool_destroy", "
            "kv_scales_bytes", "kv_num_free_blocks", "kv_block_refcount", "kv_block_alloc",
            "kv_block_share", "kv_block_free", "kv_reserve_slots", "kv_reserve_slots_cow",
            "kv_slot_mapping", "kv_append", "kv_block_copy", "paged_decode_workspace_bytes", "paged_decode_attention",
-           "paged_decode_attention_noalloc", "pkv_check_error")
+           "paged_decode_attention_window", "paged_decode_attention_noalloc", "pkv_check_error")
 
 
 class PkvError(RuntimeError):
@@ -102,6 +102,9 @@ def load() -> ctypes.CDLL:
         lib.paged_decode_attention.argtypes = [P, P, I, I, P, P, P, P, P, I, P, I, I, F, P, P,
                                                SZ, P]
         lib.paged_decode_attention.restype = I
+        lib.paged_decode_attention_window.argtypes = [P, P, I, I, P, P, P, P, P, I, P, I, I, I,
+                                                      F, P, P, SZ, P]
+        lib.paged_decode_attention_window.restype = I
         lib.paged_decode_attention_noalloc.argtypes = [P, P, I, I, P, P, P, P, P, I, P, I, I, F,
                                                        P, P]
         lib.paged_decode_attention_noalloc.restype = I
@@ -324,6 +327,25 @@ def paged_decode_attention(pool: Pool, q, k_cache, v_cache, block_tables, seq_le
         _dptr(k_scales), _dptr(v_scales), _dptr(block_tables), block_tables.shape[1],
         _dptr(seq_lens), B, int(max_seq_len), float(scale), _dptr(out), _dptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)), "paged_decode_attention")
+
+
+def paged_decode_attention_window(pool: Pool, q, k_cache, v_cache, block_tables, seq_lens,
+                                  scale: float, out, workspace, max_seq_len: int, window: int,
+                                  k_scales=None, v_scales=None, stream=None) -> None:
+    """paged_decode_attention over the last `window` rows of each sequence (0 = all)."""
+    if q.dtype not in PKV_DTYPE:
+        raise ValueError("unsupported q dtype %s" % q.dtype)
+    if out.dtype != torch.float32:
+        raise ValueError("out must be float32")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_tables and seq_lens must be int32")
+    B, Hq, _ = q.shape
+    _check(load().paged_decode_attention_window(
+        pool.handle, _dptr(q), PKV_DTYPE[q.dtype], Hq, _dptr(k_cache), _dptr(v_cache),
+        _dptr(k_scales), _dptr(v_scales), _dptr(block_tables), block_tables.shape[1],
+        _dptr(seq_lens), B, int(max_seq_len), int(window), float(scale), _dptr(out),
+        _dptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "paged_decode_attention_window")
 
 
 def paged_decode_attention_noalloc(pool: Pool, q, k_cache, v_cache, block_tables, seq_lens,
