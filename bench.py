@@ -52,12 +52,17 @@ def eb(code):
     return {W.F32: 4, W.F16: 2, W.BF16: 2, W.I8: 1}[code]
 
 
+def row_bytes(code, head_dim):
+    """Bytes of one cached row (4-bit codes: two per byte)."""
+    return head_dim // 2 if code == W.I4 else head_dim * eb(code)
+
+
 def attention_bytes(wl: W.Workload, lens: np.ndarray) -> int:
     """Algorithmic bytes of one attention call: every cached K and V row once
     (+ int8 scales), q, the fp32 output, the block-table entries and lengths."""
     L = lens.astype(np.int64)
-    kv = int(L.sum()) * wl.num_kv_heads * wl.head_dim * eb(wl.kv_dtype) * 2
-    if wl.kv_dtype == W.I8:
+    kv = int(L.sum()) * wl.num_kv_heads * row_bytes(wl.kv_dtype, wl.head_dim) * 2
+    if wl.kv_dtype in (W.I8, W.I4):
         kv += int(L.sum()) * wl.num_kv_heads * 2 * 2
     q = wl.batch * wl.num_q_heads * wl.head_dim * eb(wl.q_dtype)
     out = wl.batch * wl.num_q_heads * wl.head_dim * 4
@@ -71,8 +76,8 @@ def attention_bytes_window(wl: W.Workload, lens: np.ndarray, window: int) -> int
     L = lens.astype(np.int64)
     lo = np.maximum(L - window, 0)
     rows = int((L - lo).sum())
-    kv = rows * wl.num_kv_heads * wl.head_dim * eb(wl.kv_dtype) * 2
-    if wl.kv_dtype == W.I8:
+    kv = rows * wl.num_kv_heads * row_bytes(wl.kv_dtype, wl.head_dim) * 2
+    if wl.kv_dtype in (W.I8, W.I4):
         kv += rows * wl.num_kv_heads * 2 * 2
     q = wl.batch * wl.num_q_heads * wl.head_dim * eb(wl.q_dtype)
     out = wl.batch * wl.num_q_heads * wl.head_dim * 4
@@ -225,6 +230,66 @@ def config_block(wl, l2_note):
             "l2": l2_note}
 
 
+# ------------------------------------------------------------------ other workload shapes
+def time_workload(name: str, dev, stream, peak: float, reps: int = 20) -> dict:
+    """Attention on another workload's shape (lengths, tables, dtypes): the
+    caches are filled with random codes / values on the device (timing only;
+    parity is the tests' job).  Back-to-back calls, caches larger than L2."""
+    import torch
+    from paged_kv_cache_273_gb300 import pkv
+    inp = W.make_inputs(name, values=False)
+    wl = inp.workload
+    B, Hq, Hkv, D, bs = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
+    pool = pkv.kv_block_pool_init(inp.num_blocks, bs, Hkv, D, wl.kv_dtype)
+    kc, vc, ks, vs = pool.alloc_cache(dev)
+    for c in (kc, vc):
+        if c.dtype == torch.int8:
+            c.random_(-127, 128)
+        elif c.dtype == torch.uint8:
+            c.random_(0, 256)
+        else:
+            c.normal_()
+    for c in (ks, vs):
+        if c is not None:
+            c.uniform_(0.001, 0.05)
+    qdt = {W.F16: torch.float16, W.BF16: torch.bfloat16, W.F32: torch.float32}[wl.q_dtype]
+    q = torch.randn((B, Hq, D), device=dev).to(qdt)
+    lens_h = inp.lens_after_step(0)
+    lens = torch.from_numpy(lens_h).to(dev)
+    tables = torch.from_numpy(inp.block_tables).to(dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = pkv.alloc_workspace(pool, B, Hq, dev)
+    max_len = int(lens_h.max())
+
+    def call():
+        pkv.paged_decode_attention(pool, q, kc, vc, tables, lens, 1.0 / np.sqrt(D), out, ws,
+                                   max_len, ks, vs, stream=stream)
+
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pkv.pkv_check_error(pool) != pkv.PKV_OK:
+        raise RuntimeError("device error timing workload %s" % name)
+    us = e0.elapsed_time(e1) / reps * 1e3
+    nbytes = attention_bytes(wl, lens_h)
+    cache_mb = 2 * kc.numel() * kc.element_size() / 1e6
+    del kc, vc, ks, vs, ws
+    return {"value": nbytes / (us / 1e6) / 1e9, "unit": "GB/s",
+            "frac": nbytes / (us / 1e6) / 1e9 / peak, "launch_us": us,
+            "bytes_per_launch": nbytes, "cache_mb": cache_mb,
+            "kernel": "paged_decode_kernel<%d,%d,%s>" % (D, wl.group,
+                                                         {W.F32: "f32", W.F16: "f16",
+                                                          W.BF16: "bf16", W.I8: "i8",
+                                                          W.I4: "i4"}[wl.kv_dtype]),
+            "note": "back to back, %d calls; logical bytes (shared prefix rows counted per "
+                    "sequence)" % reps}
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_gpu(args):
     import torch
@@ -369,6 +434,18 @@ def run_gpu(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_val = e2e_bytes * world / float(tt.item()) / 1e9
 
+    # ---- measured peak
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except Exception:
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_note = "measured"
+    if not peak:
+        peak, peak_note = 6800.0, "fallback"
+
     # ---- copy-on-write block copy (kv_block_copy) on a pool of the same shape:
     # 4096 block pairs per launch, 268 MB read + 268 MB written (twice L2)
     cow_blocks = 8192
@@ -418,17 +495,12 @@ def run_gpu(args):
         raise RuntimeError("device error in the sliding-window measurement")
     del flush
 
-    # ---- peaks, traffic and the CPU baseline (rank 0)
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except Exception:
-        pass
-    peak = peaks.get("hbm_gbs")
-    peak_note = "measured"
-    if not peak:
-        peak, peak_note = 6800.0, "fallback"
+    # ---- the other workload shapes (rank 0 at N = 1 only; not part of `value`)
+    others = {}
+    if world == 1:
+        for name in ("gpt2", "llama2_70b", "int8", "int4"):
+            others[name] = time_workload(name, dev, stream, peak)
+
     traffic = None
     try:
         with open(TRAFFIC_FILE) as f:
@@ -480,6 +552,7 @@ def run_gpu(args):
                     "bytes_per_launch": win_bytes, "window": win,
                     "note": "same workload, last 1024 rows of each sequence; L2 flushed "
                             "before each call; median of 50"}},
+            "other_workloads": others,
             "clocks": clk,
         }
         print(json.dumps(line))

@@ -61,7 +61,8 @@ typedef enum {
     PKV_F32 = 0,
     PKV_F16 = 1,
     PKV_BF16 = 2,
-    PKV_I8 = 3
+    PKV_I8 = 3,
+    PKV_I4 = 4
 } pkv_dtype;
 
 typedef enum {

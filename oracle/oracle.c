@@ -38,7 +38,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_I8 = 3 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_I8 = 3, ORC_I4 = 4 };
 
 /* ------------------------------------------------------------------ */
 /* Number formats, from the IEEE 754 binary16 / bfloat16 definitions.  */
@@ -123,6 +123,13 @@ static double load_elem(const void *base, int dtype, int64_t idx)
     case ORC_F16: return orc_half_to_double(((const uint16_t *)base)[idx]);
     case ORC_BF16: return orc_bf16_to_double(((const uint16_t *)base)[idx]);
     case ORC_I8: return (double)((const int8_t *)base)[idx];
+    case ORC_I4: {
+        /* element idx is nibble idx % 2 of byte idx / 2 (low nibble first),
+         * a two's-complement 4-bit code */
+        unsigned byte = ((const uint8_t *)base)[idx / 2];
+        int nib = (int)((idx % 2) ? (byte >> 4) : (byte & 15u));
+        return (double)(nib >= 8 ? nib - 16 : nib);
+    }
     default: return NAN;
     }
 }
@@ -309,6 +316,84 @@ void orc_append_q8(const void *k_new, const void *v_new, int in_dtype, const int
 }
 
 /* ------------------------------------------------------------------ */
+/* 4-bit quantization ([NOTES] "Quantized KV cache" stores the cache in  */
+/* fewer bits; [VIS] "What the page leaves out" names 8-bit and 4-bit   */
+/* caches).  The same symmetric per-token-per-head scheme as int8 with   */
+/* the 4-bit range:                                                      */
+/*   amax = max |x_i|            (fp32)                                  */
+/*   s    = fp16_rne(amax / 7)   (fp32 division, then round to fp16)     */
+/*   code = clamp(round_half_even(x_i / s), -7, 7)                       */
+/* Codes are stored two per byte, element 2j in the low nibble of byte j */
+/* and element 2j+1 in the high nibble, as 4-bit two's complement.  A    */
+/* zero scale gives all codes 0.                                         */
+/* ------------------------------------------------------------------ */
+void orc_quantize_row_q4(const float *x, int n, int8_t *codes, uint16_t *scale_bits)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax)
+            amax = a;
+    }
+    volatile float s32 = amax / 7.0f;
+    uint16_t s16 = orc_float_to_half_rne(s32);
+    *scale_bits = s16;
+    float s = (float)orc_half_to_double(s16);
+    for (int i = 0; i < n; ++i) {
+        if (s == 0.0f) {
+            codes[i] = 0;
+            continue;
+        }
+        volatile float r = x[i] / s;
+        float c = rint_half_even_f(r);
+        if (c > 7.0f)
+            c = 7.0f;
+        if (c < -7.0f)
+            c = -7.0f;
+        codes[i] = (int8_t)c;
+    }
+}
+
+/* Two codes per byte: element 2j in the low nibble of byte j. */
+void orc_pack_q4(const int8_t *codes, int n, uint8_t *bytes)
+{
+    for (int j = 0; j < n / 2; ++j)
+        bytes[j] = (uint8_t)(((unsigned)codes[2 * j] & 15u) |
+                             (((unsigned)codes[2 * j + 1] & 15u) << 4));
+}
+
+void orc_append_q4(const void *k_new, const void *v_new, int in_dtype, const int32_t *slots,
+                   int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                   uint8_t *k_cache, uint8_t *v_cache, uint16_t *k_scales, uint16_t *v_scales)
+{
+    float *row = (float *)malloc(sizeof(float) * head_dim);
+    int8_t *codes = (int8_t *)malloc((size_t)head_dim);
+    for (int t = 0; t < num_tokens; ++t) {
+        if (slots[t] < 0)
+            continue;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t src = ((int64_t)t * num_kv_heads + h) * head_dim;
+            int64_t dst = cache_index(slots[t], h, 0, block_size, num_kv_heads, head_dim);
+            int64_t sidx = dst / head_dim;
+            for (int kv = 0; kv < 2; ++kv) {
+                const void *in = kv == 0 ? k_new : v_new;
+                for (int i = 0; i < head_dim; ++i)
+                    row[i] = (float)load_elem(in, in_dtype, src + i);
+                if (kv == 0) {
+                    orc_quantize_row_q4(row, head_dim, codes, &k_scales[sidx]);
+                    orc_pack_q4(codes, head_dim, k_cache + dst / 2);
+                } else {
+                    orc_quantize_row_q4(row, head_dim, codes, &v_scales[sidx]);
+                    orc_pack_q4(codes, head_dim, v_cache + dst / 2);
+                }
+            }
+        }
+    }
+    free(codes);
+    free(row);
+}
+
+/* ------------------------------------------------------------------ */
 /* Gather: read sequence b's first L cached rows of KV head h through   */
 /* its block table into a contiguous fp64 array [L][D]; int8 rows are    */
 /* dequantized as code * scale.  [VIS] "PagedAttention: the cache in     */
@@ -323,7 +408,7 @@ void orc_gather_range(const void *cache, const uint16_t *scales, int dtype,
         int64_t slot = orc_slot_of(block_table_row, block_size, t);
         int64_t base = cache_index(slot, head, 0, block_size, num_kv_heads, head_dim);
         double sc = 1.0;
-        if (dtype == ORC_I8)
+        if (dtype == ORC_I8 || dtype == ORC_I4)
             sc = orc_half_to_double(scales[base / head_dim]);
         for (int i = 0; i < head_dim; ++i)
             rows[(int64_t)(t - first) * head_dim + i] = load_elem(cache, dtype, base + i) * sc;

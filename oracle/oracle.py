@@ -21,7 +21,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
 
-F32, F16, BF16, I8 = 0, 1, 2, 3
+F32, F16, BF16, I8, I4 = 0, 1, 2, 3, 4
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,12 @@ def _load():
         lib.orc_quantize_row_q8.restype = None
         lib.orc_append_q8.argtypes = [P, P, I, P, I, I, I, I, P, P, P, P]
         lib.orc_append_q8.restype = None
+        lib.orc_quantize_row_q4.argtypes = [P, I, P, P]
+        lib.orc_quantize_row_q4.restype = None
+        lib.orc_pack_q4.argtypes = [P, I, P]
+        lib.orc_pack_q4.restype = None
+        lib.orc_append_q4.argtypes = [P, P, I, P, I, I, I, I, P, P, P, P]
+        lib.orc_append_q4.restype = None
         lib.orc_gather.argtypes = [P, P, I, P, I, I, I, I, I, P]
         lib.orc_gather.restype = None
         lib.orc_attend_rows.argtypes = [P, P, P, I, I, D, P, P]
@@ -99,7 +105,7 @@ def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
 
 
-_NP_OF = {F32: np.float32, F16: np.uint16, BF16: np.uint16, I8: np.int8}
+_NP_OF = {F32: np.float32, F16: np.uint16, BF16: np.uint16, I8: np.int8, I4: np.uint8}
 
 
 # ---------------------------------------------------------------- formats
@@ -192,10 +198,42 @@ def append_q8(k_new, v_new, in_dtype, slots, block_size, k_cache, v_cache, k_sca
                           _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales))
 
 
+def quantize_row_q4(x):
+    """4-bit codes (one int8 per element, -7..7) and the fp16 scale bits."""
+    x = _c(x, np.float32)
+    codes = np.empty(x.size, np.int8)
+    sb = np.zeros(1, np.uint16)
+    _load().orc_quantize_row_q4(_ptr(x), x.size, _ptr(codes), _ptr(sb))
+    return codes, int(sb[0])
+
+
+def pack_q4(codes):
+    codes = _c(codes, np.int8)
+    out = np.empty(codes.size // 2, np.uint8)
+    _load().orc_pack_q4(_ptr(codes), codes.size, _ptr(out))
+    return out
+
+
+def append_q4(k_new, v_new, in_dtype, slots, block_size, k_cache, v_cache, k_scales, v_scales):
+    """Quantize-on-append to a 4-bit cache (uint8 [NB, H, bs, D/2], two codes a byte)."""
+    k_new = _c(k_new, _NP_OF[in_dtype])
+    v_new = _c(v_new, _NP_OF[in_dtype])
+    slots = _c(slots, np.int32)
+    T, H, D = k_new.shape
+    for a, t in ((k_cache, np.uint8), (v_cache, np.uint8), (k_scales, np.uint16),
+                 (v_scales, np.uint16)):
+        assert a.dtype == t and a.flags.c_contiguous
+    assert k_cache.shape[3] * 2 == D
+    _load().orc_append_q4(_ptr(k_new), _ptr(v_new), in_dtype, _ptr(slots), T, H, D, block_size,
+                          _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales))
+
+
 # ---------------------------------------------------------------- attention
 def gather(cache, scales, dtype, block_table_row, seq_len, head, block_size):
     cache = np.ascontiguousarray(cache)
     NB, H, bs, D = cache.shape
+    if dtype == I4:
+        D *= 2                      # two codes per byte
     row = _c(block_table_row, np.int32)
     out = np.empty((seq_len, D), np.float64)
     sc = None if scales is None else _c(scales, np.uint16)
@@ -229,6 +267,8 @@ def paged_decode_attention(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
     k_cache = np.ascontiguousarray(k_cache)
     v_cache = np.ascontiguousarray(v_cache)
     NB, Hkv, bs, D = k_cache.shape
+    if kv_dtype == I4:
+        D *= 2                      # two codes per byte
     B, Hq, Dq = q.shape
     assert Dq == D
     bt = _c(block_tables, np.int32)

@@ -132,6 +132,74 @@ __global__ void __launch_bounds__(256) append_q8_kernel(
     }
 }
 
+// 4-bit cache ([NOTES] "Quantized KV cache": fewer bits per number; the
+// pages name 4-bit caches without fixing a scheme): one warp per (token,
+// head, K|V) row of D = 128 values, the same symmetric per-row scheme as int8
+// with range +-7: s = fp16_rne(amax / 7), code = clamp(round_half_even(x/s)).
+// Codes are two's-complement nibbles, element 2j in the low nibble of byte j;
+// each lane packs its 4 codes into 2 bytes.
+template <typename T>
+__global__ void __launch_bounds__(256) append_q4_kernel(
+    const T *__restrict__ k_new, const T *__restrict__ v_new,
+    const int32_t *__restrict__ slot_mapping, int64_t num_rows /* T*Hkv */, int num_kv_heads,
+    int block_size, int64_t num_slots, uint8_t *__restrict__ k_cache,
+    uint8_t *__restrict__ v_cache, __half *__restrict__ k_scales, __half *__restrict__ v_scales,
+    unsigned int *__restrict__ err)
+{
+    constexpr int D = 128, E = 4;
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t w = warp; w < 2 * num_rows; w += nwarps) {
+        const bool is_v = w >= num_rows;
+        const int64_t row = is_v ? w - num_rows : w;
+        const int64_t t = row / num_kv_heads;
+        const int h = (int)(row - t * num_kv_heads);
+        const int32_t slot = __ldg(slot_mapping + t);
+        if (slot < 0)
+            continue;
+        if ((int64_t)slot >= num_slots) {
+            if (lane == 0)
+                atomicOr(err, PKV_EBIT_SLOT);
+            continue;
+        }
+        const T *src = (is_v ? v_new : k_new) + row * D + lane * E;
+        float x[E];
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            x[e] = load_as_float<T>(src + e);
+            amax = fmaxf(amax, fabsf(x[e]));
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, m));
+        // IEEE fp32 division and round-to-nearest-even conversions only.
+        const __half s16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
+        const float s = __half2float(s16);
+        const int64_t blk = slot / block_size;
+        const int64_t off = slot - blk * block_size;
+        const int64_t srow = (blk * num_kv_heads + h) * block_size + off;
+        uint32_t word = 0;
+#pragma unroll
+        for (int u = 0; u < E; ++u) {
+            int code = 0;
+            if (s != 0.0f) {
+                float c = rintf(__fdiv_rn(x[u], s));     // round half to even
+                c = fminf(fmaxf(c, -7.0f), 7.0f);
+                code = (int)c;
+            }
+            word |= (uint32_t)(code & 0xf) << (4 * u);
+        }
+        uint8_t *dst = (is_v ? v_cache : k_cache) + srow * (D / 2) + lane * (E / 2);
+        *reinterpret_cast<uint16_t *>(dst) = (uint16_t)word;
+        if (lane == 0)
+            (is_v ? v_scales : k_scales)[srow] = s16;
+    }
+}
+
 // Copy whole blocks (copy-on-write): K and V of block src[i] -> dst[i], one
 // thread per 16-byte chunk; a block-head tile row is a multiple of 16 bytes.
 // int8 scales ([NB][Hkv][bs] fp16) follow as 2-byte elements.
@@ -189,8 +257,8 @@ int launch_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *d
 {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t rows = (int64_t)pool->num_kv_heads * pool->block_size;
-    const int64_t chunks = rows * pool->head_dim * dtype_bytes(pool->kv_dtype) / 16;
-    const int64_t scales = pool->kv_dtype == PKV_I8 ? rows : 0;
+    const int64_t chunks = rows * row_bytes(pool->kv_dtype, pool->head_dim) / 16;
+    const int64_t scales = quantized_dtype(pool->kv_dtype) ? rows : 0;
     const int threads = 256;
     const int64_t total = (int64_t)n * (2 * chunks + 2 * scales);
     launch_pdl(block_copy_kernel, dim3(grid_for(total, threads, pool->num_sms)), dim3(threads), 0,
@@ -207,7 +275,23 @@ int launch_append(const pkv_pool *pool, const void *k_new, const void *v_new, pk
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int H = pool->num_kv_heads, D = pool->head_dim, bs = pool->block_size;
     const int64_t num_slots = (int64_t)pool->num_blocks * bs;
-    if (pool->kv_dtype != PKV_I8) {
+    if (pool->kv_dtype == PKV_I4) {
+        const int64_t rows = (int64_t)num_tokens * H;
+        const int threads = 256;
+        const int grid = grid_for(2 * rows * 32, threads, pool->num_sms);
+        uint8_t *kc = static_cast<uint8_t *>(k_cache);
+        uint8_t *vc = static_cast<uint8_t *>(v_cache);
+        __half *ks = static_cast<__half *>(k_scales);
+        __half *vs = static_cast<__half *>(v_scales);
+#define PKV_Q4(T)                                                                           \
+    launch_pdl(append_q4_kernel<T>, dim3(grid), dim3(threads), 0, s,                         \
+               static_cast<const T *>(k_new), static_cast<const T *>(v_new), slot_mapping,   \
+               rows, H, bs, num_slots, kc, vc, ks, vs, pool->d_err)
+        if (in_dtype == PKV_F16) PKV_Q4(__half);
+        else if (in_dtype == PKV_BF16) PKV_Q4(__nv_bfloat16);
+        else PKV_Q4(float);
+#undef PKV_Q4
+    } else if (pool->kv_dtype != PKV_I8) {
         const int chunks_per_row = D * dtype_bytes(pool->kv_dtype) / 16;
         const int64_t total = (int64_t)num_tokens * H * chunks_per_row;
         const int threads = 256;

@@ -17,6 +17,7 @@ extern template int launch_d<PKV_F32>(const pkv_pool *, int, const Params &, int
 extern template int launch_d<PKV_F16>(const pkv_pool *, int, const Params &, int, int, cudaStream_t);
 extern template int launch_d<PKV_BF16>(const pkv_pool *, int, const Params &, int, int, cudaStream_t);
 extern template int launch_d<PKV_I8>(const pkv_pool *, int, const Params &, int, int, cudaStream_t);
+extern template int launch_d<PKV_I4>(const pkv_pool *, int, const Params &, int, int, cudaStream_t);
 }  // namespace kern
 }  // namespace pkv
 
@@ -86,6 +87,7 @@ int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int nu
     case PKV_F16: return kern::launch_d<PKV_F16>(pool, G, prm, batch, max_seq_len, s);
     case PKV_BF16: return kern::launch_d<PKV_BF16>(pool, G, prm, batch, max_seq_len, s);
     case PKV_I8: return kern::launch_d<PKV_I8>(pool, G, prm, batch, max_seq_len, s);
+    case PKV_I4: return kern::launch_d<PKV_I4>(pool, G, prm, batch, max_seq_len, s);
     }
     return PKV_ERR_UNSUPPORTED;
 }

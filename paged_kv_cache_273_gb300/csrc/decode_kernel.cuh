@@ -68,19 +68,23 @@ __host__ __device__ constexpr int consumer_warps(int G, int KV)
     return (KV != PKV_F32 && G <= 2) ? 15 : 11;
 }
 
+// Bits of one cached element.
 template <int KV>
-struct KvBytes;
-template <> struct KvBytes<PKV_F32> { static constexpr int v = 4; };
-template <> struct KvBytes<PKV_F16> { static constexpr int v = 2; };
-template <> struct KvBytes<PKV_BF16> { static constexpr int v = 2; };
-template <> struct KvBytes<PKV_I8> { static constexpr int v = 1; };
+struct KvBits;
+template <> struct KvBits<PKV_F32> { static constexpr int v = 32; };
+template <> struct KvBits<PKV_F16> { static constexpr int v = 16; };
+template <> struct KvBits<PKV_BF16> { static constexpr int v = 16; };
+template <> struct KvBits<PKV_I8> { static constexpr int v = 8; };
+template <> struct KvBits<PKV_I4> { static constexpr int v = 4; };
+
+// Quantized caches carry one fp16 scale per cached row.
+__host__ __device__ constexpr bool quantized(int KV) { return KV == PKV_I8 || KV == PKV_I4; }
 
 template <int D, int G, int KV>
 struct Cfg {
     static constexpr int W = consumer_warps(G, KV);
     static constexpr int NTHREADS = (W + 1) * 32;
-    static constexpr int EB = KvBytes<KV>::v;
-    static constexpr int ROWB = D * EB;            // bytes of one cached row
+    static constexpr int ROWB = D * KvBits<KV>::v / 8;   // bytes of one cached row
     static constexpr int NCH = ROWB / 16;          // 16-byte chunks per row
     static constexpr int DS = NCH >= 8 ? 8 : NCH;  // lanes sharing one token's dot product
     static constexpr int TQ = 32 / DS;             // token groups per warp
@@ -90,7 +94,7 @@ struct Cfg {
     static constexpr int NF = G >= 2 ? G / 2 : 1;  // scores per lane after reduction
     static constexpr int VE = D / 32;              // V elements per lane
     static constexpr int KV_BYTES = TILE * ROWB;
-    static constexpr int SC_BYTES = KV == PKV_I8 ? TILE * 2 : 0;
+    static constexpr int SC_BYTES = quantized(KV) ? TILE * 2 : 0;
     static constexpr int STAGE_BYTES = round_up(2 * KV_BYTES + 2 * SC_BYTES, 128);
     static constexpr int QSLOT = round_up(G * D * 4, 128);   // fits any q dtype
     static constexpr int MERGE_FLOATS = W * G * (D + 2);
@@ -189,6 +193,10 @@ template <int D, int G>
 struct QRegs<D, G, PKV_F32> { float4 w[G][Cfg<D, G, PKV_F32>::CPL]; };
 template <int D, int G>
 struct QRegs<D, G, PKV_I8> { float w[G][Cfg<D, G, PKV_I8>::CPL][16]; };
+// 4-bit K: q as fp16 pairs in the order the codes are unpacked (pair 4w+k of
+// a 32-code chunk holds elements 8w+k and 8w+k+4).
+template <int D, int G>
+struct QRegs<D, G, PKV_I4> { uint32_t w[G][Cfg<D, G, PKV_I4>::CPL][16]; };
 
 __device__ __forceinline__ float q_elem(const unsigned char *qs, int idx, int q_dtype)
 {
@@ -213,6 +221,14 @@ __device__ __forceinline__ void load_q(QRegs<D, G, KV> &qr, const unsigned char 
                 qr.w[g][c] = *reinterpret_cast<const uint4 *>(qs + (g * D + chunk * 8) * 2);
             } else if constexpr (KV == PKV_F32) {
                 qr.w[g][c] = *reinterpret_cast<const float4 *>(qs + (g * D + chunk * 4) * 4);
+            } else if constexpr (KV == PKV_I4) {
+#pragma unroll
+                for (int pr = 0; pr < 16; ++pr) {
+                    const int e0 = g * D + chunk * 32 + 8 * (pr >> 2) + (pr & 3);
+                    const __half2 h = __floats2half2_rn(q_elem(qs, e0, q_dtype),
+                                                        q_elem(qs, e0 + 4, q_dtype));
+                    qr.w[g][c][pr] = *reinterpret_cast<const uint32_t *>(&h);
+                }
             } else {
 #pragma unroll
                 for (int u = 0; u < 16; ++u)
@@ -278,6 +294,18 @@ __device__ __forceinline__ void qk_tile(float (&part)[Cfg<D, G, KV>::NP],
                     a = fmaf(qr.w[g][c].w, kf.w, a);
                     part[ii * G + g] = a;
                 }
+            } else if constexpr (KV == PKV_I4) {
+                const uint32_t wds[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t h = i4pair_to_half2(wds[u], k);   // codes 8u+k, 8u+k+4
+#pragma unroll
+                        for (int g = 0; g < G; ++g)
+                            part[ii * G + g] = fma_f16x2(qr.w[g][c][4 * u + k], h,
+                                                         part[ii * G + g]);
+                    }
             } else {
                 float kf[16];
                 const uint32_t wds[4] = {kw.x ^ 0x80808080u, kw.y ^ 0x80808080u,
@@ -334,8 +362,8 @@ __device__ __forceinline__ void load_v(float (&v)[D / 32], const unsigned char *
                                        int lane)
 {
     constexpr int VE = D / 32;
-    constexpr int ROWB = D * KvBytes<KV>::v;
-    const unsigned char *p = sV + t * ROWB + lane * VE * KvBytes<KV>::v;
+    constexpr int ROWB = D * KvBits<KV>::v / 8;
+    const unsigned char *p = sV + t * ROWB + lane * VE * KvBits<KV>::v / 8;
     if constexpr (KV == PKV_BF16) {
         if constexpr (VE == 4) {
             const uint2 w = *reinterpret_cast<const uint2 *>(p);
@@ -361,6 +389,12 @@ __device__ __forceinline__ void load_v(float (&v)[D / 32], const unsigned char *
             const float2 w = *reinterpret_cast<const float2 *>(p);
             v[0] = w.x; v[1] = w.y;
         }
+    } else if constexpr (KV == PKV_I4) {
+        static_assert(VE == 4, "4-bit rows are d = 128");
+        const uint32_t b = *reinterpret_cast<const uint16_t *>(p);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            v[e] = i4_to_float(b >> (4 * e));
     } else {
         if constexpr (VE == 4) {
             const uint32_t b = *reinterpret_cast<const uint32_t *>(p) ^ 0x80808080u;
@@ -378,7 +412,7 @@ __device__ __forceinline__ void load_v(float (&v)[D / 32], const unsigned char *
 // whole tile into registers and releases the stage before the arithmetic.
 template <int D, int KV>
 struct VRaw {
-    static constexpr int BYTES = (D / 32) * KvBytes<KV>::v;
+    static constexpr int BYTES = (D / 32) * KvBits<KV>::v / 8;
     static constexpr bool IN_REGS = BYTES <= 8;
     using type = typename std::conditional<(BYTES <= 4), uint32_t, uint2>::type;
 };
@@ -388,7 +422,7 @@ __device__ __forceinline__ typename VRaw<D, KV>::type load_v_raw(const unsigned 
                                                                  int lane)
 {
     constexpr int BYTES = VRaw<D, KV>::BYTES;
-    const unsigned char *p = sV + t * D * KvBytes<KV>::v + lane * BYTES;
+    const unsigned char *p = sV + t * (D * KvBits<KV>::v / 8) + lane * BYTES;
     if constexpr (BYTES == 8)
         return *reinterpret_cast<const uint2 *>(p);
     else if constexpr (BYTES == 4)
@@ -418,6 +452,11 @@ __device__ __forceinline__ void unpack_v(float (&v)[D / 32], typename VRaw<D, KV
     } else if constexpr (KV == PKV_F32) {
         static_assert(VE == 2, "fp32 rows of d = 128 are read from shared memory");
         v[0] = __uint_as_float(raw.x); v[1] = __uint_as_float(raw.y);
+    } else if constexpr (KV == PKV_I4) {
+        static_assert(VE == 4, "4-bit rows are d = 128");
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            v[e] = i4_to_float(raw >> (4 * e));
     } else {
         if constexpr (VE == 4) {
             const uint32_t b = raw ^ 0x80808080u;
@@ -657,7 +696,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     for (int u = 0; u < 4; ++u) {
                         if (u < cur.nblk) {
                             if (cur.id[u] >= 0 && cur.id[u] < p.num_blocks)
-                                total += 2 * kv_copy + (KV == PKV_I8 ? 2 * sc_copy : 0);
+                                total += 2 * kv_copy + (quantized(KV) ? 2 * sc_copy : 0);
                             else
                                 bad = true;
                         }
@@ -678,7 +717,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                                           kv_copy, &full[st], policy);
                             bulk_g2s_hint(sV + dst_row * C::ROWB, p.v_cache + row0 * C::ROWB,
                                           kv_copy, &full[st], policy);
-                            if constexpr (KV == PKV_I8) {
+                            if constexpr (quantized(KV)) {
                                 bulk_g2s(sKS + dst_row * 2, p.k_scales + row0, sc_copy, &full[st]);
                                 bulk_g2s(sVS + dst_row * 2, p.v_scales + row0, sc_copy, &full[st]);
                             }
@@ -862,7 +901,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 uint4 kr[C::TPL][C::CPL];
                 load_k<D, G, KV>(kr, sK, tq, ds);
                 float ks_t = 1.0f, vs_t = 1.0f;
-                if constexpr (KV == PKV_I8) {
+                if constexpr (quantized(KV)) {
                     ks_t = __half2float(sKS[t]);
                     vs_t = __half2float(sVS[t]);
                 }
@@ -888,7 +927,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 reduce_scatter<C::NP, C::DS / 2>(part, ds);
                 float s[C::NF];
                 float kscale = p.scale_log2;
-                if constexpr (KV == PKV_I8)
+                if constexpr (quantized(KV))
                     kscale *= ks_t;
                 bool above = false;
 #pragma unroll
@@ -1201,9 +1240,15 @@ template <int KV>
 int launch_d(const pkv_pool *pool, int G, const Params &prm, int batch, int max_seq_len,
              cudaStream_t s)
 {
-    if (pool->head_dim == 64)
-        return launch_g<64, KV>(pool, G, prm, batch, max_seq_len, s);
-    return launch_g<128, KV>(pool, G, prm, batch, max_seq_len, s);
+    if constexpr (KV == PKV_I4) {
+        // a 64-wide 4-bit row is 32 bytes, below the four 16-byte chunks a
+        // row is split into; the pool refuses that shape
+        return launch_g<128, KV>(pool, G, prm, batch, max_seq_len, s);
+    } else {
+        if (pool->head_dim == 64)
+            return launch_g<64, KV>(pool, G, prm, batch, max_seq_len, s);
+        return launch_g<128, KV>(pool, G, prm, batch, max_seq_len, s);
+    }
 }
 
 }  // namespace kern

@@ -224,6 +224,25 @@ __device__ __forceinline__ float i8_to_float(uint32_t biased)
     return __uint_as_float(f) - 8388736.0f;
 }
 
+// 4-bit two's-complement codes, code j of a word in bits 4j..4j+3.
+// Codes k and k+4 -> an fp16 pair, exactly: the biased code (code ^ 8 =
+// code + 8) becomes the low mantissa bits of 1024 (0x6400), and 1032 (0x6408)
+// is subtracted.
+__device__ __forceinline__ uint32_t i4pair_to_half2(uint32_t w, int k)
+{
+    const uint32_t t = ((w >> (4 * k)) & 0x000F000Fu) ^ 0x64086408u;
+    uint32_t h;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(t), "r"(0x64086408u));
+    return h;
+}
+
+// The code in the low 4 bits of x -> float, exactly (biased code in the
+// mantissa of 2^23, minus 2^23 + 8).
+__device__ __forceinline__ float i4_to_float(uint32_t x)
+{
+    return __uint_as_float((x & 0xFu) ^ 0x4B000008u) - 8388616.0f;
+}
+
 // Mixed-precision FMA: fp32 accumulate of the product of two bf16 (or fp16)
 // halves taken from packed words; the product is exact in fp32.
 __device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float c)

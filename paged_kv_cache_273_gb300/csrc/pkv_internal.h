@@ -42,9 +42,19 @@ inline int dtype_bytes(pkv_dtype t)
     case PKV_F32: return 4;
     case PKV_F16: case PKV_BF16: return 2;
     case PKV_I8: return 1;
+    case PKV_I4: return 0;      // two per byte: use row_bytes()
     }
     return 0;
 }
+
+// Bytes of one cached row of head_dim elements (4-bit codes: two per byte).
+inline int64_t row_bytes(pkv_dtype t, int head_dim)
+{
+    return t == PKV_I4 ? head_dim / 2 : (int64_t)head_dim * dtype_bytes(t);
+}
+
+// Caches with one fp16 scale per cached row.
+inline bool quantized_dtype(pkv_dtype t) { return t == PKV_I8 || t == PKV_I4; }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -50,11 +50,14 @@ int kv_block_pool_init(pkv_pool **out, int num_blocks, int block_size, int num_k
         return PKV_ERR_INVALID;
     if ((int64_t)num_blocks * block_size >= ((int64_t)1 << 31))
         return PKV_ERR_INVALID;
-    if (kv_dtype != PKV_F32 && kv_dtype != PKV_F16 && kv_dtype != PKV_BF16 && kv_dtype != PKV_I8)
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_F16 && kv_dtype != PKV_BF16 &&
+        kv_dtype != PKV_I8 && kv_dtype != PKV_I4)
         return PKV_ERR_INVALID;
     if (head_dim != 64 && head_dim != 128)
         return PKV_ERR_UNSUPPORTED;
-    if (block_size < 4 || (kv_dtype == PKV_I8 && block_size < 8))
+    if (kv_dtype == PKV_I4 && head_dim != 128)
+        return PKV_ERR_UNSUPPORTED;
+    if (block_size < 4 || (pkv::quantized_dtype(kv_dtype) && block_size < 8))
         return PKV_ERR_UNSUPPORTED;
 
     pkv_pool *p = new (std::nothrow) pkv_pool;
@@ -105,13 +108,13 @@ size_t kv_cache_bytes(const pkv_pool *pool)
 {
     if (!pool)
         return 0;
-    return (size_t)pool->num_blocks * pool->num_kv_heads * pool->block_size * pool->head_dim *
-           pkv::dtype_bytes(pool->kv_dtype);
+    return (size_t)pool->num_blocks * pool->num_kv_heads * pool->block_size *
+           (size_t)pkv::row_bytes(pool->kv_dtype, pool->head_dim);
 }
 
 size_t kv_scales_bytes(const pkv_pool *pool)
 {
-    if (!pool || pool->kv_dtype != PKV_I8)
+    if (!pool || !pkv::quantized_dtype(pool->kv_dtype))
         return 0;
     return (size_t)pool->num_blocks * pool->num_kv_heads * pool->block_size * 2;
 }
@@ -323,7 +326,7 @@ int kv_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, 
         (reinterpret_cast<uintptr_t>(dst) & 3u) || !pkv::aligned16(k_cache) ||
         !pkv::aligned16(v_cache))
         return PKV_ERR_INVALID;
-    if (pool->kv_dtype == PKV_I8 && (!k_scales || !v_scales ||
+    if (pkv::quantized_dtype(pool->kv_dtype) && (!k_scales || !v_scales ||
                                      (reinterpret_cast<uintptr_t>(k_scales) & 1u) ||
                                      (reinterpret_cast<uintptr_t>(v_scales) & 1u)))
         return PKV_ERR_INVALID;
@@ -339,7 +342,7 @@ int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dt
 {
     if (!pool || num_tokens < 0)
         return PKV_ERR_INVALID;
-    if (pool->kv_dtype == PKV_I8) {
+    if (pkv::quantized_dtype(pool->kv_dtype)) {
         if (in_dtype != PKV_F16 && in_dtype != PKV_BF16 && in_dtype != PKV_F32)
             return PKV_ERR_UNSUPPORTED;
     } else if (in_dtype != pool->kv_dtype) {
@@ -352,7 +355,7 @@ int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dt
     if (!pkv::aligned16(k_new) || !pkv::aligned16(v_new) || !pkv::aligned16(k_cache) ||
         !pkv::aligned16(v_cache) || (reinterpret_cast<uintptr_t>(slot_mapping) & 3u))
         return PKV_ERR_INVALID;
-    if (pool->kv_dtype == PKV_I8 && (!k_scales || !v_scales || !pkv::aligned16(k_scales) ||
+    if (pkv::quantized_dtype(pool->kv_dtype) && (!k_scales || !v_scales || !pkv::aligned16(k_scales) ||
                                      !pkv::aligned16(v_scales)))
         return PKV_ERR_INVALID;
     if (!pool->has_device)
@@ -385,7 +388,7 @@ int decode_call(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_
     int G = num_q_heads / pool->num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8)
         return PKV_ERR_UNSUPPORTED;
-    if (pool->kv_dtype == PKV_I8) {
+    if (pkv::quantized_dtype(pool->kv_dtype)) {
         if (q_dtype != PKV_F16 && q_dtype != PKV_BF16)
             return PKV_ERR_UNSUPPORTED;
     } else if (q_dtype != pool->kv_dtype) {
@@ -402,7 +405,7 @@ int decode_call(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
         (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return PKV_ERR_INVALID;
-    if (pool->kv_dtype == PKV_I8 && (!k_scales || !v_scales || !pkv::aligned16(k_scales) ||
+    if (pkv::quantized_dtype(pool->kv_dtype) && (!k_scales || !v_scales || !pkv::aligned16(k_scales) ||
                                      !pkv::aligned16(v_scales)))
         return PKV_ERR_INVALID;
     if (!pool->has_device)

@@ -23,7 +23,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
-PKV_F32, PKV_F16, PKV_BF16, PKV_I8 = 0, 1, 2, 3
+PKV_F32, PKV_F16, PKV_BF16, PKV_I8, PKV_I4 = 0, 1, 2, 3, 4
 PKV_OK = 0
 PKV_ERR_INVALID = -1
 PKV_ERR_NO_BLOCKS = -2
@@ -35,6 +35,8 @@ PKV_ERR_TIMEOUT = -6
 TORCH_DTYPE = {PKV_F32: torch.float32, PKV_F16: torch.float16, PKV_BF16: torch.bfloat16,
                PKV_I8: torch.int8}
 PKV_DTYPE = {v: k for k, v in TORCH_DTYPE.items()}
+# 4-bit caches are held as bytes, two codes each: [NB, Hkv, bs, D/2] uint8.
+TORCH_DTYPE[PKV_I4] = torch.uint8
 
 # Every symbol the header declares (checked by the tests).
 SYMBOLS = ("pkv_status_string", "kv_block_pool_init", "kv_block_pool_destroy", "kv_cache_bytes",
@@ -178,9 +180,11 @@ class Pool:
     def alloc_cache(self, device="cuda"):
         shape = (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
         dt = TORCH_DTYPE[self.kv_dtype]
+        if self.kv_dtype == PKV_I4:
+            shape = shape[:3] + (self.head_dim // 2,)
         k = torch.zeros(shape, dtype=dt, device=device)
         v = torch.zeros(shape, dtype=dt, device=device)
-        if self.kv_dtype == PKV_I8:
+        if self.kv_dtype in (PKV_I8, PKV_I4):
             sshape = shape[:3]
             return (k, v, torch.zeros(sshape, dtype=torch.float16, device=device),
                     torch.zeros(sshape, dtype=torch.float16, device=device))

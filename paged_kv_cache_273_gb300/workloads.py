@@ -21,7 +21,7 @@ import math
 
 import numpy as np
 
-F32, F16, BF16, I8 = 0, 1, 2, 3
+F32, F16, BF16, I8, I4 = 0, 1, 2, 3, 4
 
 
 @dataclasses.dataclass(frozen=True)
@@ -70,6 +70,11 @@ WORKLOADS = {
     # int8 cache on the Llama-3-8B shape: 128 sequences, lengths uniform in
     # [512, 8192], K/V drawn in fp16 with 1% outliers x8, fp16 q.
     "int8": Workload("int8", 32, 8, 128, 16, 128, I8, F16, F16, 4, "uniform", 512, 8192, 1,
+                     outlier_p=0.01, outlier_scale=8.0),
+    # 4-bit cache on the same shape (a variant beyond the five configurations
+    # above): 64 sequences, lengths uniform in [512, 8192], fp16 rows with 1%
+    # outliers x8, fp16 q.
+    "int4": Workload("int4", 32, 8, 128, 16, 64, I4, F16, F16, 5, "uniform", 512, 8192, 1,
                      outlier_p=0.01, outlier_scale=8.0),
 }
 
@@ -134,12 +139,14 @@ def _lengths(rng: np.random.Generator, wl: Workload) -> np.ndarray:
     raise ValueError(wl.lengths)
 
 
-def make_inputs(wl: Workload | str, lengths=None) -> Inputs:
+def make_inputs(wl: Workload | str, lengths=None, values=True) -> Inputs:
     """Draw the inputs of a workload.
 
     lengths: explicit final lengths (one per sequence) instead of the
     workload's recipe; e.g. (8, 4) for the tiny workload is the reading in
     which 7 and 3 are the lengths before the decode step.
+    values: False skips the K/V rows (lengths, tables and q only), for
+    timing runs that fill the caches on the device.
     """
     if isinstance(wl, str):
         wl = WORKLOADS[wl]
@@ -192,6 +199,11 @@ def make_inputs(wl: Workload | str, lengths=None) -> Inputs:
     offs = np.zeros(B + 1, np.int64)
     offs[1:] = np.cumsum(prefix)
     total = int(offs[-1])
+    if not values:
+        sq = _values(rng, (steps, B, Hq, D), wl.q_dtype)
+        empty = np.zeros((0, Hkv, D), np.float32)
+        return Inputs(wl, num_blocks, final.astype(np.int32), prefix.astype(np.int32), tables,
+                      empty, empty, offs, np.ones(total, bool), empty, empty, sq, sharers, idle)
     hk = _values(rng, (total, Hkv, D), wl.src_dtype, wl.outlier_p, wl.outlier_scale)
     hv = _values(rng, (total, Hkv, D), wl.src_dtype, wl.outlier_p, wl.outlier_scale)
     write = np.ones(total, bool)

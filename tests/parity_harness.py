@@ -20,10 +20,13 @@ from paged_kv_cache_273_gb300 import workloads as W
 # Max-abs attention error allowed against the fp64 oracle: fp32 accumulation
 # over fp32/fp16/bf16 K/V, and int8 K/V (the oracle attends over the same
 # dequantized codes, so the budget covers fp32 rounding only, with margin).
-TOL = {W.F32: 2e-3, W.F16: 2e-3, W.BF16: 2e-3, W.I8: 2e-2}
+TOL = {W.F32: 2e-3, W.F16: 2e-3, W.BF16: 2e-3, W.I8: 2e-2, W.I4: 2e-2}
 
-_NP_RAW = {W.F32: np.float32, W.F16: np.uint16, W.BF16: np.uint16, W.I8: np.int8}
-_TORCH = {W.F32: torch.float32, W.F16: torch.float16, W.BF16: torch.bfloat16, W.I8: torch.int8}
+_NP_RAW = {W.F32: np.float32, W.F16: np.uint16, W.BF16: np.uint16, W.I8: np.int8,
+           W.I4: np.uint8}
+_TORCH = {W.F32: torch.float32, W.F16: torch.float16, W.BF16: torch.bfloat16, W.I8: torch.int8,
+          W.I4: torch.uint8}
+_QUANT = (W.I8, W.I4)
 
 GUARD = 4096  # canary bytes on each side of every guarded buffer
 CANARY = 0x5A
@@ -92,6 +95,9 @@ def _append_oracle(case: Case, rows_k, rows_v, slots):
     if wl.kv_dtype == W.I8:
         O.append_q8(rows_k, rows_v, wl.src_dtype, slots, wl.block_size, case.ok, case.ov,
                     case.oks, case.ovs)
+    elif wl.kv_dtype == W.I4:
+        O.append_q4(rows_k, rows_v, wl.src_dtype, slots, wl.block_size, case.ok, case.ov,
+                    case.oks, case.ovs)
     else:
         O.append(rows_k, rows_v, wl.kv_dtype, slots, wl.block_size, case.ok, case.ov)
 
@@ -102,14 +108,14 @@ def build(inp: W.Inputs, device="cuda") -> Case:
     B, Hq, Hkv, D, bs = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
     NB = inp.num_blocks
     pool = pkv.kv_block_pool_init(NB, bs, Hkv, D, wl.kv_dtype)
-    shape = (NB, Hkv, bs, D)
+    shape = (NB, Hkv, bs, D // 2 if wl.kv_dtype == W.I4 else D)   # 4-bit: two codes a byte
     gk = Guarded(shape, _TORCH[wl.kv_dtype], device)
     gv = Guarded(shape, _TORCH[wl.kv_dtype], device)
     gks = gvs = None
     ok = np.zeros(shape, _NP_RAW[wl.kv_dtype])
     ov = np.zeros(shape, _NP_RAW[wl.kv_dtype])
     oks = ovs = None
-    if wl.kv_dtype == W.I8:
+    if wl.kv_dtype in _QUANT:
         gks = Guarded(shape[:3], torch.float16, device)
         gvs = Guarded(shape[:3], torch.float16, device)
         oks = np.zeros(shape[:3], np.uint16)
@@ -186,7 +192,7 @@ def caches_equal(case: Case) -> bool:
     wl = case.wl
     same = np.array_equal(to_raw(case.gk.tensor, wl.kv_dtype), case.ok) and \
         np.array_equal(to_raw(case.gv.tensor, wl.kv_dtype), case.ov)
-    if wl.kv_dtype == W.I8:
+    if wl.kv_dtype in _QUANT:
         same = same and np.array_equal(to_raw(case.gks.tensor, W.F16), case.oks) and \
             np.array_equal(to_raw(case.gvs.tensor, W.F16), case.ovs)
     return same
