@@ -290,6 +290,49 @@ def time_workload(name: str, dev, stream, peak: float, reps: int = 20) -> dict:
                     "sequence)" % reps}
 
 
+def time_prefill(dev, stream, peak_tflops: float, B=4, n=4096, reps=10) -> dict:
+    """Causal prefill of B prompts of n tokens on the Llama-3-8B head shape
+    (32 q / 8 KV heads, d 128, bf16, block size 16), device-filled caches."""
+    import torch
+    from paged_kv_cache_273_gb300 import pkv
+    Hq, Hkv, D, bs = 32, 8, 128, 16
+    nb = n // bs
+    pool = pkv.kv_block_pool_init(B * nb, bs, Hkv, D, pkv.PKV_BF16)
+    kc, vc, _, _ = pool.alloc_cache(dev)
+    kc.normal_()
+    vc.normal_()
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    tables = torch.randperm(B * nb, device=dev, generator=g).to(torch.int32).reshape(B, nb)
+    qs = torch.arange(0, (B + 1) * n, n, device=dev, dtype=torch.int32)
+    lens = torch.full((B,), n, device=dev, dtype=torch.int32)
+    q = torch.randn((B * n, Hq, D), device=dev).to(torch.bfloat16)
+    out = torch.empty((B * n, Hq, D), device=dev, dtype=torch.float32)
+
+    def call():
+        pkv.paged_prefill_attention(pool, q, kc, vc, tables, qs, lens, D ** -0.5, out, n,
+                                    stream=stream)
+
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pkv.pkv_check_error(pool) != pkv.PKV_OK:
+        raise RuntimeError("device error in the prefill measurement")
+    us = e0.elapsed_time(e1) / reps * 1e3
+    flops = 4.0 * B * (n * (n + 1) / 2) * D * Hq          # QK^T and PV over the causal half
+    tf = flops / (us / 1e6) / 1e12
+    return {"value": tf, "unit": "TFLOP/s", "bound": "tensor", "frac": tf / peak_tflops,
+            "launch_us": us, "flops_per_launch": flops,
+            "config": "%d prompts x %d tokens, causal, 32 q / 8 KV heads, d 128, bf16, "
+                      "block size 16" % (B, n),
+            "note": "mma.sync m16n8k16 bf16 (fp32 accumulate); peak = measured bf16 burst"}
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_gpu(args):
     import torch
@@ -500,6 +543,8 @@ def run_gpu(args):
     if world == 1:
         for name in ("gpt2", "llama2_70b", "int8", "int4"):
             others[name] = time_workload(name, dev, stream, peak)
+    bf16_peak = peaks.get("bf16_tflops") or 1900.0
+    prefill = time_prefill(dev, stream, bf16_peak) if world == 1 else None
 
     traffic = None
     try:
@@ -553,6 +598,7 @@ def run_gpu(args):
                     "note": "same workload, last 1024 rows of each sequence; L2 flushed "
                             "before each call; median of 50"}},
             "other_workloads": others,
+            "prefill": prefill,
             "clocks": clk,
         }
         print(json.dumps(line))

@@ -318,6 +318,39 @@ int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype
                                   size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * paged_prefill_attention — causal attention of a batch of new tokens over
+ * the paged cache: the prefill half of serving ([VIS] "Prefill and decode
+ * feel different": all prompt tokens at once, bound by arithmetic).
+ * Sequence b has n_b = q_start[b+1] - q_start[b] new tokens, the last n_b of
+ * its seq_lens[b] cached rows (their K and V already written by kv_append);
+ * new token i sits at position p = seq_lens[b] - n_b + i and, for each query
+ * head h (KV head h / G),
+ *   out[q_start[b] + i][h] = softmax(scale * q[q_start[b] + i][h] . K^T) . V
+ * over cached positions 0..p ([NOTES] "Concept").  With n_b = seq_lens[b]
+ * this is the prefill of a whole prompt; with fewer it continues a prompt in
+ * chunks, and n_b = 1 is a decode step.
+ *
+ *   q          device [T][Hq][D] of the pool's dtype (F16 or BF16 pools only),
+ *              T = q_start[batch]; sequence-major.
+ *   q_start    device int32 [batch + 1], q_start[0] = 0, non-decreasing.
+ *   seq_lens   device int32 [batch], seq_lens[b] >= n_b.
+ *   block_tables, max_blocks_per_seq  as for paged_decode_attention.
+ *   max_q_len  >= every n_b (sizes the grid; host value, no device read).
+ *   out        device fp32 [T][Hq][D].
+ *
+ * Runs on the tensor cores (mma.sync, fp16/bf16 inputs, fp32 accumulation;
+ * the softmax weights are rounded to the input type for the P.V product).
+ * fp32 and quantized pools return PKV_ERR_UNSUPPORTED.  Lengths or block ids
+ * out of range set PKV_ERR_BAD_INDEX in the error word (those rows are
+ * skipped).  No workspace.
+ */
+int paged_prefill_attention(const pkv_pool *pool, const void *q, int num_q_heads,
+                            const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *q_start, const int32_t *seq_lens, int batch,
+                            int max_q_len, float scale, float *out, pkv_stream_t stream);
+
+/*
  * paged_decode_attention_noalloc — paged_decode_attention for callers that
  * cannot allocate device memory.  The pages have no counterpart; this is a
  * property of this library's interface, not of the method.

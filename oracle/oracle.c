@@ -553,6 +553,74 @@ int orc_paged_decode_attention(const void *q, int q_dtype, int num_q_heads, cons
                                              nthreads);
 }
 
+/* ------------------------------------------------------------------ */
+/* Prefill attention ([VIS] "Prefill and decode feel different": prefill */
+/* handles all prompt tokens at once; [GUIDE] "How the cache turns the   */
+/* loop cheap": prefill computes K and V for the whole prompt and stores */
+/* them).  Sequence b has n_b new tokens, the last n_b of its seq_lens[b] */
+/* cached rows (already appended); new token i sits at position          */
+/* p = seq_lens[b] - n_b + i and attends over positions 0..p (causal),   */
+/* with the softmax of [NOTES] "Concept".  q rows are sequence-major:    */
+/* q[q_start[b] + i][h][:], and so is out.                                */
+/* ------------------------------------------------------------------ */
+int orc_paged_prefill_attention(const void *q, int q_dtype, int num_q_heads, const void *k_cache,
+                                const void *v_cache, int kv_dtype, int num_blocks,
+                                int num_kv_heads, int head_dim, int block_size,
+                                const int32_t *block_tables, int max_blocks_per_seq,
+                                const int32_t *q_start, const int32_t *seq_lens, int batch,
+                                double scale, double *out, int nthreads)
+{
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return -1;
+    int group = num_q_heads / num_kv_heads;
+    for (int b = 0; b < batch; ++b) {
+        int n = q_start[b + 1] - q_start[b];
+        if (n < 0 || seq_lens[b] < n || seq_lens[b] > (int64_t)max_blocks_per_seq * block_size)
+            return -1;
+        int nb = (seq_lens[b] + block_size - 1) / block_size;
+        for (int j = 0; j < nb; ++j) {
+            int32_t id = block_tables[(int64_t)b * max_blocks_per_seq + j];
+            if (id < 0 || id >= num_blocks)
+                return -1;
+        }
+    }
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t item = 0; item < (int64_t)batch * num_kv_heads; ++item) {
+        int b = (int)(item / num_kv_heads);
+        int kvh = (int)(item % num_kv_heads);
+        int L = seq_lens[b];
+        int n = q_start[b + 1] - q_start[b];
+        const int32_t *row = block_tables + (int64_t)b * max_blocks_per_seq;
+        double *kr = (double *)malloc(sizeof(double) * ((size_t)L * head_dim + 1));
+        double *vr = (double *)malloc(sizeof(double) * ((size_t)L * head_dim + 1));
+        double *sc = (double *)malloc(sizeof(double) * ((size_t)L + 1));
+        double *qd = (double *)malloc(sizeof(double) * head_dim);
+        orc_gather(k_cache, NULL, kv_dtype, row, L, kvh, num_kv_heads, head_dim, block_size, kr);
+        orc_gather(v_cache, NULL, kv_dtype, row, L, kvh, num_kv_heads, head_dim, block_size, vr);
+        for (int i = 0; i < n; ++i) {
+            int p = L - n + i;
+            for (int g = 0; g < group; ++g) {
+                int h = kvh * group + g;
+                int64_t qb = ((int64_t)(q_start[b] + i) * num_q_heads + h) * head_dim;
+                for (int d = 0; d < head_dim; ++d)
+                    qd[d] = load_elem(q, q_dtype, qb + d);
+                orc_attend_rows(qd, kr, vr, p + 1, head_dim, scale, out + qb, sc);
+            }
+        }
+        free(kr);
+        free(vr);
+        free(sc);
+        free(qd);
+    }
+    return 0;
+}
+
 int orc_max_threads(void)
 {
 #ifdef _OPENMP

@@ -87,6 +87,9 @@ def _load():
         lib.orc_paged_decode_attention_window.argtypes = [P, I, I, P, P, P, P, I, I, I, I, I, P,
                                                           I, P, I, I, D, P, I]
         lib.orc_paged_decode_attention_window.restype = I
+        lib.orc_paged_prefill_attention.argtypes = [P, I, I, P, P, I, I, I, I, I, P, I, P, P, I,
+                                                    D, P, I]
+        lib.orc_paged_prefill_attention.restype = I
         lib.orc_max_threads.argtypes = []
         lib.orc_max_threads.restype = I
         lib.orc_kv_bytes_per_token.argtypes = [I64, I64, I64, I64]
@@ -288,6 +291,35 @@ def paged_decode_attention(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
                                                 float(scale), _ptr(out), int(nthreads))
     if rc != 0:
         raise ValueError("oracle: block table entry or sequence length out of range")
+    return out
+
+
+def paged_prefill_attention(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, q_start,
+                            seq_lens, scale, nthreads=0):
+    """fp64 causal attention of the new tokens of every sequence over its cached rows.
+
+    q: [T, Hq, D] raw, sequence-major (sequence b's tokens at q_start[b] ..
+    q_start[b+1]-1, the last ones of its seq_lens[b] cached rows); returns
+    out [T, Hq, D] float64.
+    """
+    q = _c(q, _NP_OF[q_dtype])
+    k_cache = np.ascontiguousarray(k_cache)
+    v_cache = np.ascontiguousarray(v_cache)
+    NB, Hkv, bs, D = k_cache.shape
+    T, Hq, Dq = q.shape
+    assert Dq == D
+    bt = _c(block_tables, np.int32)
+    qs = _c(q_start, np.int32)
+    sl = _c(seq_lens, np.int32)
+    B = sl.size
+    assert qs.size == B + 1 and qs[-1] == T
+    out = np.zeros((T, Hq, D), np.float64)
+    rc = _load().orc_paged_prefill_attention(_ptr(q), q_dtype, Hq, _ptr(k_cache), _ptr(v_cache),
+                                             kv_dtype, NB, Hkv, D, bs, _ptr(bt), bt.shape[1],
+                                             _ptr(qs), _ptr(sl), B, float(scale), _ptr(out),
+                                             int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle: block table entry or length out of range")
     return out
 
 

@@ -59,6 +59,10 @@ inline bool quantized_dtype(pkv_dtype t) { return t == PKV_I8 || t == PKV_I4; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launchers (defined in the .cu files).  They assume validated arguments.
+int launch_prefill(const pkv_pool *pool, const void *q, int num_q_heads, const void *k_cache,
+                   const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                   const int32_t *q_start, const int32_t *seq_lens, int batch, int max_q_len,
+                   float scale, float *out, pkv_stream_t stream);
 int launch_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, int n,
                       void *k_cache, void *v_cache, void *k_scales, void *v_scales,
                       pkv_stream_t stream);

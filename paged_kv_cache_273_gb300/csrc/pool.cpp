@@ -445,6 +445,36 @@ int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype
                        scale, out, workspace, workspace_bytes, stream);
 }
 
+int paged_prefill_attention(const pkv_pool *pool, const void *q, int num_q_heads,
+                            const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *q_start, const int32_t *seq_lens, int batch,
+                            int max_q_len, float scale, float *out, pkv_stream_t stream)
+{
+    if (!pool || batch < 0 || max_blocks_per_seq < 0 || max_q_len < 0 || num_q_heads < 1 ||
+        num_q_heads % pool->num_kv_heads != 0)
+        return PKV_ERR_INVALID;
+    if (pool->kv_dtype != PKV_F16 && pool->kv_dtype != PKV_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    if (batch > 65535 || num_q_heads > 65535)
+        return PKV_ERR_UNSUPPORTED;
+    if (batch == 0 || max_q_len == 0)
+        return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !q_start || !seq_lens || !out)
+        return PKV_ERR_INVALID;
+    if (!pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(out) & 7u) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(q_start) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return PKV_ERR_INVALID;
+    if (!pool->has_device)
+        return PKV_ERR_CUDA;
+    return pkv::launch_prefill(pool, q, num_q_heads, k_cache, v_cache, block_tables,
+                               max_blocks_per_seq, q_start, seq_lens, batch, max_q_len, scale,
+                               out, stream);
+}
+
 int pkv_check_error(const pkv_pool *pool, pkv_stream_t stream)
 {
     if (!pool)

@@ -43,7 +43,8 @@ SYMBOLS = ("pkv_status_string", "kv_block_pool_init", "kv_block_pool_destroy", "
            "kv_scales_bytes", "kv_num_free_blocks", "kv_block_refcount", "kv_block_alloc",
            "kv_block_share", "kv_block_free", "kv_reserve_slots", "kv_reserve_slots_cow",
            "kv_slot_mapping", "kv_append", "kv_block_copy", "paged_decode_workspace_bytes", "paged_decode_attention",
-           "paged_decode_attention_window", "paged_decode_attention_noalloc", "pkv_check_error")
+           "paged_decode_attention_window", "paged_prefill_attention",
+           "paged_decode_attention_noalloc", "pkv_check_error")
 
 
 class PkvError(RuntimeError):
@@ -107,6 +108,8 @@ def load() -> ctypes.CDLL:
         lib.paged_decode_attention_window.argtypes = [P, P, I, I, P, P, P, P, P, I, P, I, I, I,
                                                       F, P, P, SZ, P]
         lib.paged_decode_attention_window.restype = I
+        lib.paged_prefill_attention.argtypes = [P, P, I, P, P, P, I, P, P, I, I, F, P, P]
+        lib.paged_prefill_attention.restype = I
         lib.paged_decode_attention_noalloc.argtypes = [P, P, I, I, P, P, P, P, P, I, P, I, I, F,
                                                        P, P]
         lib.paged_decode_attention_noalloc.restype = I
@@ -350,6 +353,21 @@ def paged_decode_attention_window(pool: Pool, q, k_cache, v_cache, block_tables,
         _dptr(seq_lens), B, int(max_seq_len), int(window), float(scale), _dptr(out),
         _dptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
         "paged_decode_attention_window")
+
+
+def paged_prefill_attention(pool: Pool, q, k_cache, v_cache, block_tables, q_start, seq_lens,
+                            scale: float, out, max_q_len: int, stream=None) -> None:
+    """Causal attention of the new tokens (q: [T, Hq, D], sequence-major, offsets
+    q_start [B+1]) over their cached rows; out fp32 [T, Hq, D]."""
+    if out.dtype != torch.float32:
+        raise ValueError("out must be float32")
+    for t in (block_tables, q_start, seq_lens):
+        if t.dtype != torch.int32:
+            raise ValueError("block_tables, q_start and seq_lens must be int32")
+    _check(load().paged_prefill_attention(
+        pool.handle, _dptr(q), q.shape[1], _dptr(k_cache), _dptr(v_cache), _dptr(block_tables),
+        block_tables.shape[1], _dptr(q_start), _dptr(seq_lens), seq_lens.numel(), int(max_q_len),
+        float(scale), _dptr(out), _stream(stream)), "paged_prefill_attention")
 
 
 def paged_decode_attention_noalloc(pool: Pool, q, k_cache, v_cache, block_tables, seq_lens,

@@ -1,0 +1,171 @@
+"""Prefill attention over the paged cache: oracle pins (CPU) and GPU parity.
+
+[VIS] "Prefill and decode feel different": prefill handles all prompt tokens
+at once.  Each new token attends causally over the cached rows up to its own
+position, with the softmax of [NOTES] "Concept"; the new tokens' K and V are
+already in the cache (kv_append with T > 1).
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+
+
+def _case(rng, news, cached, H=2, G=2, D=16, bs=4, dtype=np.float32):
+    """Caches holding each sequence's rows; q for its last `news[b]` tokens."""
+    B = len(news)
+    lens = [c + n for c, n in zip(cached, news)]
+    maxb = max(1, max(-(-L // bs) for L in lens))
+    NB = B * maxb + 2
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = perm[:B * maxb].reshape(B, maxb).copy()
+    kc = rng.standard_normal((NB, H, bs, D)).astype(dtype)
+    vc = rng.standard_normal((NB, H, bs, D)).astype(dtype)
+    qs = np.zeros(B + 1, np.int32)
+    qs[1:] = np.cumsum(news)
+    q = rng.standard_normal((int(qs[-1]), H * G, D)).astype(dtype)
+    return q, kc, vc, tables, qs, np.array(lens, np.int32)
+
+
+def _brute(q, kc, vc, table, L, n, h, G, bs, scale):
+    """Written separately: for every new token, walk the table up to its
+    position, score, exponentiate, normalise."""
+    outs = []
+    for i in range(n):
+        p = L - n + i
+        keys, vals = [], []
+        for pos in range(p + 1):
+            blk, off = table[pos // bs], pos % bs
+            keys.append([float(x) for x in kc[blk, h // G, off]])
+            vals.append([float(x) for x in vc[blk, h // G, off]])
+        qq = [float(x) for x in q[i, h]]
+        sc = [scale * sum(a * b for a, b in zip(qq, k)) for k in keys]
+        top = max(sc)
+        w = [math.exp(s - top) for s in sc]
+        z = sum(w)
+        outs.append([sum(w[t] * vals[t][d] for t in range(p + 1)) / z for d in range(len(qq))])
+    return np.array(outs)
+
+
+def test_prefill_matches_brute_force():
+    rng = np.random.default_rng(70)
+    G, bs = 2, 4
+    q, kc, vc, tb, qs, lens = _case(rng, news=[5, 1, 7], cached=[0, 6, 3], G=G, bs=bs)
+    out = O.paged_prefill_attention(q, O.F32, kc, vc, O.F32, tb, qs, lens, 0.3)
+    for b in range(3):
+        n = qs[b + 1] - qs[b]
+        for h in range(q.shape[1]):
+            ref = _brute(q[qs[b]:qs[b + 1]], kc, vc, tb[b], lens[b], n, h, G, bs, 0.3)
+            assert np.max(np.abs(out[qs[b]:qs[b + 1], h] - ref)) <= 1e-12
+
+
+def test_last_new_token_is_the_decode_step():
+    rng = np.random.default_rng(71)
+    q, kc, vc, tb, qs, lens = _case(rng, news=[9, 4], cached=[3, 12])
+    out = O.paged_prefill_attention(q, O.F32, kc, vc, O.F32, tb, qs, lens, 0.25)
+    dec = O.paged_decode_attention(q[qs[1:] - 1], O.F32, kc, vc, O.F32, tb, lens, 0.25)
+    assert np.array_equal(out[qs[1:] - 1], dec)
+
+
+def test_first_token_of_a_fresh_prompt_returns_its_value():
+    rng = np.random.default_rng(72)
+    G, bs = 2, 4
+    q, kc, vc, tb, qs, lens = _case(rng, news=[6], cached=[0], G=G, bs=bs)
+    out = O.paged_prefill_attention(q, O.F32, kc, vc, O.F32, tb, qs, lens, 0.5)
+    for h in range(q.shape[1]):
+        assert np.array_equal(out[0, h], vc[tb[0, 0], h // G, 0].astype(np.float64))
+
+
+def test_prefill_is_causal():
+    rng = np.random.default_rng(73)
+    bs = 4
+    q, kc, vc, tb, qs, lens = _case(rng, news=[10], cached=[2], bs=bs)
+    out = O.paged_prefill_attention(q, O.F32, kc, vc, O.F32, tb, qs, lens, 0.3)
+    # rows after position 7 (the 6th new token) are rewritten
+    kc2, vc2 = kc.copy(), vc.copy()
+    for pos in range(8, 12):
+        kc2[tb[0, pos // bs], :, pos % bs] += 3.0
+        vc2[tb[0, pos // bs], :, pos % bs] -= 2.0
+    out2 = O.paged_prefill_attention(q, O.F32, kc2, vc2, O.F32, tb, qs, lens, 0.3)
+    assert np.array_equal(out2[:6], out[:6])          # positions 2..7 cannot see them
+    assert not np.array_equal(out2[6:], out[6:])
+
+
+def test_chunked_prefill_equals_prefill_at_once():
+    rng = np.random.default_rng(74)
+    q, kc, vc, tb, qs, lens = _case(rng, news=[40], cached=[0])
+    once = O.paged_prefill_attention(q, O.F32, kc, vc, O.F32, tb, qs, lens, 0.2)
+    a = O.paged_prefill_attention(q[:25], O.F32, kc, vc, O.F32, tb, [0, 25], [25], 0.2)
+    b = O.paged_prefill_attention(q[25:], O.F32, kc, vc, O.F32, tb, [0, 15], [40], 0.2)
+    assert np.array_equal(np.concatenate([a, b]), once)
+
+
+# ------------------------------------------------------------------ GPU parity
+# Tolerance, from the arithmetic: scores are exact products summed in fp32;
+# the weights p are rounded to the input type for the P.V product, a relative
+# error of at most 2^-11 (fp16) or 2^-8 (bf16) per weight against an fp32
+# denominator, so the output can move by that fraction of max |v| (about 4
+# for N(0,1) values): ~2e-3 for fp16, ~1.6e-2 worst case for bf16, in
+# practice far less since the rounding errors do not line up.
+PREFILL_TOL = {"f16": 2e-3, "bf16": 1e-2}
+
+
+def _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, seed):
+    import torch
+    from paged_kv_cache_273_gb300 import pkv
+    import parity_harness as PH
+    from paged_kv_cache_273_gb300 import workloads as W
+    code = {"f16": W.F16, "bf16": W.BF16}[dt]
+    rng = np.random.default_rng(seed)
+    dev = torch.device("cuda", 0)
+    B = len(news)
+    lens = np.array([c + n for c, n in zip(cached, news)], np.int32)
+    maxb = max(-(-int(L) // bs) for L in lens)
+    NB = B * maxb + 5
+    tables = rng.permutation(NB)[:B * maxb].astype(np.int32).reshape(B, maxb)
+    pool = pkv.kv_block_pool_init(NB, bs, Hkv, D, code)
+    gk = PH.Guarded((NB, Hkv, bs, D), PH._TORCH[code])
+    gv = PH.Guarded((NB, Hkv, bs, D), PH._TORCH[code])
+    ok = np.zeros((NB, Hkv, bs, D), np.uint16)
+    ov = np.zeros_like(ok)
+    total = int(lens.sum())
+    rows_k = W._values(rng, (total, Hkv, D), code)
+    rows_v = W._values(rng, (total, Hkv, D), code)
+    slots = pkv.kv_slot_mapping(tables, bs, np.zeros(B, np.int32), lens)
+    pkv.kv_append(pool, PH.to_device(rows_k, code), PH.to_device(rows_v, code),
+                  torch.from_numpy(slots).to(dev), gk.tensor, gv.tensor)
+    O.append(rows_k, rows_v, code, slots, bs, ok, ov)
+    qs = np.zeros(B + 1, np.int32)
+    qs[1:] = np.cumsum(news)
+    q = W._values(rng, (int(qs[-1]), Hq, D), code)
+    out = torch.full((int(qs[-1]), Hq, D), float("nan"), dtype=torch.float32, device=dev)
+    scale = 1.0 / np.sqrt(D)
+    pkv.paged_prefill_attention(pool, PH.to_device(q, code), gk.tensor, gv.tensor,
+                                torch.from_numpy(tables).to(dev), torch.from_numpy(qs).to(dev),
+                                torch.from_numpy(lens).to(dev), scale, out, max(news))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    want = O.paged_prefill_attention(q, code, ok, ov, code, tables, qs, lens,
+                                     float(np.float32(scale)))
+    same_cache = np.array_equal(PH.to_raw(gk.tensor, code), ok) and \
+        np.array_equal(PH.to_raw(gv.tensor, code), ov)
+    return float(np.max(np.abs(got - want))), pkv.pkv_check_error(pool), same_cache, \
+        gk.intact() and gv.intact()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dt,D,Hq,Hkv,bs,news,cached", [
+    ("bf16", 128, 8, 2, 16, [200, 70, 1], [0, 263, 76]),
+    ("f16", 64, 4, 4, 4, [64, 33, 130], [0, 10, 5]),
+    ("bf16", 128, 32, 8, 16, [1000], [0]),
+    ("f16", 128, 16, 2, 32, [129, 5, 64], [0, 300, 64]),
+    ("f16", 128, 8, 8, 16, [1], [1]),
+])
+def test_gpu_prefill_matches_oracle(dt, D, Hq, Hkv, bs, news, cached):
+    from paged_kv_cache_273_gb300 import pkv
+    err, status, same_cache, intact = _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, 80)
+    assert same_cache and intact
+    assert status == pkv.PKV_OK
+    assert err <= PREFILL_TOL[dt], err
