@@ -330,7 +330,8 @@ def time_prefill(dev, stream, peak_tflops: float, B=4, n=4096, reps=10) -> dict:
             "launch_us": us, "flops_per_launch": flops,
             "config": "%d prompts x %d tokens, causal, 32 q / 8 KV heads, d 128, bf16, "
                       "block size 16" % (B, n),
-            "note": "mma.sync m16n8k16 bf16 (fp32 accumulate); peak = measured bf16 burst"}
+            "note": "tcgen05.mma kind::f16, bf16 in, fp32 accumulators in tensor memory; "
+                    "peak = measured bf16 burst"}
 
 
 # ------------------------------------------------------------------ GPU arm

@@ -338,8 +338,9 @@ int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype
  *   max_q_len  >= every n_b (sizes the grid; host value, no device read).
  *   out        device fp32 [T][Hq][D].
  *
- * Runs on the tensor cores (mma.sync, fp16/bf16 inputs, fp32 accumulation;
- * the softmax weights are rounded to the input type for the P.V product).
+ * Runs on the fifth-generation tensor cores (tcgen05.mma, fp16/bf16 inputs,
+ * fp32 accumulators in tensor memory; the softmax weights are rounded to the
+ * input type for the P.V product).  Head dim 64 or 128.
  * fp32 and quantized pools return PKV_ERR_UNSUPPORTED.  Lengths or block ids
  * out of range set PKV_ERR_BAD_INDEX in the error word (those rows are
  * skipped).  No workspace.

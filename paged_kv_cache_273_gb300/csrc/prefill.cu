@@ -3,18 +3,11 @@
 //
 // KV cache visualization page, "Prefill and decode feel different": prefill
 // handles all prompt tokens at once and is bound by arithmetic, not by bytes,
-// so it runs on the tensor cores.  Token i of the n_b new tokens of sequence
-// b sits at position p = seq_lens[b] - n_b + i and attends over positions
-// 0..p ("KV cache: the engine behind fast LLM inference", "Concept").
-//
-// FlashAttention-style tiles ("Flash attention: don't build the giant
-// matrix" in the guide): a CTA of 4 warps takes 64 queries of one (sequence,
-// query head); each warp owns 16 query rows.  Key tiles of 64 rows stream
-// through shared memory (16-byte async copies, each row found through the
-// block table, double buffered); S = Q K^T and O += P V run as
-// mma.sync m16n8k16 (fp16 or bf16 in, fp32 accumulate), the online softmax
-// stays in registers and P is fed back as the A operand without a trip
-// through shared memory.
+// so it runs on the fifth-generation tensor cores.  Token i of the n_b new
+// tokens of sequence b sits at position p = seq_lens[b] - n_b + i and attends
+// over positions 0..p ("KV cache: the engine behind fast LLM inference",
+// "Concept"), in FlashAttention-style tiles that never hold the whole score
+// matrix ("Flash attention: don't build the giant matrix" in the guide).
 
 #include <cuda_runtime.h>
 
@@ -24,18 +17,6 @@ namespace pkv {
 namespace {
 
 using namespace dev;
-
-constexpr int BQ = 64;         // queries per CTA
-constexpr int BK = 64;         // keys per tile
-constexpr int NWARP = 4;
-
-template <int D>
-struct PCfg {
-    static constexpr int LD = D + 8;                 // padded smem row (elements): conflict-free ldmatrix
-    static constexpr int TILE_ELEMS = 64 * LD;
-    static constexpr int SMEM_BYTES = (1 + 2 * 2) * TILE_ELEMS * 2;   // Q, K x2, V x2
-    static constexpr int CHUNKS = D / 8;             // 16-byte chunks per row
-};
 
 template <typename T> struct MmaType;
 template <> struct MmaType<__half> { static constexpr bool bf16 = false; };
@@ -51,39 +32,6 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool va
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_addr(p)));
-}
-
-// d (16x8 fp32) += a (16x16) * b (16x8), row.col.
-template <bool BF16>
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1)
-{
-    if constexpr (BF16) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-            "{%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    } else {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-            "{%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    }
-}
 
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
@@ -110,55 +58,189 @@ struct PrefillParams {
     float scale_log2;
 };
 
-template <int D, typename T>
-__global__ void __launch_bounds__(NWARP * 32) paged_prefill_kernel(const PrefillParams p)
+// ---- tcgen05: 128 queries x 64 keys per step
+//
+// A CTA of 4 warps takes 128 queries of one (sequence, query head); thread
+// t owns query row t; two CTAs share an SM.  Q, K and V tiles are brought
+// by 16-byte cp.async copies (each key row located through the block table)
+// into shared memory in the tensor cores' core-matrix layout (8 rows x 16
+// bytes per 128-byte core matrix, no swizzle), K/V double buffered.  S = Q K^T
+// (M 128, N 64, K = D) and O += P V (M 128, N = D, K 64) are single-thread
+// tcgen05.mma issues with fp32 accumulators in tensor memory: S in columns
+// [0, 64), O in [64, 64 + D).  Each thread reads its S row with tcgen05.ld,
+// does the online softmax for it, writes its P row (fp16/bf16) back to
+// shared memory as the next A operand, and rescales its O row in tensor
+// memory when its maximum moved by more than 2^8.
+
+constexpr int TBQ = 128, TBK = 64;
+
+template <int D>
+struct TcCfg {
+    static constexpr int Q_BYTES = TBQ * D * 2;
+    static constexpr int KV_BYTES = TBK * D * 2;
+    static constexpr int P_BYTES = TBQ * TBK * 2;
+    static constexpr int SMEM_BYTES = Q_BYTES + 4 * KV_BYTES + P_BYTES + 64;
+    static constexpr int TMEM_COLS = 256;          // S: 64 columns, O: D <= 128 columns
+};
+
+// Byte offset of the 16-byte chunk c (8 elements along the contiguous
+// dimension) of row r in a core-matrix tile whose rows hold `chunks` chunks.
+__device__ __forceinline__ uint32_t core_off(int r, int c, int chunks)
 {
-    using C = PCfg<D>;
-    constexpr bool BF16 = MmaType<T>::bf16;
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    T *sQ = reinterpret_cast<T *>(smem_raw);
-    T *sK = sQ + C::TILE_ELEMS;                 // two buffers
-    T *sV = sK + 2 * C::TILE_ELEMS;             // two buffers
+    return (uint32_t)(((r >> 3) * chunks + c) * 128 + (r & 7) * 16);
+}
+
+// Shared-memory matrix descriptor: start, stride between core matrices along
+// K (lbo) and along M/N (sbo), descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulate, A/B fp16 (0) or
+// bf16 (1), A K-major, B K-major (b_mn = 0) or MN-major (1), N, M = 128.
+__device__ __forceinline__ uint32_t umma_idesc(uint32_t ab, uint32_t b_mn, uint32_t n)
+{
+    return (1u << 4) | (ab << 7) | (ab << 10) | (b_mn << 16) | ((n >> 3) << 17) |
+           ((uint32_t)(TBQ >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+                 "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+// 2^x with the hardware approximation (-inf -> +0).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+                 "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+                   "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+                   "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+                   "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+                   "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+                 "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+                 "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+                 "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+                 "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+                 "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+                 "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+                 "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+                 "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+                 "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillParams p)
+{
+    using C = TcCfg<D>;
+    constexpr uint32_t AB = MmaType<T>::bf16 ? 1u : 0u;
+    constexpr int DCH = D / 8;                    // 16-byte chunks of a D-wide row
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sQ = smem_raw;
+    unsigned char *sK = sQ + C::Q_BYTES;          // two buffers
+    unsigned char *sV = sK + 2 * C::KV_BYTES;     // two buffers
+    unsigned char *sP = sV + 2 * C::KV_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sP + C::P_BYTES);   // [0] S done, [2] O done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     grid_dependency_wait();
     grid_dependents_launch();
 
     const int b = blockIdx.z;
     const int h = blockIdx.y;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // long (late) query tiles first
+    const int qt = gridDim.x - 1 - blockIdx.x;    // long (late) query tiles first
     const int q0 = __ldg(p.q_start + b);
     const int n = __ldg(p.q_start + b + 1) - q0;
     const int L = __ldg(p.seq_lens + b);
-    if (qt * BQ >= n)
+    if (qt * TBQ >= n)
         return;
-    if (n < 0 || L < n || L > p.max_blocks_per_seq * p.block_size) {
+    if (L < n || L > p.max_blocks_per_seq * p.block_size) {
         if (threadIdx.x == 0 && qt == 0 && h == 0)
             atomicOr(p.err, PKV_EBIT_SEQLEN);
         return;
     }
     const int G = p.num_q_heads / p.num_kv_heads;
     const int kvh = h / G;
-    const int base = L - n;                        // position of new token 0
-    const int rows = min(BQ, n - qt * BQ);         // valid query rows of this tile
-    const int last_pos = base + qt * BQ + rows - 1;
-    const int ntiles = last_pos / BK + 1;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int base = L - n;
+    const int rows = min(TBQ, n - qt * TBQ);
+    const int first_pos = base + qt * TBQ;        // position of this CTA's first query
+    const int last_pos = first_pos + rows - 1;
+    const int ntiles = last_pos / TBK + 1;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int32_t *table = p.block_tables + (int64_t)b * p.max_blocks_per_seq;
     const T *qg = static_cast<const T *>(p.q);
     const T *kg = static_cast<const T *>(p.k_cache);
     const T *vg = static_cast<const T *>(p.v_cache);
 
-    // ---- async loads: Q once, K/V tiles double buffered
-    for (int idx = tid; idx < BQ * C::CHUNKS; idx += NWARP * 32) {
-        const int r = idx / C::CHUNKS, c = idx % C::CHUNKS;
-        const bool ok = r < rows;
-        const T *src = qg + ((int64_t)(q0 + qt * BQ + (ok ? r : 0)) * p.num_q_heads + h) * D + c * 8;
-        cp_async16(sQ + r * C::LD + c * 8, src, ok);
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
+        *abort_flag = 0;
+        mbar_fence_init();
     }
-    auto load_kv = [&](int kt, int buf) {
-        for (int idx = tid; idx < BK * C::CHUNKS; idx += NWARP * 32) {
-            const int r = idx / C::CHUNKS, c = idx % C::CHUNKS;
-            const int pos = kt * BK + r;
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "n"(C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+
+    // ---- async loads into the core-matrix layout
+    for (int idx = tid; idx < TBQ * DCH; idx += 128) {
+        const int r = idx / DCH, c = idx % DCH;
+        const bool ok = r < rows;
+        const T *src = qg + ((int64_t)(q0 + qt * TBQ + (ok ? r : 0)) * p.num_q_heads + h) * D + c * 8;
+        cp_async16(sQ + core_off(r, c, DCH), src, ok);
+    }
+    // K or V rows of key tile kt into buffer buf
+    auto load_rows = [&](const T *src_cache, unsigned char *dst_tile, int kt) {
+        for (int idx = tid; idx < TBK * DCH; idx += 128) {
+            const int r = idx / DCH, c = idx % DCH;
+            const int pos = kt * TBK + r;
             bool ok = pos <= last_pos;
             int64_t row = 0;
             if (ok) {
@@ -170,155 +252,174 @@ __global__ void __launch_bounds__(NWARP * 32) paged_prefill_kernel(const Prefill
                     row = ((int64_t)blk * p.num_kv_heads + kvh) * p.block_size + pos % p.block_size;
                 }
             }
-            cp_async16(sK + buf * C::TILE_ELEMS + r * C::LD + c * 8, kg + row * D + c * 8, ok);
-            cp_async16(sV + buf * C::TILE_ELEMS + r * C::LD + c * 8, vg + row * D + c * 8, ok);
+            cp_async16(dst_tile + core_off(r, c, DCH), src_cache + row * D + c * 8, ok);
         }
     };
-    load_kv(0, 0);
-    cp_async_commit();
+    load_rows(kg, sK, 0);
+    load_rows(vg, sV, 0);
+    cp_async_commit();                            // group: Q, K0, V0
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_s = tmem;                 // S: columns [0, 64)
+    const uint32_t tmem_o = tmem + TBK;           // O: columns [64, 64 + D)
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t idesc_s = umma_idesc(AB, 0u, TBK);
+    const uint32_t idesc_o = umma_idesc(AB, 1u, D);
+    const uint32_t sQa = smem_addr(sQ), sKa = smem_addr(sK), sVa = smem_addr(sV), sPa = smem_addr(sP);
 
-    // Per thread: query rows r0 = 16*warp + lane/4 and r0 + 8.
-    const int r0 = warp * 16 + (lane >> 2);
-    const int qpos0 = base + qt * BQ + min(r0, rows - 1);        // padding rows copy a valid one
-    const int qpos1 = base + qt * BQ + min(r0 + 8, rows - 1);
-
-    float o[D / 8][4];
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j)
-        o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    uint32_t qf[D / 16][4];
+    const int r = tid;                             // this thread's query row
+    const int qpos = first_pos + min(r, rows - 1);
+    float m_run = -INFINITY, l_run = 0.0f;
+    auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
+        if (!mbar_wait_bounded(bar, parity, abort_flag) && !*abort_flag) {
+            *abort_flag = 1;
+            atomicOr(p.err, PKV_EBIT_TIMEOUT);
+        }
+    };
 
     for (int kt = 0; kt < ntiles; ++kt) {
         const int buf = kt & 1;
+        // K/V of the next tile go to the other buffer, which P.V(kt-1) (waited
+        // below in the previous round) was the last to read
         if (kt + 1 < ntiles) {
-            load_kv(kt + 1, buf ^ 1);
+            load_rows(kg, sK + (buf ^ 1) * C::KV_BYTES, kt + 1);
+            load_rows(vg, sV + (buf ^ 1) * C::KV_BYTES, kt + 1);
             cp_async_commit();
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
         __syncthreads();
-        if (kt == 0) {
-            // Q fragments: rows 16*warp .. +15, all of D, kept in registers
+        tc_fence_after();
+        // S = Q K^T.  Q and K tiles are K-major with DCH chunks a row:
+        // K-direction core stride 128 B, row-group stride DCH*128 B; a K = 16
+        // step is two chunks.
+        if (tid == 0 && !*abort_flag) {
+            const uint32_t kb = sKa + buf * C::KV_BYTES;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-                ldsm_x4(qf[ks], sQ + (warp * 16 + (lane & 15)) * C::LD + ks * 16 + (lane >> 4) * 8);
+                umma_f16(tmem_s, umma_desc(sQa + ks * 256, 128, DCH * 128),
+                         umma_desc(kb + ks * 256, 128, DCH * 128), idesc_s, ks > 0 ? 1u : 0u);
+            umma_commit(&bars[0]);
         }
-        const T *Kt = sK + buf * C::TILE_ELEMS;
-        const T *Vt = sV + buf * C::TILE_ELEMS;
+        wait_bar(&bars[0], (uint32_t)(kt & 1));
+        tc_fence_after();
 
-        // ---- S = Q K^T for 64 keys: 8 n-tiles of 8 keys
-        float s[8][4];
+        // ---- this row's scores in the log2 domain, masked where the tile
+        // crosses the diagonal
+        float v[TBK];
+        tmem_ld32(tmem_s + lane_base, *reinterpret_cast<float(*)[32]>(&v[0]));
+        tmem_ld32(tmem_s + lane_base + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+        const bool diag = kt * TBK + TBK - 1 > first_pos;
+        float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
+        for (int j = 0; j < TBK; ++j) {
+            v[j] *= p.scale_log2;
+            if (diag && kt * TBK + j > qpos)
+                v[j] = -INFINITY;
+            mx = fmaxf(mx, v[j]);
+        }
+        // The running maximum moves only when a score exceeds it by more
+        // than 2^8 (or on the first tile): below that the weights stay
+        // <= 256, exact in fp32 and representable in fp16/bf16, and the
+        // final division by the sum of the same weights is unchanged.
+        const bool move = kt == 0 || mx > m_run + 8.0f;
+        const float m_new = move ? fmaxf(m_run, mx) : m_run;
+        const float corr = kt == 0 ? 1.0f : ex2_approx(m_run - m_new);
+        m_run = m_new;
+        float sum = 0.0f;
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {          // pairs of n-tiles (16 keys)
+        for (int j = 0; j < TBK; j += 8) {
+            uint32_t w[4];
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                uint32_t kb[4];
-                ldsm_x4(kb, Kt + (np * 16 + (lane & 7) + ((lane >> 4) << 3)) * C::LD + ks * 16 +
-                                ((lane >> 3) & 1) * 8);
-                mma16816<BF16>(s[2 * np], qf[ks], kb[0], kb[1]);
-                mma16816<BF16>(s[2 * np + 1], qf[ks], kb[2], kb[3]);
+            for (int u = 0; u < 4; ++u) {
+                const float p0 = ex2_approx(v[j + 2 * u] - m_new);
+                const float p1 = ex2_approx(v[j + 2 * u + 1] - m_new);
+                sum += p0 + p1;
+                w[u] = pack2<T>(p0, p1);
+            }
+            *reinterpret_cast<uint4 *>(sP + core_off(r, j >> 3, TBK / 8)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l_run = l_run * corr + sum;
+        // rescale this warp's O rows when some row maximum moved
+        if (kt > 0 && __any_sync(FULL_MASK, move)) {
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float o[32];
+                tmem_ld32(tmem_o + lane_base + c0, o);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    o[j] *= corr;
+                tmem_st32(tmem_o + lane_base + c0, o);
             }
         }
-        // ---- scale, causal mask, online softmax (rows r0 and r0 + 8)
-        float mx0 = m0, mx1 = m1;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // O += P V.  P: K-major, TBK/8 chunks a row.  V is the MN-major B: K
+        // (key) direction stride DCH*128 B per group of 8 keys, N (d)
+        // direction stride 128 B; a step of 16 keys is two key groups.
+        if (tid == 0 && !*abort_flag) {
+            const uint32_t vb = sVa + buf * C::KV_BYTES;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int key = kt * BK + j * 8 + 2 * (lane & 3);
-            s[j][0] = key <= qpos0 ? s[j][0] * p.scale_log2 : -INFINITY;
-            s[j][1] = key + 1 <= qpos0 ? s[j][1] * p.scale_log2 : -INFINITY;
-            s[j][2] = key <= qpos1 ? s[j][2] * p.scale_log2 : -INFINITY;
-            s[j][3] = key + 1 <= qpos1 ? s[j][3] * p.scale_log2 : -INFINITY;
-            mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
-            mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+            for (int ks = 0; ks < TBK / 16; ++ks)
+                umma_f16(tmem_o, umma_desc(sPa + ks * 256, 128, (TBK / 8) * 128),
+                         umma_desc(vb + ks * 2 * DCH * 128, DCH * 128, 128), idesc_o,
+                         (kt > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(&bars[2]);
         }
-#pragma unroll
-        for (int off = 1; off <= 2; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, off));
-        }
-        // every row sees key 0 in the first tile, so mx0, mx1 are finite
-        const float c0 = exp2f(m0 - mx0), c1 = exp2f(m1 - mx1);
-        m0 = mx0;
-        m1 = mx1;
-        float sum0 = 0.0f, sum1 = 0.0f;
-        uint32_t pf[4][4];                         // P as A fragments, 4 k-steps of 16 keys
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float p0 = exp2f(s[j][0] - m0), p1 = exp2f(s[j][1] - m0);
-            const float p2 = exp2f(s[j][2] - m1), p3 = exp2f(s[j][3] - m1);
-            sum0 += p0 + p1;
-            sum1 += p2 + p3;
-            // n-tile j covers keys 8j..8j+7: k-step j/2, low (j even) or high half
-            pf[j >> 1][(j & 1) * 2 + 0] = pack2<T>(p0, p1);
-            pf[j >> 1][(j & 1) * 2 + 1] = pack2<T>(p2, p3);
-        }
-#pragma unroll
-        for (int off = 1; off <= 2; off <<= 1) {
-            sum0 += __shfl_xor_sync(FULL_MASK, sum0, off);
-            sum1 += __shfl_xor_sync(FULL_MASK, sum1, off);
-        }
-        l0 = l0 * c0 + sum0;
-        l1 = l1 * c1 + sum1;
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-            o[j][0] *= c0;
-            o[j][1] *= c0;
-            o[j][2] *= c1;
-            o[j][3] *= c1;
-        }
-        // ---- O += P V: 4 k-steps of 16 keys, D/8 n-tiles of 8 dims
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            // A fragment order: (rows 0-7, k 0-7), (rows 8-15, k 0-7), (rows 0-7, k 8-15), (rows 8-15, k 8-15)
-            const uint32_t a[4] = {pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3]};
-#pragma unroll
-            for (int dp = 0; dp < D / 16; ++dp) {
-                uint32_t vb[4];
-                ldsm_x4_t(vb, Vt + (kk * 16 + (lane & 15)) * C::LD + dp * 16 + (lane >> 4) * 8);
-                mma16816<BF16>(o[2 * dp], a, vb[0], vb[1]);
-                mma16816<BF16>(o[2 * dp + 1], a, vb[2], vb[3]);
-            }
-        }
-        __syncthreads();                           // the buffer is refilled next round
+        wait_bar(&bars[2], (uint32_t)(kt & 1));
+        tc_fence_after();
     }
 
-    // ---- normalise and store rows r0, r0 + 8 (fp32 [token][head][D])
-    const float inv0 = 1.0f / l0, inv1 = 1.0f / l1;
+
+    // ---- O / l for this thread's row (the TMEM loads are warp-wide and run
+    // converged; padding rows load without storing)
+    {
+        const float inv = 1.0f / l_run;
+        float *dst = p.out + ((int64_t)(q0 + qt * TBQ + min(r, rows - 1)) * p.num_q_heads + h) * D;
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-        const int col = j * 8 + 2 * (lane & 3);
-        if (r0 < rows) {
-            float *dst = p.out + ((int64_t)(q0 + qt * BQ + r0) * p.num_q_heads + h) * D + col;
-            *reinterpret_cast<float2 *>(dst) = make_float2(o[j][0] * inv0, o[j][1] * inv0);
-        }
-        if (r0 + 8 < rows) {
-            float *dst = p.out + ((int64_t)(q0 + qt * BQ + r0 + 8) * p.num_q_heads + h) * D + col;
-            *reinterpret_cast<float2 *>(dst) = make_float2(o[j][2] * inv1, o[j][3] * inv1);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float o[32];
+            tmem_ld32(tmem_o + lane_base + c0, o);
+            if (r < rows) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(dst + c0 + j) =
+                        make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
+            }
         }
     }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "n"(C::TMEM_COLS));
 }
 
 template <int D, typename T>
 int launch_prefill_t(const pkv_pool *pool, const PrefillParams &prm, int max_q_len,
                      cudaStream_t s)
 {
-    using C = PCfg<D>;
+    (void)pool;
+    using C = TcCfg<D>;
     static bool configured = false;
     if (!configured) {
-        if (cudaFuncSetAttribute(paged_prefill_kernel<D, T>,
+        if (cudaFuncSetAttribute(paged_prefill_tc_kernel<D, T>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_BYTES) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured = true;
     }
-    const dim3 grid((unsigned)((max_q_len + BQ - 1) / BQ), (unsigned)prm.num_q_heads,
+    const dim3 grid((unsigned)((max_q_len + TBQ - 1) / TBQ), (unsigned)prm.num_q_heads,
                     (unsigned)prm.batch);
-    if (launch_pdl(paged_prefill_kernel<D, T>, grid, dim3(NWARP * 32), (size_t)C::SMEM_BYTES, s,
+    if (launch_pdl(paged_prefill_tc_kernel<D, T>, grid, dim3(128), (size_t)C::SMEM_BYTES, s,
                    prm) != cudaSuccess)
         return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
