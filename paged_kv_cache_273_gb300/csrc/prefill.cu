@@ -54,7 +54,7 @@ struct PrefillParams {
     const int32_t *seq_lens;
     float *out;
     unsigned int *err;
-    int batch, num_q_heads, num_kv_heads, block_size, max_blocks_per_seq, num_blocks;
+    int batch, num_q_heads, num_kv_heads, block_size, bs_log2, max_blocks_per_seq, num_blocks;
     float scale_log2;
 };
 
@@ -236,27 +236,32 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
         const T *src = qg + ((int64_t)(q0 + qt * TBQ + (ok ? r : 0)) * p.num_q_heads + h) * D + c * 8;
         cp_async16(sQ + core_off(r, c, DCH), src, ok);
     }
-    // K or V rows of key tile kt into buffer buf
-    auto load_rows = [&](const T *src_cache, unsigned char *dst_tile, int kt) {
-        for (int idx = tid; idx < TBK * DCH; idx += 128) {
-            const int r = idx / DCH, c = idx % DCH;
+    // K and V rows of key tile kt into buffer buf: thread t copies chunk
+    // t % DCH of rows t / DCH, t / DCH + 128 / DCH, ... of both (block sizes
+    // are powers of two: shifts, no divisions)
+    auto load_kv = [&](int kt, int buf) {
+        const int c = tid % DCH;
+#pragma unroll 4
+        for (int r = tid / DCH; r < TBK; r += 128 / DCH) {
             const int pos = kt * TBK + r;
             bool ok = pos <= last_pos;
             int64_t row = 0;
             if (ok) {
-                const int32_t blk = __ldg(table + pos / p.block_size);
+                const int32_t blk = __ldg(table + (pos >> p.bs_log2));
                 if (blk < 0 || blk >= p.num_blocks) {
                     atomicOr(p.err, PKV_EBIT_BLOCK);
                     ok = false;
                 } else {
-                    row = ((int64_t)blk * p.num_kv_heads + kvh) * p.block_size + pos % p.block_size;
+                    row = (((int64_t)blk * p.num_kv_heads + kvh) << p.bs_log2) +
+                          (pos & (p.block_size - 1));
                 }
             }
-            cp_async16(dst_tile + core_off(r, c, DCH), src_cache + row * D + c * 8, ok);
+            const uint32_t o = core_off(r, c, DCH);
+            cp_async16(sK + buf * C::KV_BYTES + o, kg + row * D + c * 8, ok);
+            cp_async16(sV + buf * C::KV_BYTES + o, vg + row * D + c * 8, ok);
         }
     };
-    load_rows(kg, sK, 0);
-    load_rows(vg, sV, 0);
+    load_kv(0, 0);
     cp_async_commit();                            // group: Q, K0, V0
     tc_fence_before();
     __syncthreads();
@@ -284,8 +289,7 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
         // K/V of the next tile go to the other buffer, which P.V(kt-1) (waited
         // below in the previous round) was the last to read
         if (kt + 1 < ntiles) {
-            load_rows(kg, sK + (buf ^ 1) * C::KV_BYTES, kt + 1);
-            load_rows(vg, sV + (buf ^ 1) * C::KV_BYTES, kt + 1);
+            load_kv(kt + 1, buf ^ 1);
             cp_async_commit();
             cp_async_wait<1>();
         } else {
@@ -315,14 +319,17 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
         tmem_ld32(tmem_s + lane_base, *reinterpret_cast<float(*)[32]>(&v[0]));
         tmem_ld32(tmem_s + lane_base + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
         const bool diag = kt * TBK + TBK - 1 > first_pos;
+        if (diag) {
+#pragma unroll
+            for (int j = 0; j < TBK; ++j)
+                if (kt * TBK + j > qpos)
+                    v[j] = -INFINITY;
+        }
         float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < TBK; ++j) {
-            v[j] *= p.scale_log2;
-            if (diag && kt * TBK + j > qpos)
-                v[j] = -INFINITY;
+        for (int j = 0; j < TBK; ++j)
             mx = fmaxf(mx, v[j]);
-        }
+        mx *= p.scale_log2;                        // scale > 0: the maximum commutes
         // The running maximum moves only when a score exceeds it by more
         // than 2^8 (or on the first tile): below that the weights stay
         // <= 256, exact in fp32 and representable in fp16/bf16, and the
@@ -337,8 +344,8 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
             uint32_t w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const float p0 = ex2_approx(v[j + 2 * u] - m_new);
-                const float p1 = ex2_approx(v[j + 2 * u + 1] - m_new);
+                const float p0 = ex2_approx(fmaf(v[j + 2 * u], p.scale_log2, -m_new));
+                const float p1 = ex2_approx(fmaf(v[j + 2 * u + 1], p.scale_log2, -m_new));
                 sum += p0 + p1;
                 w[u] = pack2<T>(p0, p1);
             }
@@ -445,6 +452,9 @@ int launch_prefill(const pkv_pool *pool, const void *q, int num_q_heads, const v
     prm.num_q_heads = num_q_heads;
     prm.num_kv_heads = pool->num_kv_heads;
     prm.block_size = pool->block_size;
+    prm.bs_log2 = 0;
+    while ((1 << prm.bs_log2) < pool->block_size)
+        ++prm.bs_log2;
     prm.max_blocks_per_seq = max_blocks_per_seq;
     prm.num_blocks = pool->num_blocks;
     prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
