@@ -171,8 +171,26 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// One fp32 column of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float x)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr),
+                 "r"(__float_as_uint(x))
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr)
+{
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    return __uint_as_float(r);
+}
+
+constexpr int TNT = 256;      // threads: two per query row, each with half the columns
+
 template <int D, typename T>
-__global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillParams p)
+__global__ void __launch_bounds__(TNT, 2) paged_prefill_tc_kernel(const PrefillParams p)
 {
     using C = TcCfg<D>;
     constexpr uint32_t AB = MmaType<T>::bf16 ? 1u : 0u;
@@ -210,6 +228,8 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
     const int last_pos = first_pos + rows - 1;
     const int ntiles = last_pos / TBK + 1;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int quad = warp & 3;                     // TMEM lanes 32*quad .. 32*quad+31
+    const int hf = warp >> 2;                      // which half of the columns
     const int32_t *table = p.block_tables + (int64_t)b * p.max_blocks_per_seq;
     const T *qg = static_cast<const T *>(p.q);
     const T *kg = static_cast<const T *>(p.k_cache);
@@ -230,19 +250,19 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
     }
 
     // ---- async loads into the core-matrix layout
-    for (int idx = tid; idx < TBQ * DCH; idx += 128) {
+    for (int idx = tid; idx < TBQ * DCH; idx += TNT) {
         const int r = idx / DCH, c = idx % DCH;
         const bool ok = r < rows;
         const T *src = qg + ((int64_t)(q0 + qt * TBQ + (ok ? r : 0)) * p.num_q_heads + h) * D + c * 8;
         cp_async16(sQ + core_off(r, c, DCH), src, ok);
     }
     // K and V rows of key tile kt into buffer buf: thread t copies chunk
-    // t % DCH of rows t / DCH, t / DCH + 128 / DCH, ... of both (block sizes
+    // t % DCH of rows t / DCH, t / DCH + TNT / DCH, ... of both (block sizes
     // are powers of two: shifts, no divisions)
     auto load_kv = [&](int kt, int buf) {
         const int c = tid % DCH;
 #pragma unroll 4
-        for (int r = tid / DCH; r < TBK; r += 128 / DCH) {
+        for (int r = tid / DCH; r < TBK; r += TNT / DCH) {
             const int pos = kt * TBK + r;
             bool ok = pos <= last_pos;
             int64_t row = 0;
@@ -269,13 +289,23 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_s = tmem;                 // S: columns [0, 64)
     const uint32_t tmem_o = tmem + TBK;           // O: columns [64, 64 + D)
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tmem_x = tmem + TBK + D;       // exchange columns between the two halves
     const uint32_t idesc_s = umma_idesc(AB, 0u, TBK);
     const uint32_t idesc_o = umma_idesc(AB, 1u, D);
     const uint32_t sQa = smem_addr(sQ), sKa = smem_addr(sK), sVa = smem_addr(sV), sPa = smem_addr(sP);
 
-    const int r = tid;                             // this thread's query row
+    const int r = tid & (TBQ - 1);                 // this thread's query row
     const int qpos = first_pos + min(r, rows - 1);
+    // The two threads of a row (warps quad and quad + 4) swap one value
+    // through a spare TMEM column; a named barrier per warp pair orders it.
+    auto swap_with_partner = [&](float mine, int slot) {
+        tmem_st1(tmem_x + lane_base + 2 * slot + hf, mine);
+        tc_fence_before();
+        named_bar_sync(1 + quad, 64);
+        tc_fence_after();
+        return tmem_ld1(tmem_x + lane_base + 2 * slot + (hf ^ 1));
+    };
     float m_run = -INFINITY, l_run = 0.0f;
     auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
         if (!mbar_wait_bounded(bar, parity, abort_flag) && !*abort_flag) {
@@ -315,20 +345,21 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
 
         // ---- this row's scores in the log2 domain, masked where the tile
         // crosses the diagonal
-        float v[TBK];
-        tmem_ld32(tmem_s + lane_base, *reinterpret_cast<float(*)[32]>(&v[0]));
-        tmem_ld32(tmem_s + lane_base + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+        constexpr int HC = TBK / 2;                // score columns of this thread
+        float v[HC];
+        tmem_ld32(tmem_s + lane_base + hf * HC, v);
         const bool diag = kt * TBK + TBK - 1 > first_pos;
         if (diag) {
 #pragma unroll
-            for (int j = 0; j < TBK; ++j)
-                if (kt * TBK + j > qpos)
+            for (int j = 0; j < HC; ++j)
+                if (kt * TBK + hf * HC + j > qpos)
                     v[j] = -INFINITY;
         }
         float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < TBK; ++j)
+        for (int j = 0; j < HC; ++j)
             mx = fmaxf(mx, v[j]);
+        mx = fmaxf(mx, swap_with_partner(mx, kt & 1));   // the row's maximum
         mx *= p.scale_log2;                        // scale > 0: the maximum commutes
         // The running maximum moves only when a score exceeds it by more
         // than 2^8 (or on the first tile): below that the weights stay
@@ -340,7 +371,7 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
         m_run = m_new;
         float sum = 0.0f;
 #pragma unroll
-        for (int j = 0; j < TBK; j += 8) {
+        for (int j = 0; j < HC; j += 8) {
             uint32_t w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -349,20 +380,20 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
                 sum += p0 + p1;
                 w[u] = pack2<T>(p0, p1);
             }
-            *reinterpret_cast<uint4 *>(sP + core_off(r, j >> 3, TBK / 8)) =
+            *reinterpret_cast<uint4 *>(sP + core_off(r, (hf * HC + j) >> 3, TBK / 8)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
         }
         l_run = l_run * corr + sum;
-        // rescale this warp's O rows when some row maximum moved
+        // rescale this warp's half of its O rows when some row maximum moved
         if (kt > 0 && __any_sync(FULL_MASK, move)) {
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < D / 2; c0 += 32) {
                 float o[32];
-                tmem_ld32(tmem_o + lane_base + c0, o);
+                tmem_ld32(tmem_o + lane_base + hf * (D / 2) + c0, o);
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     o[j] *= corr;
-                tmem_st32(tmem_o + lane_base + c0, o);
+                tmem_st32(tmem_o + lane_base + hf * (D / 2) + c0, o);
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -386,15 +417,16 @@ __global__ void __launch_bounds__(128, 2) paged_prefill_tc_kernel(const PrefillP
     }
 
 
-    // ---- O / l for this thread's row (the TMEM loads are warp-wide and run
-    // converged; padding rows load without storing)
+    // ---- O / l for this thread's half row (the TMEM loads are warp-wide
+    // and run converged; padding rows load without storing)
     {
-        const float inv = 1.0f / l_run;
-        float *dst = p.out + ((int64_t)(q0 + qt * TBQ + min(r, rows - 1)) * p.num_q_heads + h) * D;
+        const float inv = 1.0f / (l_run + swap_with_partner(l_run, 0));
+        float *dst = p.out + ((int64_t)(q0 + qt * TBQ + min(r, rows - 1)) * p.num_q_heads + h) * D +
+                     hf * (D / 2);
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
             float o[32];
-            tmem_ld32(tmem_o + lane_base + c0, o);
+            tmem_ld32(tmem_o + lane_base + hf * (D / 2) + c0, o);
             if (r < rows) {
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
@@ -426,7 +458,7 @@ int launch_prefill_t(const pkv_pool *pool, const PrefillParams &prm, int max_q_l
     }
     const dim3 grid((unsigned)((max_q_len + TBQ - 1) / TBQ), (unsigned)prm.num_q_heads,
                     (unsigned)prm.batch);
-    if (launch_pdl(paged_prefill_tc_kernel<D, T>, grid, dim3(128), (size_t)C::SMEM_BYTES, s,
+    if (launch_pdl(paged_prefill_tc_kernel<D, T>, grid, dim3(TNT), (size_t)C::SMEM_BYTES, s,
                    prm) != cudaSuccess)
         return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
