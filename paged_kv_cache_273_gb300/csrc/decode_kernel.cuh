@@ -681,7 +681,12 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                         *qcount = qn + 1;
                         q_done = true;
                     }
-                    if (!t_done && mbar_test_wait(&empty[st], (uint32_t)(rnd & 1) ^ 1u)) {
+                    // Staggered start: the first group's tiles beyond the first W
+                    // (one per consumer warp) go out once tile 0 has landed, so
+                    // the first tiles are not queued behind the whole ring's
+                    // burst and the consumers start earlier.
+                    const bool hold = k0 == 0 && lane >= W && !mbar_test_wait(&full[0], 0u);
+                    if (!t_done && !hold && mbar_test_wait(&empty[st], (uint32_t)(rnd & 1) ^ 1u)) {
                     unsigned char *sK = stages + st * C::STAGE_BYTES;
                     unsigned char *sV = sK + C::KV_BYTES;
                     unsigned char *sKS = sV + C::KV_BYTES;
