@@ -58,29 +58,44 @@ struct PrefillParams {
     float scale_log2;
 };
 
-// ---- tcgen05: 128 queries x 64 keys per step
+// ---- tcgen05: 2 x 128 queries x 64 keys per step, warp-specialised
 //
-// A CTA of 4 warps takes 128 queries of one (sequence, query head); thread
-// t owns query row t; two CTAs share an SM.  Q, K and V tiles are brought
-// by 16-byte cp.async copies (each key row located through the block table)
-// into shared memory in the tensor cores' core-matrix layout (8 rows x 16
-// bytes per 128-byte core matrix, no swizzle), K/V double buffered.  S = Q K^T
-// (M 128, N 64, K = D) and O += P V (M 128, N = D, K 64) are single-thread
-// tcgen05.mma issues with fp32 accumulators in tensor memory: S in columns
-// [0, 64), O in [64, 64 + D).  Each thread reads its S row with tcgen05.ld,
-// does the online softmax for it, writes its P row (fp16/bf16) back to
-// shared memory as the next A operand, and rescales its O row in tensor
-// memory when its maximum moved by more than 2^8.
+// A CTA takes 256 queries of one (sequence, query head) as two 128-row
+// halves A and B that share every K/V tile (one CTA per SM), with three
+// roles:
+//  * producer warps copy a quarter of Q each, then K/V tiles into a ring of
+//    shared-memory stages (warp w fills stage w with tiles w, w + 4, ...)
+//    with 16-byte cp.async copies, each key row located through the block
+//    table, in the tensor cores' core-matrix layout (8 rows x 16 bytes per
+//    128-byte core matrix, no swizzle);
+//  * one thread issues the tcgen05.mma: S = Q K^T (M 128, N 64, K = D) and
+//    O += P V (M 128, N = D, K 64) per half, fp32 accumulators in tensor
+//    memory (half h: S in columns [h C, h C + 64), O in the next D);
+//  * one warpgroup per half, one thread per query row, reads its S row with
+//    tcgen05.ld, does the online softmax, writes P (fp16/bf16) to shared
+//    memory as the A operand of P V, and rescales its O row in tensor memory
+//    when the row maximum moved by more than 2^8.
+// The issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) lets one half's
+// softmax run while the tensor cores work on the other half.  mbarriers hand
+// the tiles over: kv_full / kv_empty per stage, s_full (tcgen05.commit after
+// S_h; it also covers the P V issued before it, so P_h and O_h are free),
+// p_full (the half's 128 softmax threads) and o_done (after the last P V).
 
-constexpr int TBQ = 128, TBK = 64;
+constexpr int TBQ = 128, TBK = 64, NQH = 2, NSTAGE = 4;
+constexpr int SOFT_WARPS = 4 * NQH, PROD_WARPS = NSTAGE;   // producer warp w fills stage w
+constexpr int MMA_WARP = SOFT_WARPS + PROD_WARPS;
+constexpr int TNT = (MMA_WARP + 1) * 32;
 
 template <int D>
 struct TcCfg {
-    static constexpr int Q_BYTES = TBQ * D * 2;
-    static constexpr int KV_BYTES = TBK * D * 2;
-    static constexpr int P_BYTES = TBQ * TBK * 2;
-    static constexpr int SMEM_BYTES = Q_BYTES + 4 * KV_BYTES + P_BYTES + 64;
-    static constexpr int TMEM_COLS = 256;          // S: 64 columns, O: D <= 128 columns
+    static constexpr int Q_BYTES = TBQ * D * 2;          // one half
+    static constexpr int KV_BYTES = TBK * D * 2;          // one K or V tile
+    static constexpr int P_BYTES = TBQ * TBK * 2;         // one half
+    static constexpr int BAR_OFF = NQH * Q_BYTES + 2 * NSTAGE * KV_BYTES + NQH * P_BYTES;
+    static constexpr int NBARS = 2 * NSTAGE + 3 * NQH + 2;
+    static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16;
+    static constexpr int TMEM_COLS = D == 128 ? 512 : 256;
+    static constexpr int HALF_COLS = TMEM_COLS / 2;       // >= TBK + D
 };
 
 // Byte offset of the 16-byte chunk c (8 elements along the contiguous
@@ -171,37 +186,26 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// One fp32 column of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, float x)
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr),
-                 "r"(__float_as_uint(x))
-                 : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float tmem_ld1(uint32_t taddr)
-{
-    uint32_t r;
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    return __uint_as_float(r);
-}
-
-constexpr int TNT = 256;      // threads: two per query row, each with half the columns
-
 template <int D, typename T>
-__global__ void __launch_bounds__(TNT, 2) paged_prefill_tc_kernel(const PrefillParams p)
+__global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillParams p)
 {
     using C = TcCfg<D>;
     constexpr uint32_t AB = MmaType<T>::bf16 ? 1u : 0u;
     constexpr int DCH = D / 8;                    // 16-byte chunks of a D-wide row
+    constexpr int QT = NQH * TBQ;                 // queries of this CTA
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sQ = smem_raw;
-    unsigned char *sK = sQ + C::Q_BYTES;          // two buffers
-    unsigned char *sV = sK + 2 * C::KV_BYTES;     // two buffers
-    unsigned char *sP = sV + 2 * C::KV_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sP + C::P_BYTES);   // [0] S done, [2] O done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3);
+    unsigned char *sQ = smem_raw;                              // NQH halves
+    unsigned char *sK = sQ + NQH * C::Q_BYTES;                 // NSTAGE stages
+    unsigned char *sV = sK + NSTAGE * C::KV_BYTES;             // NSTAGE stages
+    unsigned char *sP = sV + NSTAGE * C::KV_BYTES;             // NQH halves
+    uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem_raw + C::BAR_OFF);
+    uint64_t *kv_empty = kv_full + NSTAGE;
+    uint64_t *s_full = kv_empty + NSTAGE;
+    uint64_t *p_full = s_full + NQH;
+    uint64_t *o_done = p_full + NQH;
+    uint64_t *q_full = o_done + NQH;
+    uint64_t *drain = q_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     grid_dependency_wait();
@@ -213,233 +217,291 @@ __global__ void __launch_bounds__(TNT, 2) paged_prefill_tc_kernel(const PrefillP
     const int q0 = __ldg(p.q_start + b);
     const int n = __ldg(p.q_start + b + 1) - q0;
     const int L = __ldg(p.seq_lens + b);
-    if (qt * TBQ >= n)
+    if (qt * QT >= n)
         return;
     if (L < n || L > p.max_blocks_per_seq * p.block_size) {
         if (threadIdx.x == 0 && qt == 0 && h == 0)
             atomicOr(p.err, PKV_EBIT_SEQLEN);
         return;
     }
-    const int G = p.num_q_heads / p.num_kv_heads;
-    const int kvh = h / G;
-    const int base = L - n;
-    const int rows = min(TBQ, n - qt * TBQ);
-    const int first_pos = base + qt * TBQ;        // position of this CTA's first query
-    const int last_pos = first_pos + rows - 1;
+    const int kvh = h / (p.num_q_heads / p.num_kv_heads);
+    const int rows_all = min(QT, n - qt * QT);
+    const int first_pos = L - n + qt * QT;         // position of this CTA's first query
+    const int last_pos = first_pos + rows_all - 1;
     const int ntiles = last_pos / TBK + 1;
+    // rows and key tiles of each half (the second may be empty)
+    const int rows_h[NQH] = {min(TBQ, rows_all), max(0, rows_all - TBQ)};
+    const int tiles_h[NQH] = {(first_pos + rows_h[0] - 1) / TBK + 1, rows_h[1] > 0 ? ntiles : 0};
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int quad = warp & 3;                     // TMEM lanes 32*quad .. 32*quad+31
-    const int hf = warp >> 2;                      // which half of the columns
-    const int32_t *table = p.block_tables + (int64_t)b * p.max_blocks_per_seq;
-    const T *qg = static_cast<const T *>(p.q);
-    const T *kg = static_cast<const T *>(p.k_cache);
-    const T *vg = static_cast<const T *>(p.v_cache);
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&kv_full[i], 32);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < NQH; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], TBQ);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(q_full, PROD_WARPS * 32);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 0) {
+    if (warp == MMA_WARP) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tmem_slot)),
                      "n"(C::TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-
-    // ---- async loads into the core-matrix layout
-    for (int idx = tid; idx < TBQ * DCH; idx += TNT) {
-        const int r = idx / DCH, c = idx % DCH;
-        const bool ok = r < rows;
-        const T *src = qg + ((int64_t)(q0 + qt * TBQ + (ok ? r : 0)) * p.num_q_heads + h) * D + c * 8;
-        cp_async16(sQ + core_off(r, c, DCH), src, ok);
-    }
-    // K and V rows of key tile kt into buffer buf: thread t copies chunk
-    // t % DCH of rows t / DCH, t / DCH + TNT / DCH, ... of both (block sizes
-    // are powers of two: shifts, no divisions)
-    auto load_kv = [&](int kt, int buf) {
-        const int c = tid % DCH;
-#pragma unroll 4
-        for (int r = tid / DCH; r < TBK; r += TNT / DCH) {
-            const int pos = kt * TBK + r;
-            bool ok = pos <= last_pos;
-            int64_t row = 0;
-            if (ok) {
-                const int32_t blk = __ldg(table + (pos >> p.bs_log2));
-                if (blk < 0 || blk >= p.num_blocks) {
-                    atomicOr(p.err, PKV_EBIT_BLOCK);
-                    ok = false;
-                } else {
-                    row = (((int64_t)blk * p.num_kv_heads + kvh) << p.bs_log2) +
-                          (pos & (p.block_size - 1));
-                }
-            }
-            const uint32_t o = core_off(r, c, DCH);
-            cp_async16(sK + buf * C::KV_BYTES + o, kg + row * D + c * 8, ok);
-            cp_async16(sV + buf * C::KV_BYTES + o, vg + row * D + c * 8, ok);
-        }
-    };
-    load_kv(0, 0);
-    cp_async_commit();                            // group: Q, K0, V0
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_s = tmem;                 // S: columns [0, 64)
-    const uint32_t tmem_o = tmem + TBK;           // O: columns [64, 64 + D)
-    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t tmem_x = tmem + TBK + D;       // exchange columns between the two halves
-    const uint32_t idesc_s = umma_idesc(AB, 0u, TBK);
-    const uint32_t idesc_o = umma_idesc(AB, 1u, D);
-    const uint32_t sQa = smem_addr(sQ), sKa = smem_addr(sK), sVa = smem_addr(sV), sPa = smem_addr(sP);
-
-    const int r = tid & (TBQ - 1);                 // this thread's query row
-    const int qpos = first_pos + min(r, rows - 1);
-    // The two threads of a row (warps quad and quad + 4) swap one value
-    // through a spare TMEM column; a named barrier per warp pair orders it.
-    auto swap_with_partner = [&](float mine, int slot) {
-        tmem_st1(tmem_x + lane_base + 2 * slot + hf, mine);
-        tc_fence_before();
-        named_bar_sync(1 + quad, 64);
-        tc_fence_after();
-        return tmem_ld1(tmem_x + lane_base + 2 * slot + (hf ^ 1));
-    };
-    float m_run = -INFINITY, l_run = 0.0f;
-    auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
-        if (!mbar_wait_bounded(bar, parity, abort_flag) && !*abort_flag) {
+    // A timed-out wait raises the error bit once and makes every role stop.
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_wait_bounded(bar, parity, abort_flag))
+            return true;
+        if (!*abort_flag) {
             *abort_flag = 1;
             atomicOr(p.err, PKV_EBIT_TIMEOUT);
         }
+        return false;
     };
 
-    for (int kt = 0; kt < ntiles; ++kt) {
-        const int buf = kt & 1;
-        // K/V of the next tile go to the other buffer, which P.V(kt-1) (waited
-        // below in the previous round) was the last to read
-        if (kt + 1 < ntiles) {
-            load_kv(kt + 1, buf ^ 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+    if (warp < SOFT_WARPS) {
+        // ================= softmax: one thread per query row of half hh
+        const int hh = warp >> 2, quad = warp & 3;
+        const int r = quad * 32 + (tid & 31);
+        const int rows = rows_h[hh], my_tiles = tiles_h[hh];
+        const int qpos = first_pos + hh * TBQ + min(r, max(rows, 1) - 1);
+        const uint32_t t_s = tmem + hh * C::HALF_COLS + ((uint32_t)(quad * 32) << 16);
+        const uint32_t t_o = t_s + TBK;
+        unsigned char *sPh = sP + hh * C::P_BYTES;
+        float m_run = -INFINITY, l_run = 0.0f;
+        bool ok = true;
+        for (int kt = 0; kt < my_tiles; ++kt) {
+            ok = __all_sync(FULL_MASK, wait(&s_full[hh], (uint32_t)(kt & 1)));
+            if (!ok)
+                break;
+            tc_fence_after();
+            float v[TBK];
+            tmem_ld32(t_s, *reinterpret_cast<float(*)[32]>(v));
+            tmem_ld32(t_s + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+            // scores of keys past this row's position (the tile crosses the
+            // diagonal) drop out
+            if (kt * TBK + TBK - 1 > first_pos + hh * TBQ) {
+#pragma unroll
+                for (int j = 0; j < TBK; ++j)
+                    if (kt * TBK + j > qpos)
+                        v[j] = -INFINITY;
+            }
+            float mx = v[0];
+#pragma unroll
+            for (int j = 1; j < TBK; ++j)
+                mx = fmaxf(mx, v[j]);
+            mx *= p.scale_log2;                    // scale > 0: the maximum commutes
+            // The running maximum moves only when a score exceeds it by more
+            // than 2^8 (or on the first tile): below that the weights stay
+            // <= 256, exact in fp32 and representable in fp16/bf16, and the
+            // final division by the sum of the same weights is unchanged.
+            const bool move = kt == 0 || mx > m_run + 8.0f;
+            const float m_new = move ? fmaxf(m_run, mx) : m_run;
+            const float corr = kt == 0 ? 1.0f : ex2_approx(m_run - m_new);
+            m_run = m_new;
+            float sum = 0.0f;
+#pragma unroll
+            for (int j = 0; j < TBK; j += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float p0 = ex2_approx(fmaf(v[j + 2 * u], p.scale_log2, -m_new));
+                    const float p1 = ex2_approx(fmaf(v[j + 2 * u + 1], p.scale_log2, -m_new));
+                    sum += p0 + p1;
+                    w[u] = pack2<T>(p0, p1);
+                }
+                *reinterpret_cast<uint4 *>(sPh + core_off(r, j >> 3, TBK / 8)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            l_run = l_run * corr + sum;
+            // O_h is idle here: the P V of the previous tile finished before
+            // S_h(kt) did, the next one waits for p_full
+            if (kt > 0 && __any_sync(FULL_MASK, move)) {
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(t_o + c0, o);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        o[j] *= corr;
+                    tmem_st32(t_o + c0, o);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(&p_full[hh]);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // S = Q K^T.  Q and K tiles are K-major with DCH chunks a row:
+        // ---- O / l (warp-uniform branch: the TMEM loads run converged;
+        // padding rows load without storing)
+        if (my_tiles > 0 && ok && __all_sync(FULL_MASK, wait(&o_done[hh], 0u))) {
+            tc_fence_after();
+            const float inv = 1.0f / l_run;
+            float *dst = p.out + ((int64_t)(q0 + qt * QT + hh * TBQ + min(r, max(rows, 1) - 1)) *
+                                      p.num_q_heads + h) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float o[32];
+                tmem_ld32(t_o + c0, o);
+                if (r < rows) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(dst + c0 + j) =
+                            make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
+                }
+            }
+        }
+    } else if (warp < MMA_WARP) {
+        // ================= producer warp pw: rows pw*64 .. pw*64+63 of Q, then
+        // K/V tiles pw, pw + NSTAGE, ... into stage pw.  Eight consecutive
+        // lanes fill one core matrix (8 rows x 16 B: a conflict-free 128-byte
+        // shared-memory write); a warp reads 64 contiguous bytes of 8 rows.
+        const int pw = warp - SOFT_WARPS;
+        const int rr = tid & 7, cq = (tid >> 3) & 3;
+        constexpr int RG = TBK / 8;                // 8-row groups of a tile
+        const T *qg = static_cast<const T *>(p.q);
+        const T *kg = static_cast<const T *>(p.k_cache);
+        const T *vg = static_cast<const T *>(p.v_cache);
+        const int32_t *table = p.block_tables + (int64_t)b * p.max_blocks_per_seq;
+#pragma unroll
+        for (int g = 0; g < RG; ++g) {
+            const int r = pw * TBK + g * 8 + rr;   // query of this CTA, 0..255
+            const bool ok = r < rows_all;
+            const T *src = qg + ((int64_t)(q0 + qt * QT + (ok ? r : 0)) * p.num_q_heads + h) * D;
+#pragma unroll
+            for (int c = cq; c < DCH; c += 4)
+                cp_async16(sQ + (r >> 7) * C::Q_BYTES + core_off(r & (TBQ - 1), c, DCH), src + c * 8, ok);
+        }
+        cp_async_commit();
+        bool ok = true, q_sent = false;
+        for (int kt = pw; kt < ntiles; kt += NSTAGE) {
+            // block ids first (their loads overlap the wait for the stage)
+            int32_t blk[RG];
+#pragma unroll
+            for (int g = 0; g < RG; ++g) {
+                const int pos = kt * TBK + g * 8 + rr;
+                blk[g] = pos <= last_pos ? __ldg(table + (pos >> p.bs_log2)) : 0;
+            }
+            if (kt >= NSTAGE && !wait(&kv_empty[pw], (uint32_t)(((kt / NSTAGE) & 1) ^ 1))) {
+                ok = false;
+                break;
+            }
+            // block sizes are powers of two: shifts, no divisions
+#pragma unroll
+            for (int g = 0; g < RG; ++g) {
+                const int pos = kt * TBK + g * 8 + rr;
+                bool valid = pos <= last_pos;
+                int64_t row = 0;
+                if (valid && (blk[g] < 0 || blk[g] >= p.num_blocks)) {
+                    atomicOr(p.err, PKV_EBIT_BLOCK);
+                    valid = false;
+                } else if (valid) {
+                    row = (((int64_t)blk[g] * p.num_kv_heads + kvh) << p.bs_log2) +
+                          (pos & (p.block_size - 1));
+                }
+#pragma unroll
+                for (int c = cq; c < DCH; c += 4) {
+                    const uint32_t o = pw * C::KV_BYTES + core_off(g * 8 + rr, c, DCH);
+                    cp_async16(sK + o, kg + row * D + c * 8, valid);
+                    cp_async16(sV + o, vg + row * D + c * 8, valid);
+                }
+            }
+            cp_async_commit();
+            if (!q_sent) {                         // Q (the older group) has landed
+                cp_async_wait<1>();
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(q_full);
+                q_sent = true;
+            }
+            cp_async_wait<0>();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&kv_full[pw]);
+        }
+        cp_async_wait<0>();
+        if (ok && !q_sent) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(q_full);
+        }
+    } else if ((tid & 31) == 0) {
+        // ================= MMA issue (one thread)
+        const uint32_t idesc_s = umma_idesc(AB, 0u, TBK);
+        const uint32_t idesc_o = umma_idesc(AB, 1u, D);
+        const uint32_t sQa = smem_addr(sQ), sKa = smem_addr(sK), sVa = smem_addr(sV),
+                       sPa = smem_addr(sP);
+        const int last_half = tiles_h[1] > 0 ? 1 : 0;   // the last reader of each K/V tile
+        // S_hh = Q_hh K^T.  Q and K are K-major with DCH chunks a row:
         // K-direction core stride 128 B, row-group stride DCH*128 B; a K = 16
         // step is two chunks.
-        if (tid == 0 && !*abort_flag) {
-            const uint32_t kb = sKa + buf * C::KV_BYTES;
+        auto issue_s = [&](int hh, int kt) {
+            const uint32_t kb = sKa + (kt % NSTAGE) * C::KV_BYTES, qb = sQa + hh * C::Q_BYTES;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-                umma_f16(tmem_s, umma_desc(sQa + ks * 256, 128, DCH * 128),
+                umma_f16(tmem + hh * C::HALF_COLS, umma_desc(qb + ks * 256, 128, DCH * 128),
                          umma_desc(kb + ks * 256, 128, DCH * 128), idesc_s, ks > 0 ? 1u : 0u);
-            umma_commit(&bars[0]);
-        }
-        wait_bar(&bars[0], (uint32_t)(kt & 1));
-        tc_fence_after();
-
-        // ---- this row's scores in the log2 domain, masked where the tile
-        // crosses the diagonal
-        constexpr int HC = TBK / 2;                // score columns of this thread
-        float v[HC];
-        tmem_ld32(tmem_s + lane_base + hf * HC, v);
-        const bool diag = kt * TBK + TBK - 1 > first_pos;
-        if (diag) {
-#pragma unroll
-            for (int j = 0; j < HC; ++j)
-                if (kt * TBK + hf * HC + j > qpos)
-                    v[j] = -INFINITY;
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < HC; ++j)
-            mx = fmaxf(mx, v[j]);
-        mx = fmaxf(mx, swap_with_partner(mx, kt & 1));   // the row's maximum
-        mx *= p.scale_log2;                        // scale > 0: the maximum commutes
-        // The running maximum moves only when a score exceeds it by more
-        // than 2^8 (or on the first tile): below that the weights stay
-        // <= 256, exact in fp32 and representable in fp16/bf16, and the
-        // final division by the sum of the same weights is unchanged.
-        const bool move = kt == 0 || mx > m_run + 8.0f;
-        const float m_new = move ? fmaxf(m_run, mx) : m_run;
-        const float corr = kt == 0 ? 1.0f : ex2_approx(m_run - m_new);
-        m_run = m_new;
-        float sum = 0.0f;
-#pragma unroll
-        for (int j = 0; j < HC; j += 8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float p0 = ex2_approx(fmaf(v[j + 2 * u], p.scale_log2, -m_new));
-                const float p1 = ex2_approx(fmaf(v[j + 2 * u + 1], p.scale_log2, -m_new));
-                sum += p0 + p1;
-                w[u] = pack2<T>(p0, p1);
-            }
-            *reinterpret_cast<uint4 *>(sP + core_off(r, (hf * HC + j) >> 3, TBK / 8)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        l_run = l_run * corr + sum;
-        // rescale this warp's half of its O rows when some row maximum moved
-        if (kt > 0 && __any_sync(FULL_MASK, move)) {
-#pragma unroll
-            for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                float o[32];
-                tmem_ld32(tmem_o + lane_base + hf * (D / 2) + c0, o);
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    o[j] *= corr;
-                tmem_st32(tmem_o + lane_base + hf * (D / 2) + c0, o);
-            }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // O += P V.  P: K-major, TBK/8 chunks a row.  V is the MN-major B: K
-        // (key) direction stride DCH*128 B per group of 8 keys, N (d)
+            umma_commit(&s_full[hh]);
+        };
+        // O_hh += P_hh V.  P: K-major, TBK/8 chunks a row.  V is the MN-major
+        // B: K (key) direction stride DCH*128 B per group of 8 keys, N (d)
         // direction stride 128 B; a step of 16 keys is two key groups.
-        if (tid == 0 && !*abort_flag) {
-            const uint32_t vb = sVa + buf * C::KV_BYTES;
+        auto issue_pv = [&](int hh, int kt) {
+            const uint32_t vb = sVa + (kt % NSTAGE) * C::KV_BYTES, pb = sPa + hh * C::P_BYTES;
 #pragma unroll
             for (int ks = 0; ks < TBK / 16; ++ks)
-                umma_f16(tmem_o, umma_desc(sPa + ks * 256, 128, (TBK / 8) * 128),
+                umma_f16(tmem + hh * C::HALF_COLS + TBK,
+                         umma_desc(pb + ks * 256, 128, (TBK / 8) * 128),
                          umma_desc(vb + ks * 2 * DCH * 128, DCH * 128, 128), idesc_o,
                          (kt > 0 || ks > 0) ? 1u : 0u);
-            umma_commit(&bars[2]);
+        };
+        bool ok = wait(q_full, 0u) && wait(&kv_full[0], 0u);
+        if (ok) {
+            tc_fence_after();
+            for (int hh = 0; hh < NQH; ++hh)
+                if (tiles_h[hh] > 0)
+                    issue_s(hh, 0);
         }
-        wait_bar(&bars[2], (uint32_t)(kt & 1));
-        tc_fence_after();
-    }
-
-
-    // ---- O / l for this thread's half row (the TMEM loads are warp-wide
-    // and run converged; padding rows load without storing)
-    {
-        const float inv = 1.0f / (l_run + swap_with_partner(l_run, 0));
-        float *dst = p.out + ((int64_t)(q0 + qt * TBQ + min(r, rows - 1)) * p.num_q_heads + h) * D +
-                     hf * (D / 2);
-#pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-            float o[32];
-            tmem_ld32(tmem_o + lane_base + hf * (D / 2) + c0, o);
-            if (r < rows) {
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(dst + c0 + j) =
-                        make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
+        for (int kt = 0; kt < ntiles && ok; ++kt) {
+            for (int hh = 0; hh < NQH; ++hh) {
+                if (kt >= tiles_h[hh])
+                    continue;
+                if (!(ok = wait(&p_full[hh], (uint32_t)(kt & 1))))
+                    break;
+                tc_fence_after();
+                issue_pv(hh, kt);
+                if (hh == last_half)
+                    umma_commit(&kv_empty[kt % NSTAGE]);
+                if (kt + 1 < tiles_h[hh]) {
+                    if (!(ok = wait(&kv_full[(kt + 1) % NSTAGE], (uint32_t)(((kt + 1) / NSTAGE) & 1))))
+                        break;
+                    tc_fence_after();
+                    issue_s(hh, kt + 1);
+                } else {
+                    umma_commit(&o_done[hh]);
+                }
             }
+        }
+        // every issued MMA has finished before tensor memory is released
+        umma_commit(drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(drain, 0u) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0)
+    if (warp == MMA_WARP) {
+        __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "n"(C::TMEM_COLS));
+    }
 }
 
 template <int D, typename T>
@@ -456,7 +518,8 @@ int launch_prefill_t(const pkv_pool *pool, const PrefillParams &prm, int max_q_l
             return PKV_ERR_CUDA;
         configured = true;
     }
-    const dim3 grid((unsigned)((max_q_len + TBQ - 1) / TBQ), (unsigned)prm.num_q_heads,
+    constexpr int QT = NQH * TBQ;
+    const dim3 grid((unsigned)((max_q_len + QT - 1) / QT), (unsigned)prm.num_q_heads,
                     (unsigned)prm.batch);
     if (launch_pdl(paged_prefill_tc_kernel<D, T>, grid, dim3(TNT), (size_t)C::SMEM_BYTES, s,
                    prm) != cudaSuccess)
