@@ -58,31 +58,34 @@ struct PrefillParams {
     float scale_log2;
 };
 
-// ---- tcgen05: 2 x 128 queries x 64 keys per step, warp-specialised
+// ---- tcgen05: 2 x 128 queries x 128 keys per step, warp-specialised
 //
 // A CTA takes 256 queries of one (sequence, query head) as two 128-row
 // halves A and B that share every K/V tile (one CTA per SM), with three
 // roles:
-//  * producer warps copy a quarter of Q each, then K/V tiles into a ring of
-//    shared-memory stages (warp w fills stage w with tiles w, w + 4, ...)
-//    with 16-byte cp.async copies, each key row located through the block
-//    table, in the tensor cores' core-matrix layout (8 rows x 16 bytes per
-//    128-byte core matrix, no swizzle);
-//  * one thread issues the tcgen05.mma: S = Q K^T (M 128, N 64, K = D) and
-//    O += P V (M 128, N = D, K 64) per half, fp32 accumulators in tensor
-//    memory (half h: S in columns [h C, h C + 64), O in the next D);
+//  * four producer warps copy a quarter of Q each, then K tiles (warps 0, 1)
+//    and V tiles (warps 2, 3) into two-slot rings in shared memory with
+//    16-byte cp.async copies, each key row located through the block table,
+//    in the tensor cores' core-matrix layout (8 rows x 16 bytes per 128-byte
+//    core matrix, no swizzle);
+//  * one thread issues the tcgen05.mma: S = Q K^T (M 128, N 128, K = D, both
+//    operands in shared memory) and O += P V (M 128, N = D, K 128, P read
+//    from tensor memory) per half, fp32 accumulators in tensor memory (half
+//    h: S in columns [256 h, 256 h + 128), O in the next D);
 //  * one warpgroup per half, one thread per query row, reads its S row with
-//    tcgen05.ld, does the online softmax, writes P (fp16/bf16) to shared
-//    memory as the A operand of P V, and rescales its O row in tensor memory
-//    when the row maximum moved by more than 2^8.
+//    tcgen05.ld, does the online softmax, writes P as fp16/bf16 pairs over
+//    the S columns it has read, and rescales its O row in tensor memory when
+//    the row maximum moved by more than 2^8.
 // The issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) lets one half's
-// softmax run while the tensor cores work on the other half.  mbarriers hand
-// the tiles over: kv_full / kv_empty per stage, s_full (tcgen05.commit after
-// S_h; it also covers the P V issued before it, so P_h and O_h are free),
-// p_full (the half's 128 softmax threads) and o_done (after the last P V).
+// softmax run while the tensor cores work on the other half; tcgen05.mma
+// runs in issue order, so S_h(j+1) overwrites P_h(j) only after P_h(j) V
+// has read it.  mbarriers hand the tiles over: k_full / k_empty and v_full /
+// v_empty per slot, s_full (tcgen05.commit after S_h, which also covers the
+// P V issued before it, so O_h is idle), p_full (the half's 128 softmax
+// threads) and o_done (after the last P V).
 
-constexpr int TBQ = 128, TBK = 64, NQH = 2, NSTAGE = 4;
-constexpr int SOFT_WARPS = 4 * NQH, PROD_WARPS = NSTAGE;   // producer warp w fills stage w
+constexpr int TBQ = 128, TBK = 128, NQH = 2, NSLOT = 2;
+constexpr int SOFT_WARPS = 4 * NQH, PROD_WARPS = 2 * NSLOT;   // K slots, then V slots
 constexpr int MMA_WARP = SOFT_WARPS + PROD_WARPS;
 constexpr int TNT = (MMA_WARP + 1) * 32;
 
@@ -90,12 +93,11 @@ template <int D>
 struct TcCfg {
     static constexpr int Q_BYTES = TBQ * D * 2;          // one half
     static constexpr int KV_BYTES = TBK * D * 2;          // one K or V tile
-    static constexpr int P_BYTES = TBQ * TBK * 2;         // one half
-    static constexpr int BAR_OFF = NQH * Q_BYTES + 2 * NSTAGE * KV_BYTES + NQH * P_BYTES;
-    static constexpr int NBARS = 2 * NSTAGE + 3 * NQH + 2;
+    static constexpr int BAR_OFF = NQH * Q_BYTES + 2 * NSLOT * KV_BYTES;
+    static constexpr int NBARS = 4 * NSLOT + 3 * NQH + 2;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16;
-    static constexpr int TMEM_COLS = D == 128 ? 512 : 256;
-    static constexpr int HALF_COLS = TMEM_COLS / 2;       // >= TBK + D
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int HALF_COLS = 256;                 // >= TBK + D
 };
 
 // Byte offset of the 16-byte chunk c (8 elements along the contiguous
@@ -127,6 +129,17 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t da, uint64_t 
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
                  "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// The same with A (M rows in TMEM lanes, K as 16-bit pairs along columns) read
+// from tensor memory.
+__device__ __forceinline__ void umma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t db,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+                 "r"(tmem_a), "l"(db), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
 
@@ -186,6 +199,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+                 "%12,%13,%14,%15,%16};" ::"r"(taddr),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                 "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
+                 "r"(w[14]), "r"(w[15])
+                 : "memory");
+}
+
 template <int D, typename T>
 __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillParams p)
 {
@@ -195,12 +219,13 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
     constexpr int QT = NQH * TBQ;                 // queries of this CTA
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sQ = smem_raw;                              // NQH halves
-    unsigned char *sK = sQ + NQH * C::Q_BYTES;                 // NSTAGE stages
-    unsigned char *sV = sK + NSTAGE * C::KV_BYTES;             // NSTAGE stages
-    unsigned char *sP = sV + NSTAGE * C::KV_BYTES;             // NQH halves
-    uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem_raw + C::BAR_OFF);
-    uint64_t *kv_empty = kv_full + NSTAGE;
-    uint64_t *s_full = kv_empty + NSTAGE;
+    unsigned char *sK = sQ + NQH * C::Q_BYTES;                 // NSLOT K tiles
+    unsigned char *sV = sK + NSLOT * C::KV_BYTES;              // NSLOT V tiles
+    uint64_t *k_full = reinterpret_cast<uint64_t *>(smem_raw + C::BAR_OFF);
+    uint64_t *k_empty = k_full + NSLOT;
+    uint64_t *v_full = k_empty + NSLOT;
+    uint64_t *v_empty = v_full + NSLOT;
+    uint64_t *s_full = v_empty + NSLOT;
     uint64_t *p_full = s_full + NQH;
     uint64_t *o_done = p_full + NQH;
     uint64_t *q_full = o_done + NQH;
@@ -235,9 +260,11 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
     const int tid = threadIdx.x, warp = tid >> 5;
 
     if (tid == 0) {
-        for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&kv_full[i], 32);
-            mbar_init(&kv_empty[i], 1);
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(&k_full[i], 32);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 32);
+            mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < NQH; ++i) {
             mbar_init(&s_full[i], 1);
@@ -278,7 +305,6 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
         const int qpos = first_pos + hh * TBQ + min(r, max(rows, 1) - 1);
         const uint32_t t_s = tmem + hh * C::HALF_COLS + ((uint32_t)(quad * 32) << 16);
         const uint32_t t_o = t_s + TBK;
-        unsigned char *sPh = sP + hh * C::P_BYTES;
         float m_run = -INFINITY, l_run = 0.0f;
         bool ok = true;
         for (int kt = 0; kt < my_tiles; ++kt) {
@@ -286,21 +312,31 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
             if (!ok)
                 break;
             tc_fence_after();
-            float v[TBK];
-            tmem_ld32(t_s, *reinterpret_cast<float(*)[32]>(v));
-            tmem_ld32(t_s + 32, *reinterpret_cast<float(*)[32]>(v + 32));
-            // scores of keys past this row's position (the tile crosses the
-            // diagonal) drop out
-            if (kt * TBK + TBK - 1 > first_pos + hh * TBQ) {
+            // keys past this row's position (the tile crosses the diagonal)
+            // drop out
+            const bool diag = kt * TBK + TBK - 1 > first_pos + hh * TBQ;
+            const int lim = qpos - kt * TBK;       // last unmasked column
+            // pass 1: the row maximum, 32 columns at a time
+            // (chunk loops stay rolled: the three roles share the
+            // instruction cache)
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int c0 = 0; c0 < TBK; c0 += 32) {
+                float v[32];
+                tmem_ld32(t_s + c0, v);
+                if (diag) {
 #pragma unroll
-                for (int j = 0; j < TBK; ++j)
-                    if (kt * TBK + j > qpos)
-                        v[j] = -INFINITY;
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j > lim)
+                            v[j] = -INFINITY;
+                }
+#pragma unroll
+                for (int w = 16; w > 0; w >>= 1)      // tree: 5 dependent steps
+#pragma unroll
+                    for (int j = 0; j < w; ++j)
+                        v[j] = fmaxf(v[j], v[j + w]);
+                mx = fmaxf(mx, v[0]);
             }
-            float mx = v[0];
-#pragma unroll
-            for (int j = 1; j < TBK; ++j)
-                mx = fmaxf(mx, v[j]);
             mx *= p.scale_log2;                    // scale > 0: the maximum commutes
             // The running maximum moves only when a score exceeds it by more
             // than 2^8 (or on the first tile): below that the weights stay
@@ -310,25 +346,10 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
             const float m_new = move ? fmaxf(m_run, mx) : m_run;
             const float corr = kt == 0 ? 1.0f : ex2_approx(m_run - m_new);
             m_run = m_new;
-            float sum = 0.0f;
-#pragma unroll
-            for (int j = 0; j < TBK; j += 8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float p0 = ex2_approx(fmaf(v[j + 2 * u], p.scale_log2, -m_new));
-                    const float p1 = ex2_approx(fmaf(v[j + 2 * u + 1], p.scale_log2, -m_new));
-                    sum += p0 + p1;
-                    w[u] = pack2<T>(p0, p1);
-                }
-                *reinterpret_cast<uint4 *>(sPh + core_off(r, j >> 3, TBK / 8)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            l_run = l_run * corr + sum;
             // O_h is idle here: the P V of the previous tile finished before
             // S_h(kt) did, the next one waits for p_full
             if (kt > 0 && __any_sync(FULL_MASK, move)) {
-#pragma unroll
+#pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     float o[32];
                     tmem_ld32(t_o + c0, o);
@@ -338,7 +359,36 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
                     tmem_st32(t_o + c0, o);
                 }
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // pass 2: weights, their sum, and P (keys 32c..32c+31 as 16-bit
+            // pairs in columns 16c..16c+15, over S columns already read)
+            float sum = 0.0f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < TBK; c0 += 32) {
+                float v[32];
+                tmem_ld32(t_s + c0, v);
+                if (diag) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j > lim)
+                            v[j] = -INFINITY;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = ex2_approx(fmaf(v[j], p.scale_log2, -m_new));
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    w[j] = pack2<T>(v[2 * j], v[2 * j + 1]);
+                tmem_st16(t_s + c0 / 2, w);
+#pragma unroll
+                for (int k = 16; k > 0; k >>= 1)      // tree sum
+#pragma unroll
+                    for (int j = 0; j < k; ++j)
+                        v[j] += v[j + k];
+                sum += v[0];
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            l_run = l_run * corr + sum;
             tc_fence_before();
             mbar_arrive(&p_full[hh]);
         }
@@ -349,7 +399,7 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
             const float inv = 1.0f / l_run;
             float *dst = p.out + ((int64_t)(q0 + qt * QT + hh * TBQ + min(r, max(rows, 1) - 1)) *
                                       p.num_q_heads + h) * D;
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 float o[32];
                 tmem_ld32(t_o + c0, o);
@@ -362,20 +412,25 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
             }
         }
     } else if (warp < MMA_WARP) {
-        // ================= producer warp pw: rows pw*64 .. pw*64+63 of Q, then
-        // K/V tiles pw, pw + NSTAGE, ... into stage pw.  Eight consecutive
-        // lanes fill one core matrix (8 rows x 16 B: a conflict-free 128-byte
-        // shared-memory write); a warp reads 64 contiguous bytes of 8 rows.
+        // ================= producer warp pw: rows pw*64 .. pw*64+63 of Q,
+        // then K (pw < NSLOT) or V tiles pw % NSLOT, pw % NSLOT + NSLOT, ...
+        // into slot pw % NSLOT.  Eight consecutive lanes fill one core matrix
+        // (8 rows x 16 B: a conflict-free 128-byte shared-memory write); a
+        // warp reads 64 contiguous bytes of 8 rows.
         const int pw = warp - SOFT_WARPS;
+        const int slot = pw % NSLOT;
+        const bool is_k = pw < NSLOT;
         const int rr = tid & 7, cq = (tid >> 3) & 3;
         constexpr int RG = TBK / 8;                // 8-row groups of a tile
         const T *qg = static_cast<const T *>(p.q);
-        const T *kg = static_cast<const T *>(p.k_cache);
-        const T *vg = static_cast<const T *>(p.v_cache);
+        const T *cache = static_cast<const T *>(is_k ? p.k_cache : p.v_cache);
+        unsigned char *ring = (is_k ? sK : sV) + slot * C::KV_BYTES;
+        uint64_t *full = is_k ? &k_full[slot] : &v_full[slot];
+        uint64_t *empty = is_k ? &k_empty[slot] : &v_empty[slot];
         const int32_t *table = p.block_tables + (int64_t)b * p.max_blocks_per_seq;
-#pragma unroll
-        for (int g = 0; g < RG; ++g) {
-            const int r = pw * TBK + g * 8 + rr;   // query of this CTA, 0..255
+#pragma unroll 1
+        for (int g = 0; g < QT / PROD_WARPS / 8; ++g) {
+            const int r = pw * (QT / PROD_WARPS) + g * 8 + rr;   // query of this CTA
             const bool ok = r < rows_all;
             const T *src = qg + ((int64_t)(q0 + qt * QT + (ok ? r : 0)) * p.num_q_heads + h) * D;
 #pragma unroll
@@ -384,37 +439,47 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
         }
         cp_async_commit();
         bool ok = true, q_sent = false;
-        for (int kt = pw; kt < ntiles; kt += NSTAGE) {
-            // block ids first (their loads overlap the wait for the stage)
-            int32_t blk[RG];
+        const int lane = tid & 31;
+        const bool wide = (TBK >> p.bs_log2) > 32;  // block size < 4: more than 32 blocks a tile
+        const int last_bi = last_pos >> p.bs_log2;
+        for (int kt = slot; kt < ntiles; kt += NSLOT) {
+            // the tile's block ids, entry e in lane e % 32, register e / 32
+            // (block sizes are powers of two: shifts, no divisions); the
+            // loads overlap the wait for the slot
+            const int b0 = (kt * TBK) >> p.bs_log2;
+            int32_t ids[4];
 #pragma unroll
-            for (int g = 0; g < RG; ++g) {
-                const int pos = kt * TBK + g * 8 + rr;
-                blk[g] = pos <= last_pos ? __ldg(table + (pos >> p.bs_log2)) : 0;
+            for (int k = 0; k < 4; ++k) {
+                const int bi = b0 + lane + 32 * k;
+                ids[k] = ((k == 0 || wide) && bi <= last_bi) ? __ldg(table + bi) : 0;
             }
-            if (kt >= NSTAGE && !wait(&kv_empty[pw], (uint32_t)(((kt / NSTAGE) & 1) ^ 1))) {
+            if (kt >= NSLOT && !wait(empty, (uint32_t)(((kt / NSLOT) & 1) ^ 1))) {
                 ok = false;
                 break;
             }
-            // block sizes are powers of two: shifts, no divisions
-#pragma unroll
+#pragma unroll 4
             for (int g = 0; g < RG; ++g) {
                 const int pos = kt * TBK + g * 8 + rr;
                 bool valid = pos <= last_pos;
+                const int e = (pos >> p.bs_log2) - b0;
+                int32_t blk = __shfl_sync(FULL_MASK, ids[0], e & 31);
+                if (wide) {
+                    const int32_t a1 = __shfl_sync(FULL_MASK, ids[1], e & 31);
+                    const int32_t a2 = __shfl_sync(FULL_MASK, ids[2], e & 31);
+                    const int32_t a3 = __shfl_sync(FULL_MASK, ids[3], e & 31);
+                    blk = e < 32 ? blk : e < 64 ? a1 : e < 96 ? a2 : a3;
+                }
                 int64_t row = 0;
-                if (valid && (blk[g] < 0 || blk[g] >= p.num_blocks)) {
+                if (valid && (blk < 0 || blk >= p.num_blocks)) {
                     atomicOr(p.err, PKV_EBIT_BLOCK);
                     valid = false;
                 } else if (valid) {
-                    row = (((int64_t)blk[g] * p.num_kv_heads + kvh) << p.bs_log2) +
+                    row = (((int64_t)blk * p.num_kv_heads + kvh) << p.bs_log2) +
                           (pos & (p.block_size - 1));
                 }
 #pragma unroll
-                for (int c = cq; c < DCH; c += 4) {
-                    const uint32_t o = pw * C::KV_BYTES + core_off(g * 8 + rr, c, DCH);
-                    cp_async16(sK + o, kg + row * D + c * 8, valid);
-                    cp_async16(sV + o, vg + row * D + c * 8, valid);
-                }
+                for (int c = cq; c < DCH; c += 4)
+                    cp_async16(ring + core_off(g * 8 + rr, c, DCH), cache + row * D + c * 8, valid);
             }
             cp_async_commit();
             if (!q_sent) {                         // Q (the older group) has landed
@@ -425,7 +490,7 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
             }
             cp_async_wait<0>();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&kv_full[pw]);
+            mbar_arrive(full);
         }
         cp_async_wait<0>();
         if (ok && !q_sent) {
@@ -436,33 +501,36 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
         // ================= MMA issue (one thread)
         const uint32_t idesc_s = umma_idesc(AB, 0u, TBK);
         const uint32_t idesc_o = umma_idesc(AB, 1u, D);
-        const uint32_t sQa = smem_addr(sQ), sKa = smem_addr(sK), sVa = smem_addr(sV),
-                       sPa = smem_addr(sP);
+        const uint32_t sQa = smem_addr(sQ), sKa = smem_addr(sK), sVa = smem_addr(sV);
         const int last_half = tiles_h[1] > 0 ? 1 : 0;   // the last reader of each K/V tile
         // S_hh = Q_hh K^T.  Q and K are K-major with DCH chunks a row:
         // K-direction core stride 128 B, row-group stride DCH*128 B; a K = 16
         // step is two chunks.
         auto issue_s = [&](int hh, int kt) {
-            const uint32_t kb = sKa + (kt % NSTAGE) * C::KV_BYTES, qb = sQa + hh * C::Q_BYTES;
+            const uint32_t kb = sKa + (kt % NSLOT) * C::KV_BYTES, qb = sQa + hh * C::Q_BYTES;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
                 umma_f16(tmem + hh * C::HALF_COLS, umma_desc(qb + ks * 256, 128, DCH * 128),
                          umma_desc(kb + ks * 256, 128, DCH * 128), idesc_s, ks > 0 ? 1u : 0u);
+            if (hh == last_half)
+                umma_commit(&k_empty[kt % NSLOT]);
             umma_commit(&s_full[hh]);
         };
-        // O_hh += P_hh V.  P: K-major, TBK/8 chunks a row.  V is the MN-major
-        // B: K (key) direction stride DCH*128 B per group of 8 keys, N (d)
-        // direction stride 128 B; a step of 16 keys is two key groups.
+        // O_hh += P_hh V.  P: in tensor memory over the S columns, 16 keys
+        // (a K step) per 8 columns.  V is the MN-major B: K (key) direction
+        // stride DCH*128 B per group of 8 keys, N (d) direction stride 128 B;
+        // a step of 16 keys is two key groups.
         auto issue_pv = [&](int hh, int kt) {
-            const uint32_t vb = sVa + (kt % NSTAGE) * C::KV_BYTES, pb = sPa + hh * C::P_BYTES;
+            const uint32_t vb = sVa + (kt % NSLOT) * C::KV_BYTES;
 #pragma unroll
             for (int ks = 0; ks < TBK / 16; ++ks)
-                umma_f16(tmem + hh * C::HALF_COLS + TBK,
-                         umma_desc(pb + ks * 256, 128, (TBK / 8) * 128),
-                         umma_desc(vb + ks * 2 * DCH * 128, DCH * 128, 128), idesc_o,
-                         (kt > 0 || ks > 0) ? 1u : 0u);
+                umma_f16_ta(tmem + hh * C::HALF_COLS + TBK, tmem + hh * C::HALF_COLS + ks * 8,
+                            umma_desc(vb + ks * 2 * DCH * 128, DCH * 128, 128), idesc_o,
+                            (kt > 0 || ks > 0) ? 1u : 0u);
+            if (hh == last_half)
+                umma_commit(&v_empty[kt % NSLOT]);
         };
-        bool ok = wait(q_full, 0u) && wait(&kv_full[0], 0u);
+        bool ok = wait(q_full, 0u) && wait(&k_full[0], 0u);
         if (ok) {
             tc_fence_after();
             for (int hh = 0; hh < NQH; ++hh)
@@ -473,14 +541,13 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
             for (int hh = 0; hh < NQH; ++hh) {
                 if (kt >= tiles_h[hh])
                     continue;
-                if (!(ok = wait(&p_full[hh], (uint32_t)(kt & 1))))
+                if (!(ok = wait(&p_full[hh], (uint32_t)(kt & 1)) &&
+                           wait(&v_full[kt % NSLOT], (uint32_t)((kt / NSLOT) & 1))))
                     break;
                 tc_fence_after();
                 issue_pv(hh, kt);
-                if (hh == last_half)
-                    umma_commit(&kv_empty[kt % NSTAGE]);
                 if (kt + 1 < tiles_h[hh]) {
-                    if (!(ok = wait(&kv_full[(kt + 1) % NSTAGE], (uint32_t)(((kt + 1) / NSTAGE) & 1))))
+                    if (!(ok = wait(&k_full[(kt + 1) % NSLOT], (uint32_t)(((kt + 1) / NSLOT) & 1))))
                         break;
                     tc_fence_after();
                     issue_s(hh, kt + 1);
