@@ -237,6 +237,16 @@ __device__ __forceinline__ void load_q(QRegs<D, G, KV> &qr, const unsigned char 
         }
 }
 
+// (a0, a1) += (b0, b1) * (c0, c1) as one packed fp32x2 FMA.
+__device__ __forceinline__ void fma2(float &a0, float &a1, float b0, float b1, float c0, float c1)
+{
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%0, %1};\n\t"
+        "fma.rn.f32x2 z, x, y, z;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // This lane's K chunks of a tile: chunk ds + DS*c of token tq + TQ*ii.
 template <int D, int G, int KV>
 __device__ __forceinline__ void load_k(uint4 (&kr)[Cfg<D, G, KV>::TPL][Cfg<D, G, KV>::CPL],
@@ -307,23 +317,24 @@ __device__ __forceinline__ void qk_tile(float (&part)[Cfg<D, G, KV>::NP],
                                                          part[ii * G + g]);
                     }
             } else {
+                // codes -> exact floats two at a time; the dot products as
+                // packed fp32x2 FMAs over element pairs (two partial sums per
+                // head, added at the end of the chunk)
                 float kf[16];
                 const uint32_t wds[4] = {kw.x ^ 0x80808080u, kw.y ^ 0x80808080u,
                                          kw.z ^ 0x80808080u, kw.w ^ 0x80808080u};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    kf[4 * u + 0] = i8_to_float<0>(wds[u]);
-                    kf[4 * u + 1] = i8_to_float<1>(wds[u]);
-                    kf[4 * u + 2] = i8_to_float<2>(wds[u]);
-                    kf[4 * u + 3] = i8_to_float<3>(wds[u]);
+                    i8pair_to_float2<0>(wds[u], kf[4 * u + 0], kf[4 * u + 1]);
+                    i8pair_to_float2<1>(wds[u], kf[4 * u + 2], kf[4 * u + 3]);
                 }
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    float a = part[ii * G + g];
+                    float a0 = part[ii * G + g], a1 = 0.0f;
 #pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        a = fmaf(qr.w[g][c][u], kf[u], a);
-                    part[ii * G + g] = a;
+                    for (int u = 0; u < 16; u += 2)
+                        fma2(a0, a1, qr.w[g][c][u], qr.w[g][c][u + 1], kf[u], kf[u + 1]);
+                    part[ii * G + g] = a0 + a1;
                 }
             }
         }
@@ -398,11 +409,11 @@ __device__ __forceinline__ void load_v(float (&v)[D / 32], const unsigned char *
     } else {
         if constexpr (VE == 4) {
             const uint32_t b = *reinterpret_cast<const uint32_t *>(p) ^ 0x80808080u;
-            v[0] = i8_to_float<0>(b); v[1] = i8_to_float<1>(b);
-            v[2] = i8_to_float<2>(b); v[3] = i8_to_float<3>(b);
+            i8pair_to_float2<0>(b, v[0], v[1]);
+            i8pair_to_float2<1>(b, v[2], v[3]);
         } else {
             const uint32_t b = (uint32_t)(*reinterpret_cast<const uint16_t *>(p)) ^ 0x8080u;
-            v[0] = i8_to_float<0>(b); v[1] = i8_to_float<1>(b);
+            i8pair_to_float2<0>(b, v[0], v[1]);
         }
     }
 }
@@ -460,11 +471,11 @@ __device__ __forceinline__ void unpack_v(float (&v)[D / 32], typename VRaw<D, KV
     } else {
         if constexpr (VE == 4) {
             const uint32_t b = raw ^ 0x80808080u;
-            v[0] = i8_to_float<0>(b); v[1] = i8_to_float<1>(b);
-            v[2] = i8_to_float<2>(b); v[3] = i8_to_float<3>(b);
+            i8pair_to_float2<0>(b, v[0], v[1]);
+            i8pair_to_float2<1>(b, v[2], v[3]);
         } else {
             const uint32_t b = raw ^ 0x8080u;
-            v[0] = i8_to_float<0>(b); v[1] = i8_to_float<1>(b);
+            i8pair_to_float2<0>(b, v[0], v[1]);
         }
     }
 }
@@ -475,16 +486,6 @@ __device__ __forceinline__ float exp2_approx(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// (a0, a1) += (b0, b1) * (c0, c1) as one packed fp32x2 FMA.
-__device__ __forceinline__ void fma2(float &a0, float &a1, float b0, float b1, float c0, float c1)
-{
-    asm("{\n\t.reg .b64 x, y, z;\n\t"
-        "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%0, %1};\n\t"
-        "fma.rn.f32x2 z, x, y, z;\n\tmov.b64 {%0, %1}, z;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
 // ---- the kernel ---------------------------------------------------------------

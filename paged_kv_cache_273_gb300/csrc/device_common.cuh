@@ -215,13 +215,18 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t w)
     return __half22float2(h);
 }
 
-// Byte i (0..3) of a word of four int8 codes -> exact float, via the biased
-// byte placed in the mantissa of 2^23 (code + 128 + 2^23) minus (2^23 + 128).
-template <int I>
-__device__ __forceinline__ float i8_to_float(uint32_t biased)
+// Bytes 2J and 2J+1 of a word of biased int8 codes -> two exact floats: each
+// biased byte becomes the low mantissa bits of 2^23, and one packed add takes
+// 2^23 + 128 off both.
+template <int J>
+__device__ __forceinline__ void i8pair_to_float2(uint32_t biased, float &lo, float &hi)
 {
-    const uint32_t f = __byte_perm(biased, 0x4B000000u, 0x7440u + I);
-    return __uint_as_float(f) - 8388736.0f;
+    const float a = __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7440u + 2 * J));
+    const float b = __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7441u + 2 * J));
+    asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\t"
+        "add.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "f"(a), "f"(b), "f"(-8388736.0f));
 }
 
 // 4-bit two's-complement codes, code j of a word in bits 4j..4j+3.
