@@ -440,19 +440,14 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
         cp_async_commit();
         bool ok = true, q_sent = false;
         const int lane = tid & 31;
-        const bool wide = (TBK >> p.bs_log2) > 32;  // block size < 4: more than 32 blocks a tile
         const int last_bi = last_pos >> p.bs_log2;
         for (int kt = slot; kt < ntiles; kt += NSLOT) {
-            // the tile's block ids, entry e in lane e % 32, register e / 32
-            // (block sizes are powers of two: shifts, no divisions); the
-            // loads overlap the wait for the slot
+            // the tile's block ids, entry e in lane e: pool blocks hold at
+            // least 4 rows, so a 128-key tile spans at most 32 of them (block
+            // sizes are powers of two: shifts, no divisions); the loads
+            // overlap the wait for the slot
             const int b0 = (kt * TBK) >> p.bs_log2;
-            int32_t ids[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int bi = b0 + lane + 32 * k;
-                ids[k] = ((k == 0 || wide) && bi <= last_bi) ? __ldg(table + bi) : 0;
-            }
+            const int32_t ids = b0 + lane <= last_bi ? __ldg(table + b0 + lane) : 0;
             if (kt >= NSLOT && !wait(empty, (uint32_t)(((kt / NSLOT) & 1) ^ 1))) {
                 ok = false;
                 break;
@@ -461,14 +456,7 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
             for (int g = 0; g < RG; ++g) {
                 const int pos = kt * TBK + g * 8 + rr;
                 bool valid = pos <= last_pos;
-                const int e = (pos >> p.bs_log2) - b0;
-                int32_t blk = __shfl_sync(FULL_MASK, ids[0], e & 31);
-                if (wide) {
-                    const int32_t a1 = __shfl_sync(FULL_MASK, ids[1], e & 31);
-                    const int32_t a2 = __shfl_sync(FULL_MASK, ids[2], e & 31);
-                    const int32_t a3 = __shfl_sync(FULL_MASK, ids[3], e & 31);
-                    blk = e < 32 ? blk : e < 64 ? a1 : e < 96 ? a2 : a3;
-                }
+                const int32_t blk = __shfl_sync(FULL_MASK, ids, ((pos >> p.bs_log2) - b0) & 31);
                 int64_t row = 0;
                 if (valid && (blk < 0 || blk >= p.num_blocks)) {
                     atomicOr(p.err, PKV_EBIT_BLOCK);

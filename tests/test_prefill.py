@@ -163,6 +163,7 @@ def _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, seed):
     ("f16", 128, 16, 2, 32, [129, 5, 64], [0, 300, 64]),
     ("f16", 128, 8, 8, 16, [1], [1]),
     ("bf16", 64, 8, 4, 8, [300, 513, 256], [17, 0, 40]),
+    ("bf16", 128, 4, 2, 256, [700, 3], [300, 509]),
 ])
 def test_gpu_prefill_matches_oracle(dt, D, Hq, Hkv, bs, news, cached):
     from paged_kv_cache_273_gb300 import pkv
