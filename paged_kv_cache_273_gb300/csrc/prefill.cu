@@ -9,6 +9,8 @@
 // "Concept"), in FlashAttention-style tiles that never hold the whole score
 // matrix ("Flash attention: don't build the giant matrix" in the guide).
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -46,6 +48,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 }
 
 struct PrefillParams {
+    // K and V caches as 3-D tensors {D, block_size, num_blocks * num_kv_heads}
+    // for the tensor-memory-access unit: boxes of 64 x min(block_size, 128)
+    // rows, 128-byte swizzle
+    CUtensorMap tm_k, tm_v;
     const void *q;
     const void *k_cache;
     const void *v_cache;
@@ -55,6 +61,7 @@ struct PrefillParams {
     float *out;
     unsigned int *err;
     int batch, num_q_heads, num_kv_heads, block_size, bs_log2, max_blocks_per_seq, num_blocks;
+    int box_rows;       // min(block_size, 128)
     float scale_log2;
 };
 
@@ -63,11 +70,14 @@ struct PrefillParams {
 // A CTA takes 256 queries of one (sequence, query head) as two 128-row
 // halves A and B that share every K/V tile (one CTA per SM), with three
 // roles:
-//  * four producer warps copy a quarter of Q each, then K tiles (warps 0, 1)
-//    and V tiles (warps 2, 3) into two-slot rings in shared memory with
-//    16-byte cp.async copies, each key row located through the block table,
-//    in the tensor cores' core-matrix layout (8 rows x 16 bytes per 128-byte
-//    core matrix, no swizzle);
+//  * four producer warps copy a quarter of Q each with 16-byte cp.async
+//    copies into the tensor cores' core-matrix layout (8 rows x 16 bytes per
+//    128-byte core matrix, no swizzle); then warps 0, 1 bring K tiles and
+//    warps 2, 3 V tiles into two-slot rings, 128-byte swizzled (row r of a
+//    64-column panel at 128 r, its 16-byte chunks permuted by r mod 8):
+//    one tensor-memory-access copy per cache block and panel (lane j takes
+//    the j-th block of the tile), 16-byte cp.async copies for blocks of 4
+//    rows and for the block where the sequence ends;
 //  * one thread issues the tcgen05.mma: S = Q K^T (M 128, N 128, K = D, both
 //    operands in shared memory) and O += P V (M 128, N = D, K 128, P read
 //    from tensor memory) per half, fp32 accumulators in tensor memory (half
@@ -113,6 +123,24 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
 {
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+
+// The same for a 128-byte swizzled operand (layout type 2 in bits 61-63).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return umma_desc(saddr, lbo, sbo) | ((uint64_t)2 << 61);
+}
+
+// One box of a 3-D tensor map into shared memory, completion counted in bytes
+// on an mbarrier.  Coordinates past the tensor's end read zeros.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulate, A/B fp16 (0) or
@@ -211,7 +239,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16
 }
 
 template <int D, typename T>
-__global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillParams p)
+__global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_constant__ PrefillParams p)
 {
     using C = TcCfg<D>;
     constexpr uint32_t AB = MmaType<T>::bf16 ? 1u : 0u;
@@ -261,9 +289,9 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
 
     if (tid == 0) {
         for (int i = 0; i < NSLOT; ++i) {
-            mbar_init(&k_full[i], 32);
+            mbar_init(&k_full[i], 2);              // tensor-copy bytes + the 16-byte copies
             mbar_init(&k_empty[i], 1);
-            mbar_init(&v_full[i], 32);
+            mbar_init(&v_full[i], 2);
             mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < NQH; ++i) {
@@ -421,9 +449,7 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
         const int slot = pw % NSLOT;
         const bool is_k = pw < NSLOT;
         const int rr = tid & 7, cq = (tid >> 3) & 3;
-        constexpr int RG = TBK / 8;                // 8-row groups of a tile
         const T *qg = static_cast<const T *>(p.q);
-        const T *cache = static_cast<const T *>(is_k ? p.k_cache : p.v_cache);
         unsigned char *ring = (is_k ? sK : sV) + slot * C::KV_BYTES;
         uint64_t *full = is_k ? &k_full[slot] : &v_full[slot];
         uint64_t *empty = is_k ? &k_empty[slot] : &v_empty[slot];
@@ -440,45 +466,74 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
         cp_async_commit();
         bool ok = true, q_sent = false;
         const int lane = tid & 31;
-        const int last_bi = last_pos >> p.bs_log2;
+        const CUtensorMap *tm = is_k ? &p.tm_k : &p.tm_v;
+        const T *cache = static_cast<const T *>(is_k ? p.k_cache : p.v_cache);
+        const int R = p.box_rows;                  // rows of one box: min(block size, 128)
+        const int nbox = TBK / R;                  // boxes a tile: at most 32 (blocks >= 4 rows)
+        const int oob = p.num_blocks * p.num_kv_heads;   // a block index past the end: zero fill
         for (int kt = slot; kt < ntiles; kt += NSLOT) {
-            // the tile's block ids, entry e in lane e: pool blocks hold at
-            // least 4 rows, so a 128-key tile spans at most 32 of them (block
-            // sizes are powers of two: shifts, no divisions); the loads
-            // overlap the wait for the slot
-            const int b0 = (kt * TBK) >> p.bs_log2;
-            const int32_t ids = b0 + lane <= last_bi ? __ldg(table + b0 + lane) : 0;
+            // lane j: rows [j R, j R + R) of the tile, one cache block (block
+            // sizes are powers of two: shifts, no divisions); the block-id
+            // load overlaps the wait for the slot
+            const int pos0 = kt * TBK + lane * R;
+            const bool inbox = lane < nbox;
+            const bool live = inbox && pos0 <= last_pos;
+            const int32_t blk = live ? __ldg(table + (pos0 >> p.bs_log2)) : 0;
             if (kt >= NSLOT && !wait(empty, (uint32_t)(((kt / NSLOT) & 1) ^ 1))) {
                 ok = false;
                 break;
             }
-#pragma unroll 4
-            for (int g = 0; g < RG; ++g) {
-                const int pos = kt * TBK + g * 8 + rr;
-                bool valid = pos <= last_pos;
-                const int32_t blk = __shfl_sync(FULL_MASK, ids, ((pos >> p.bs_log2) - b0) & 31);
-                int64_t row = 0;
-                if (valid && (blk < 0 || blk >= p.num_blocks)) {
+            int z = oob;
+            if (live) {
+                if (blk < 0 || blk >= p.num_blocks)
                     atomicOr(p.err, PKV_EBIT_BLOCK);
-                    valid = false;
-                } else if (valid) {
-                    row = (((int64_t)blk * p.num_kv_heads + kvh) << p.bs_log2) +
-                          (pos & (p.block_size - 1));
-                }
-#pragma unroll
-                for (int c = cq; c < DCH; c += 4)
-                    cp_async16(ring + core_off(g * 8 + rr, c, DCH), cache + row * D + c * 8, valid);
+                else
+                    z = blk * p.num_kv_heads + kvh;
             }
-            cp_async_commit();
-            if (!q_sent) {                         // Q (the older group) has landed
-                cp_async_wait<1>();
+            const int y = pos0 & (p.block_size - 1);
+            // A box goes by one tensor copy per 64-column panel when it starts
+            // on a 1024-byte boundary (boxes of >= 8 rows) and holds no row
+            // past the sequence end (those must be zeros: P is 0 there, but 0
+            // times a stale NaN is not); the other boxes go by 16-byte copies.
+            const bool by_tma = inbox && R >= 8 && (z == oob || pos0 + R - 1 <= last_pos);
+            const unsigned tma_boxes = __popc(__ballot_sync(FULL_MASK, by_tma));
+            const unsigned cp_boxes = __ballot_sync(FULL_MASK, inbox && !by_tma);
+            if (lane == 0)
+                mbar_arrive_expect_tx(full, tma_boxes * (uint32_t)R * 2u * D);
+            __syncwarp();
+            if (by_tma) {
+#pragma unroll
+                for (int pn = 0; pn < D / 64; ++pn)
+                    tma_load_3d(ring + pn * (TBK * 128) + lane * R * 128, tm, pn * 64, y, z, full);
+            }
+            if (cp_boxes) {
+                // chunk c of tile row r lands at 128 r + 16 (c mod 8 xor r mod 8)
+                // in panel c / 8 (the pattern of the 128-byte swizzle)
+                for (unsigned m = cp_boxes; m; m &= m - 1) {
+                    const int bx = __ffs(m) - 1;
+                    const int zb = __shfl_sync(FULL_MASK, z, bx);
+                    const int yb = __shfl_sync(FULL_MASK, y, bx);
+                    for (int idx = lane; idx < R * DCH; idx += 32) {
+                        const int r = bx * R + idx / DCH, c = idx % DCH;
+                        const bool valid = zb != oob && kt * TBK + r <= last_pos;
+                        const int64_t row = valid ? (int64_t)zb * p.block_size + yb + idx / DCH : 0;
+                        cp_async16(ring + (c >> 3) * (TBK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+                                   cache + row * D + c * 8, valid);
+                    }
+                }
+                cp_async_commit();
+                cp_async_wait<0>();
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            __syncwarp();
+            if (lane == 0)                         // the 16-byte copies (if any) have landed
+                mbar_arrive(full);
+            if (!q_sent) {                         // Q (this thread's cp.async group) has landed
+                cp_async_wait<0>();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(q_full);
                 q_sent = true;
             }
-            cp_async_wait<0>();
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(full);
         }
         cp_async_wait<0>();
         if (ok && !q_sent) {
@@ -491,29 +546,32 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const PrefillP
         const uint32_t idesc_o = umma_idesc(AB, 1u, D);
         const uint32_t sQa = smem_addr(sQ), sKa = smem_addr(sK), sVa = smem_addr(sV);
         const int last_half = tiles_h[1] > 0 ? 1 : 0;   // the last reader of each K/V tile
-        // S_hh = Q_hh K^T.  Q and K are K-major with DCH chunks a row:
-        // K-direction core stride 128 B, row-group stride DCH*128 B; a K = 16
-        // step is two chunks.
+        // S_hh = Q_hh K^T, both K-major.  Q: core-matrix layout with DCH
+        // chunks a row (K-direction core stride 128 B, row-group stride
+        // DCH*128 B; a K = 16 step is two chunks).  K: 128-byte swizzled
+        // panels of 64 d (8-row groups 1024 B apart); a K = 16 step is 32 B
+        // into the panel's rows.
         auto issue_s = [&](int hh, int kt) {
             const uint32_t kb = sKa + (kt % NSLOT) * C::KV_BYTES, qb = sQa + hh * C::Q_BYTES;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
                 umma_f16(tmem + hh * C::HALF_COLS, umma_desc(qb + ks * 256, 128, DCH * 128),
-                         umma_desc(kb + ks * 256, 128, DCH * 128), idesc_s, ks > 0 ? 1u : 0u);
+                         umma_desc_sw128(kb + (ks / 4) * (TBK * 128) + (ks % 4) * 32, 16, 1024),
+                         idesc_s, ks > 0 ? 1u : 0u);
             if (hh == last_half)
                 umma_commit(&k_empty[kt % NSLOT]);
             umma_commit(&s_full[hh]);
         };
         // O_hh += P_hh V.  P: in tensor memory over the S columns, 16 keys
-        // (a K step) per 8 columns.  V is the MN-major B: K (key) direction
-        // stride DCH*128 B per group of 8 keys, N (d) direction stride 128 B;
-        // a step of 16 keys is two key groups.
+        // (a K step) per 8 columns.  V is the MN-major B in 128-byte swizzled
+        // panels: a key row of 64 d every 128 B, 8-key groups 1024 B apart,
+        // the next 64 d a panel (TBK*128 B) on; a step of 16 keys is 2048 B.
         auto issue_pv = [&](int hh, int kt) {
             const uint32_t vb = sVa + (kt % NSLOT) * C::KV_BYTES;
 #pragma unroll
             for (int ks = 0; ks < TBK / 16; ++ks)
                 umma_f16_ta(tmem + hh * C::HALF_COLS + TBK, tmem + hh * C::HALF_COLS + ks * 8,
-                            umma_desc(vb + ks * 2 * DCH * 128, DCH * 128, 128), idesc_o,
+                            umma_desc_sw128(vb + ks * 2048, TBK * 128, 1024), idesc_o,
                             (kt > 0 || ks > 0) ? 1u : 0u);
             if (hh == last_half)
                 umma_commit(&v_empty[kt % NSLOT]);
@@ -582,6 +640,41 @@ int launch_prefill_t(const pkv_pool *pool, const PrefillParams &prm, int max_q_l
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// A cache [num_blocks][num_kv_heads][block_size][D] of 16-bit elements as the
+// 3-D tensor {D, block_size, num_blocks * num_kv_heads}, boxes of 64 x rows x 1.
+bool encode_cache_map(CUtensorMap *m, const pkv_pool *pool, const void *base, int rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const int D = pool->head_dim, bs = pool->block_size;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)bs,
+                                (cuuint64_t)pool->num_blocks * (cuuint64_t)pool->num_kv_heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)bs * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = pool->kv_dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int launch_prefill(const pkv_pool *pool, const void *q, int num_q_heads, const void *k_cache,
@@ -608,6 +701,10 @@ int launch_prefill(const pkv_pool *pool, const void *q, int num_q_heads, const v
     prm.max_blocks_per_seq = max_blocks_per_seq;
     prm.num_blocks = pool->num_blocks;
     prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    prm.box_rows = pool->block_size < TBK ? pool->block_size : TBK;
+    if (!encode_cache_map(&prm.tm_k, pool, k_cache, prm.box_rows) ||
+        !encode_cache_map(&prm.tm_v, pool, v_cache, prm.box_rows))
+        return PKV_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool bf = pool->kv_dtype == PKV_BF16;
     if (pool->head_dim == 64)
