@@ -62,6 +62,7 @@ struct PrefillParams {
     unsigned int *err;
     int batch, num_q_heads, num_kv_heads, block_size, bs_log2, max_blocks_per_seq, num_blocks;
     int box_rows;       // min(block_size, 128)
+    int nqt;            // query tiles of 256 per sequence: ceil(max_q_len / 256)
     float scale_log2;
 };
 
@@ -104,7 +105,7 @@ struct TcCfg {
     static constexpr int Q_BYTES = TBQ * D * 2;          // one half
     static constexpr int KV_BYTES = TBK * D * 2;          // one K or V tile
     static constexpr int BAR_OFF = NQH * Q_BYTES + 2 * NSLOT * KV_BYTES;
-    static constexpr int NBARS = 4 * NSLOT + 3 * NQH + 2;
+    static constexpr int NBARS = 4 * NSLOT + 4 * NQH + 3;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16;
     static constexpr int TMEM_COLS = 512;
     static constexpr int HALF_COLS = 256;                 // >= TBK + D
@@ -238,13 +239,50 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16
                  : "memory");
 }
 
+// One unit of work: 256 queries (two halves of 128) of sequence b, query
+// head h, query tile qt.  Items are numbered longest (latest) tiles first;
+// every role of a CTA derives the same items in the same order.
+struct Item {
+    int b, h, qt, q0, kvh, rows_all, first_pos, last_pos, ntiles;
+    int rows_h[NQH], tiles_h[NQH];
+    bool live;       // has rows and valid lengths
+    bool bad_len;    // has rows but its length fields are inconsistent
+};
+
+__device__ __forceinline__ Item make_item(const PrefillParams &p, int i)
+{
+    constexpr int QT = NQH * TBQ;
+    Item it;
+    const int per = p.num_q_heads * p.batch;
+    const int qt_rev = i / per, rem = i - qt_rev * per;
+    it.qt = p.nqt - 1 - qt_rev;
+    it.b = rem % p.batch;
+    it.h = rem / p.batch;
+    it.q0 = __ldg(p.q_start + it.b);
+    const int n = __ldg(p.q_start + it.b + 1) - it.q0;
+    const int L = __ldg(p.seq_lens + it.b);
+    const bool rows = it.qt * QT < n;
+    it.bad_len = rows && (L < n || L > p.max_blocks_per_seq * p.block_size);
+    it.live = rows && !it.bad_len;
+    it.kvh = it.h / (p.num_q_heads / p.num_kv_heads);
+    it.rows_all = it.live ? min(QT, n - it.qt * QT) : 0;
+    it.first_pos = L - n + it.qt * QT;              // position of the item's first query
+    it.last_pos = it.first_pos + it.rows_all - 1;
+    it.ntiles = it.live ? it.last_pos / TBK + 1 : 0;
+    it.rows_h[0] = min(TBQ, it.rows_all);
+    it.rows_h[1] = max(0, it.rows_all - TBQ);
+    it.tiles_h[0] = it.live ? (it.first_pos + it.rows_h[0] - 1) / TBK + 1 : 0;
+    it.tiles_h[1] = it.rows_h[1] > 0 ? it.ntiles : 0;
+    return it;
+}
+
 template <int D, typename T>
 __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_constant__ PrefillParams p)
 {
     using C = TcCfg<D>;
     constexpr uint32_t AB = MmaType<T>::bf16 ? 1u : 0u;
     constexpr int DCH = D / 8;                    // 16-byte chunks of a D-wide row
-    constexpr int QT = NQH * TBQ;                 // queries of this CTA
+    constexpr int QT = NQH * TBQ;                 // queries of an item
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sQ = smem_raw;                              // NQH halves
     unsigned char *sK = sQ + NQH * C::Q_BYTES;                 // NSLOT K tiles
@@ -256,35 +294,17 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
     uint64_t *s_full = v_empty + NSLOT;
     uint64_t *p_full = s_full + NQH;
     uint64_t *o_done = p_full + NQH;
-    uint64_t *q_full = o_done + NQH;
-    uint64_t *drain = q_full + 1;
+    uint64_t *o_free = o_done + NQH;
+    uint64_t *q_full = o_free + NQH;
+    uint64_t *q_empty = q_full + 1;
+    uint64_t *drain = q_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     grid_dependency_wait();
     grid_dependents_launch();
 
-    const int b = blockIdx.z;
-    const int h = blockIdx.y;
-    const int qt = gridDim.x - 1 - blockIdx.x;    // long (late) query tiles first
-    const int q0 = __ldg(p.q_start + b);
-    const int n = __ldg(p.q_start + b + 1) - q0;
-    const int L = __ldg(p.seq_lens + b);
-    if (qt * QT >= n)
-        return;
-    if (L < n || L > p.max_blocks_per_seq * p.block_size) {
-        if (threadIdx.x == 0 && qt == 0 && h == 0)
-            atomicOr(p.err, PKV_EBIT_SEQLEN);
-        return;
-    }
-    const int kvh = h / (p.num_q_heads / p.num_kv_heads);
-    const int rows_all = min(QT, n - qt * QT);
-    const int first_pos = L - n + qt * QT;         // position of this CTA's first query
-    const int last_pos = first_pos + rows_all - 1;
-    const int ntiles = last_pos / TBK + 1;
-    // rows and key tiles of each half (the second may be empty)
-    const int rows_h[NQH] = {min(TBQ, rows_all), max(0, rows_all - TBQ)};
-    const int tiles_h[NQH] = {(first_pos + rows_h[0] - 1) / TBK + 1, rows_h[1] > 0 ? ntiles : 0};
+    const int nitems = p.nqt * p.num_q_heads * p.batch;
     const int tid = threadIdx.x, warp = tid >> 5;
 
     if (tid == 0) {
@@ -298,8 +318,10 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], TBQ);
             mbar_init(&o_done[i], 1);
+            mbar_init(&o_free[i], TBQ);
         }
         mbar_init(q_full, PROD_WARPS * 32);
+        mbar_init(q_empty, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -329,278 +351,336 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
         // ================= softmax: one thread per query row of half hh
         const int hh = warp >> 2, quad = warp & 3;
         const int r = quad * 32 + (tid & 31);
-        const int rows = rows_h[hh], my_tiles = tiles_h[hh];
-        const int qpos = first_pos + hh * TBQ + min(r, max(rows, 1) - 1);
         const uint32_t t_s = tmem + hh * C::HALF_COLS + ((uint32_t)(quad * 32) << 16);
         const uint32_t t_o = t_s + TBK;
-        float m_run = -INFINITY, l_run = 0.0f;
-        bool ok = true;
-        for (int kt = 0; kt < my_tiles; ++kt) {
-            ok = __all_sync(FULL_MASK, wait(&s_full[hh], (uint32_t)(kt & 1)));
-            if (!ok)
-                break;
-            tc_fence_after();
-            // keys past this row's position (the tile crosses the diagonal)
-            // drop out
-            const bool diag = kt * TBK + TBK - 1 > first_pos + hh * TBQ;
-            const int lim = qpos - kt * TBK;       // last unmasked column
-            // pass 1: the row maximum, 32 columns at a time
-            // (chunk loops stay rolled: the three roles share the
-            // instruction cache)
-            float mx = -INFINITY;
+        uint32_t sc = 0, od = 0;                   // phases used of s_full[hh], o_done[hh]
+        for (int i = blockIdx.x; i < nitems; i += gridDim.x) {
+            const Item it = make_item(p, i);
+            const int rows = it.rows_h[hh], my_tiles = it.tiles_h[hh];
+            if (my_tiles == 0)
+                continue;
+            const int qpos = it.first_pos + hh * TBQ + min(r, max(rows, 1) - 1);
+            float m_run = -INFINITY, l_run = 0.0f;
+            for (int kt = 0; kt < my_tiles; ++kt) {
+                if (!__all_sync(FULL_MASK, wait(&s_full[hh], sc & 1)))
+                    goto softmax_done;
+                ++sc;
+                tc_fence_after();
+                // keys past this row's position (the tile crosses the
+                // diagonal) drop out
+                const bool diag = kt * TBK + TBK - 1 > it.first_pos + hh * TBQ;
+                const int lim = qpos - kt * TBK;   // last unmasked column
+                // pass 1: the row maximum, 32 columns at a time (chunk loops
+                // stay rolled: the three roles share the instruction cache)
+                float mx = -INFINITY;
 #pragma unroll 1
-            for (int c0 = 0; c0 < TBK; c0 += 32) {
-                float v[32];
-                tmem_ld32(t_s + c0, v);
-                if (diag) {
+                for (int c0 = 0; c0 < TBK; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(t_s + c0, v);
+                    if (diag) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c0 + j > lim)
+                                v[j] = -INFINITY;
+                    }
+#pragma unroll
+                    for (int w = 16; w > 0; w >>= 1)   // tree: 5 dependent steps
+#pragma unroll
+                        for (int j = 0; j < w; ++j)
+                            v[j] = fmaxf(v[j], v[j + w]);
+                    mx = fmaxf(mx, v[0]);
+                }
+                mx *= p.scale_log2;                // scale > 0: the maximum commutes
+                // The running maximum moves only when a score exceeds it by
+                // more than 2^8 (or on the first tile): below that the weights
+                // stay <= 256, exact in fp32 and representable in fp16/bf16,
+                // and the final division by the sum of the same weights is
+                // unchanged.
+                const bool move = kt == 0 || mx > m_run + 8.0f;
+                const float m_new = move ? fmaxf(m_run, mx) : m_run;
+                const float corr = kt == 0 ? 1.0f : ex2_approx(m_run - m_new);
+                m_run = m_new;
+                // O_h is idle here: the P V of the previous tile finished
+                // before S_h(kt) did, the next one waits for p_full
+                if (kt > 0 && __any_sync(FULL_MASK, move)) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        float o[32];
+                        tmem_ld32(t_o + c0, o);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            o[j] *= corr;
+                        tmem_st32(t_o + c0, o);
+                    }
+                }
+                // pass 2: weights, their sum, and P (keys 32c..32c+31 as
+                // 16-bit pairs in columns 16c..16c+15, over S columns already
+                // read)
+                float sum = 0.0f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < TBK; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(t_s + c0, v);
+                    if (diag) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c0 + j > lim)
+                                v[j] = -INFINITY;
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (c0 + j > lim)
-                            v[j] = -INFINITY;
+                        v[j] = ex2_approx(fmaf(v[j], p.scale_log2, -m_new));
+                    uint32_t w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        w[j] = pack2<T>(v[2 * j], v[2 * j + 1]);
+                    tmem_st16(t_s + c0 / 2, w);
+#pragma unroll
+                    for (int k = 16; k > 0; k >>= 1)   // tree sum
+#pragma unroll
+                        for (int j = 0; j < k; ++j)
+                            v[j] += v[j + k];
+                    sum += v[0];
                 }
-#pragma unroll
-                for (int w = 16; w > 0; w >>= 1)      // tree: 5 dependent steps
-#pragma unroll
-                    for (int j = 0; j < w; ++j)
-                        v[j] = fmaxf(v[j], v[j + w]);
-                mx = fmaxf(mx, v[0]);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                l_run = l_run * corr + sum;
+                tc_fence_before();
+                mbar_arrive(&p_full[hh]);
             }
-            mx *= p.scale_log2;                    // scale > 0: the maximum commutes
-            // The running maximum moves only when a score exceeds it by more
-            // than 2^8 (or on the first tile): below that the weights stay
-            // <= 256, exact in fp32 and representable in fp16/bf16, and the
-            // final division by the sum of the same weights is unchanged.
-            const bool move = kt == 0 || mx > m_run + 8.0f;
-            const float m_new = move ? fmaxf(m_run, mx) : m_run;
-            const float corr = kt == 0 ? 1.0f : ex2_approx(m_run - m_new);
-            m_run = m_new;
-            // O_h is idle here: the P V of the previous tile finished before
-            // S_h(kt) did, the next one waits for p_full
-            if (kt > 0 && __any_sync(FULL_MASK, move)) {
+            // ---- O / l (warp-uniform: the TMEM loads run converged; padding
+            // rows load without storing), then O_h is free for the next item
+            if (!__all_sync(FULL_MASK, wait(&o_done[hh], od & 1)))
+                goto softmax_done;
+            ++od;
+            tc_fence_after();
+            {
+                const float inv = 1.0f / l_run;
+                float *dst = p.out + ((int64_t)(it.q0 + it.qt * QT + hh * TBQ +
+                                                min(r, max(rows, 1) - 1)) * p.num_q_heads + it.h) * D;
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     float o[32];
                     tmem_ld32(t_o + c0, o);
+                    if (r < rows) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        o[j] *= corr;
-                    tmem_st32(t_o + c0, o);
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(dst + c0 + j) = make_float4(
+                                o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
+                    }
                 }
             }
-            // pass 2: weights, their sum, and P (keys 32c..32c+31 as 16-bit
-            // pairs in columns 16c..16c+15, over S columns already read)
-            float sum = 0.0f;
-#pragma unroll 1
-            for (int c0 = 0; c0 < TBK; c0 += 32) {
-                float v[32];
-                tmem_ld32(t_s + c0, v);
-                if (diag) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (c0 + j > lim)
-                            v[j] = -INFINITY;
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    v[j] = ex2_approx(fmaf(v[j], p.scale_log2, -m_new));
-                uint32_t w[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    w[j] = pack2<T>(v[2 * j], v[2 * j + 1]);
-                tmem_st16(t_s + c0 / 2, w);
-#pragma unroll
-                for (int k = 16; k > 0; k >>= 1)      // tree sum
-#pragma unroll
-                    for (int j = 0; j < k; ++j)
-                        v[j] += v[j + k];
-                sum += v[0];
-            }
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            l_run = l_run * corr + sum;
             tc_fence_before();
-            mbar_arrive(&p_full[hh]);
+            mbar_arrive(&o_free[hh]);
         }
-        // ---- O / l (warp-uniform branch: the TMEM loads run converged;
-        // padding rows load without storing)
-        if (my_tiles > 0 && ok && __all_sync(FULL_MASK, wait(&o_done[hh], 0u))) {
-            tc_fence_after();
-            const float inv = 1.0f / l_run;
-            float *dst = p.out + ((int64_t)(q0 + qt * QT + hh * TBQ + min(r, max(rows, 1) - 1)) *
-                                      p.num_q_heads + h) * D;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float o[32];
-                tmem_ld32(t_o + c0, o);
-                if (r < rows) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(dst + c0 + j) =
-                            make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
-                }
-            }
-        }
+    softmax_done:;
     } else if (warp < MMA_WARP) {
-        // ================= producer warp pw: rows pw*64 .. pw*64+63 of Q,
-        // then K (pw < NSLOT) or V tiles pw % NSLOT, pw % NSLOT + NSLOT, ...
-        // into slot pw % NSLOT.  Eight consecutive lanes fill one core matrix
-        // (8 rows x 16 B: a conflict-free 128-byte shared-memory write); a
-        // warp reads 64 contiguous bytes of 8 rows.
+        // ================= producer warp pw: per item, rows pw*64 .. pw*64+63
+        // of Q (once the previous item's last S has read Q), then K (pw <
+        // NSLOT) or V tiles into slot pw % NSLOT: the CTA's tiles are counted
+        // across items, tile g in slot g % NSLOT.  Q: eight consecutive lanes
+        // fill one core matrix (8 rows x 16 B, a conflict-free 128-byte
+        // shared-memory write); a warp reads 64 contiguous bytes of 8 rows.
         const int pw = warp - SOFT_WARPS;
         const int slot = pw % NSLOT;
         const bool is_k = pw < NSLOT;
         const int rr = tid & 7, cq = (tid >> 3) & 3;
+        const int lane = tid & 31;
         const T *qg = static_cast<const T *>(p.q);
         unsigned char *ring = (is_k ? sK : sV) + slot * C::KV_BYTES;
         uint64_t *full = is_k ? &k_full[slot] : &v_full[slot];
         uint64_t *empty = is_k ? &k_empty[slot] : &v_empty[slot];
-        const int32_t *table = p.block_tables + (int64_t)b * p.max_blocks_per_seq;
-#pragma unroll 1
-        for (int g = 0; g < QT / PROD_WARPS / 8; ++g) {
-            const int r = pw * (QT / PROD_WARPS) + g * 8 + rr;   // query of this CTA
-            const bool ok = r < rows_all;
-            const T *src = qg + ((int64_t)(q0 + qt * QT + (ok ? r : 0)) * p.num_q_heads + h) * D;
-#pragma unroll
-            for (int c = cq; c < DCH; c += 4)
-                cp_async16(sQ + (r >> 7) * C::Q_BYTES + core_off(r & (TBQ - 1), c, DCH), src + c * 8, ok);
-        }
-        cp_async_commit();
-        bool ok = true, q_sent = false;
-        const int lane = tid & 31;
         const CUtensorMap *tm = is_k ? &p.tm_k : &p.tm_v;
         const T *cache = static_cast<const T *>(is_k ? p.k_cache : p.v_cache);
         const int R = p.box_rows;                  // rows of one box: min(block size, 128)
         const int nbox = TBK / R;                  // boxes a tile: at most 32 (blocks >= 4 rows)
         const int oob = p.num_blocks * p.num_kv_heads;   // a block index past the end: zero fill
-        for (int kt = slot; kt < ntiles; kt += NSLOT) {
-            // lane j: rows [j R, j R + R) of the tile, one cache block (block
-            // sizes are powers of two: shifts, no divisions); the block-id
-            // load overlaps the wait for the slot
-            const int pos0 = kt * TBK + lane * R;
-            const bool inbox = lane < nbox;
-            const bool live = inbox && pos0 <= last_pos;
-            const int32_t blk = live ? __ldg(table + (pos0 >> p.bs_log2)) : 0;
-            if (kt >= NSLOT && !wait(empty, (uint32_t)(((kt / NSLOT) & 1) ^ 1))) {
-                ok = false;
-                break;
-            }
-            int z = oob;
-            if (live) {
-                if (blk < 0 || blk >= p.num_blocks)
-                    atomicOr(p.err, PKV_EBIT_BLOCK);
-                else
-                    z = blk * p.num_kv_heads + kvh;
-            }
-            const int y = pos0 & (p.block_size - 1);
-            // A box goes by one tensor copy per 64-column panel when it starts
-            // on a 1024-byte boundary (boxes of >= 8 rows) and holds no row
-            // past the sequence end (those must be zeros: P is 0 there, but 0
-            // times a stale NaN is not); the other boxes go by 16-byte copies.
-            const bool by_tma = inbox && R >= 8 && (z == oob || pos0 + R - 1 <= last_pos);
-            const unsigned tma_boxes = __popc(__ballot_sync(FULL_MASK, by_tma));
-            const unsigned cp_boxes = __ballot_sync(FULL_MASK, inbox && !by_tma);
-            if (lane == 0)
-                mbar_arrive_expect_tx(full, tma_boxes * (uint32_t)R * 2u * D);
-            __syncwarp();
-            if (by_tma) {
+        int gt = 0;                                // the CTA's tiles so far
+        uint32_t qc = 0;                           // items so far
+        for (int i = blockIdx.x; i < nitems; i += gridDim.x) {
+            const Item it = make_item(p, i);
+            if (!it.live)
+                continue;
+            const int32_t *table = p.block_tables + (int64_t)it.b * p.max_blocks_per_seq;
+            if (qc > 0 && !wait(q_empty, (qc - 1) & 1))
+                goto producer_done;
+#pragma unroll 1
+            for (int g = 0; g < QT / PROD_WARPS / 8; ++g) {
+                const int r = pw * (QT / PROD_WARPS) + g * 8 + rr;   // query of the item
+                const bool ok = r < it.rows_all;
+                const T *src = qg + ((int64_t)(it.q0 + it.qt * QT + (ok ? r : 0)) * p.num_q_heads +
+                                     it.h) * D;
 #pragma unroll
-                for (int pn = 0; pn < D / 64; ++pn)
-                    tma_load_3d(ring + pn * (TBK * 128) + lane * R * 128, tm, pn * 64, y, z, full);
+                for (int c = cq; c < DCH; c += 4)
+                    cp_async16(sQ + (r >> 7) * C::Q_BYTES + core_off(r & (TBQ - 1), c, DCH),
+                               src + c * 8, ok);
             }
-            if (cp_boxes) {
-                // chunk c of tile row r lands at 128 r + 16 (c mod 8 xor r mod 8)
-                // in panel c / 8 (the pattern of the 128-byte swizzle)
-                for (unsigned m = cp_boxes; m; m &= m - 1) {
-                    const int bx = __ffs(m) - 1;
-                    const int zb = __shfl_sync(FULL_MASK, z, bx);
-                    const int yb = __shfl_sync(FULL_MASK, y, bx);
-                    for (int idx = lane; idx < R * DCH; idx += 32) {
-                        const int r = bx * R + idx / DCH, c = idx % DCH;
-                        const bool valid = zb != oob && kt * TBK + r <= last_pos;
-                        const int64_t row = valid ? (int64_t)zb * p.block_size + yb + idx / DCH : 0;
-                        cp_async16(ring + (c >> 3) * (TBK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4),
-                                   cache + row * D + c * 8, valid);
-                    }
+            cp_async_commit();
+            bool q_sent = false;
+            for (int kt = 0; kt < it.ntiles; ++kt) {
+                const int g = gt + kt;
+                if (g % NSLOT != slot)
+                    continue;
+                // lane j: rows [j R, j R + R) of the tile, one cache block
+                // (block sizes are powers of two: shifts, no divisions); the
+                // block-id load overlaps the wait for the slot
+                const int pos0 = kt * TBK + lane * R;
+                const bool inbox = lane < nbox;
+                const bool live = inbox && pos0 <= it.last_pos;
+                const int32_t blk = live ? __ldg(table + (pos0 >> p.bs_log2)) : 0;
+                if (g >= NSLOT && !wait(empty, (uint32_t)(((g / NSLOT) & 1) ^ 1)))
+                    goto producer_done;
+                int z = oob;
+                if (live) {
+                    if (blk < 0 || blk >= p.num_blocks)
+                        atomicOr(p.err, PKV_EBIT_BLOCK);
+                    else
+                        z = blk * p.num_kv_heads + it.kvh;
                 }
-                cp_async_commit();
-                cp_async_wait<0>();
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const int y = pos0 & (p.block_size - 1);
+                // A box goes by one tensor copy per 64-column panel when it
+                // starts on a 1024-byte boundary (boxes of >= 8 rows) and
+                // holds no row past the sequence end (those must be zeros: P
+                // is 0 there, but 0 times a stale NaN is not); the other
+                // boxes go by 16-byte copies.
+                const bool by_tma = inbox && R >= 8 && (z == oob || pos0 + R - 1 <= it.last_pos);
+                const unsigned tma_boxes = __popc(__ballot_sync(FULL_MASK, by_tma));
+                const unsigned cp_boxes = __ballot_sync(FULL_MASK, inbox && !by_tma);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full, tma_boxes * (uint32_t)R * 2u * D);
+                __syncwarp();
+                if (by_tma) {
+#pragma unroll
+                    for (int pn = 0; pn < D / 64; ++pn)
+                        tma_load_3d(ring + pn * (TBK * 128) + lane * R * 128, tm, pn * 64, y, z,
+                                    full);
+                }
+                if (cp_boxes) {
+                    // chunk c of tile row r lands at 128 r + 16 (c mod 8 xor
+                    // r mod 8) in panel c / 8 (the 128-byte swizzle pattern)
+                    for (unsigned m = cp_boxes; m; m &= m - 1) {
+                        const int bx = __ffs(m) - 1;
+                        const int zb = __shfl_sync(FULL_MASK, z, bx);
+                        const int yb = __shfl_sync(FULL_MASK, y, bx);
+                        for (int idx = lane; idx < R * DCH; idx += 32) {
+                            const int r = bx * R + idx / DCH, c = idx % DCH;
+                            const bool valid = zb != oob && kt * TBK + r <= it.last_pos;
+                            const int64_t row =
+                                valid ? (int64_t)zb * p.block_size + yb + idx / DCH : 0;
+                            cp_async16(ring + (c >> 3) * (TBK * 128) + r * 128 +
+                                           (((c & 7) ^ (r & 7)) << 4),
+                                       cache + row * D + c * 8, valid);
+                        }
+                    }
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0)                     // the 16-byte copies (if any) have landed
+                    mbar_arrive(full);
+                if (!q_sent) {                     // Q (this thread's cp.async group) has landed
+                    cp_async_wait<0>();
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive(q_full);
+                    q_sent = true;
+                }
             }
-            __syncwarp();
-            if (lane == 0)                         // the 16-byte copies (if any) have landed
-                mbar_arrive(full);
-            if (!q_sent) {                         // Q (this thread's cp.async group) has landed
+            if (!q_sent) {
                 cp_async_wait<0>();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(q_full);
-                q_sent = true;
             }
+            gt += it.ntiles;
+            ++qc;
         }
+    producer_done:
         cp_async_wait<0>();
-        if (ok && !q_sent) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(q_full);
-        }
     } else if ((tid & 31) == 0) {
         // ================= MMA issue (one thread)
         const uint32_t idesc_s = umma_idesc(AB, 0u, TBK);
         const uint32_t idesc_o = umma_idesc(AB, 1u, D);
         const uint32_t sQa = smem_addr(sQ), sKa = smem_addr(sK), sVa = smem_addr(sV);
-        const int last_half = tiles_h[1] > 0 ? 1 : 0;   // the last reader of each K/V tile
-        // S_hh = Q_hh K^T, both K-major.  Q: core-matrix layout with DCH
-        // chunks a row (K-direction core stride 128 B, row-group stride
-        // DCH*128 B; a K = 16 step is two chunks).  K: 128-byte swizzled
-        // panels of 64 d (8-row groups 1024 B apart); a K = 16 step is 32 B
-        // into the panel's rows.
-        auto issue_s = [&](int hh, int kt) {
-            const uint32_t kb = sKa + (kt % NSLOT) * C::KV_BYTES, qb = sQa + hh * C::Q_BYTES;
+        int gt = 0;                                // the CTA's tiles so far
+        uint32_t qc = 0, pc[NQH] = {0, 0}, ofc[NQH] = {0, 0};
+        bool o_used[NQH] = {false, false};         // O_h holds an earlier item's result
+        bool ok = true;
+        for (int i = blockIdx.x; i < nitems && ok; i += gridDim.x) {
+            const Item it = make_item(p, i);
+            if (it.bad_len)
+                atomicOr(p.err, PKV_EBIT_SEQLEN);
+            if (!it.live)
+                continue;
+            const int last_half = it.tiles_h[1] > 0 ? 1 : 0;   // the last reader of each tile
+            int s_left = it.tiles_h[0] + it.tiles_h[1];         // S issues until Q is free
+            // S_hh = Q_hh K^T, both K-major.  Q: core-matrix layout with DCH
+            // chunks a row (K-direction core stride 128 B, row-group stride
+            // DCH*128 B; a K = 16 step is two chunks).  K: 128-byte swizzled
+            // panels of 64 d (8-row groups 1024 B apart); a K = 16 step is
+            // 32 B into the panel's rows.
+            auto issue_s = [&](int hh, int g) {
+                const uint32_t kb = sKa + (g % NSLOT) * C::KV_BYTES, qb = sQa + hh * C::Q_BYTES;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-                umma_f16(tmem + hh * C::HALF_COLS, umma_desc(qb + ks * 256, 128, DCH * 128),
-                         umma_desc_sw128(kb + (ks / 4) * (TBK * 128) + (ks % 4) * 32, 16, 1024),
-                         idesc_s, ks > 0 ? 1u : 0u);
-            if (hh == last_half)
-                umma_commit(&k_empty[kt % NSLOT]);
-            umma_commit(&s_full[hh]);
-        };
-        // O_hh += P_hh V.  P: in tensor memory over the S columns, 16 keys
-        // (a K step) per 8 columns.  V is the MN-major B in 128-byte swizzled
-        // panels: a key row of 64 d every 128 B, 8-key groups 1024 B apart,
-        // the next 64 d a panel (TBK*128 B) on; a step of 16 keys is 2048 B.
-        auto issue_pv = [&](int hh, int kt) {
-            const uint32_t vb = sVa + (kt % NSLOT) * C::KV_BYTES;
+                for (int ks = 0; ks < D / 16; ++ks)
+                    umma_f16(tmem + hh * C::HALF_COLS, umma_desc(qb + ks * 256, 128, DCH * 128),
+                             umma_desc_sw128(kb + (ks / 4) * (TBK * 128) + (ks % 4) * 32, 16, 1024),
+                             idesc_s, ks > 0 ? 1u : 0u);
+                if (hh == last_half)
+                    umma_commit(&k_empty[g % NSLOT]);
+                umma_commit(&s_full[hh]);
+                if (--s_left == 0)
+                    umma_commit(q_empty);
+            };
+            // O_hh += P_hh V.  P: in tensor memory over the S columns, 16
+            // keys (a K step) per 8 columns.  V is the MN-major B in 128-byte
+            // swizzled panels: a key row of 64 d every 128 B, 8-key groups
+            // 1024 B apart, the next 64 d a panel (TBK*128 B) on; a step of
+            // 16 keys is 2048 B.
+            auto issue_pv = [&](int hh, int g, int kt) {
+                const uint32_t vb = sVa + (g % NSLOT) * C::KV_BYTES;
 #pragma unroll
-            for (int ks = 0; ks < TBK / 16; ++ks)
-                umma_f16_ta(tmem + hh * C::HALF_COLS + TBK, tmem + hh * C::HALF_COLS + ks * 8,
-                            umma_desc_sw128(vb + ks * 2048, TBK * 128, 1024), idesc_o,
-                            (kt > 0 || ks > 0) ? 1u : 0u);
-            if (hh == last_half)
-                umma_commit(&v_empty[kt % NSLOT]);
-        };
-        bool ok = wait(q_full, 0u) && wait(&k_full[0], 0u);
-        if (ok) {
+                for (int ks = 0; ks < TBK / 16; ++ks)
+                    umma_f16_ta(tmem + hh * C::HALF_COLS + TBK, tmem + hh * C::HALF_COLS + ks * 8,
+                                umma_desc_sw128(vb + ks * 2048, TBK * 128, 1024), idesc_o,
+                                (kt > 0 || ks > 0) ? 1u : 0u);
+                if (hh == last_half)
+                    umma_commit(&v_empty[g % NSLOT]);
+            };
+            if (!(ok = wait(q_full, qc & 1) &&
+                       wait(&k_full[gt % NSLOT], (uint32_t)((gt / NSLOT) & 1))))
+                break;
+            ++qc;
             tc_fence_after();
             for (int hh = 0; hh < NQH; ++hh)
-                if (tiles_h[hh] > 0)
-                    issue_s(hh, 0);
-        }
-        for (int kt = 0; kt < ntiles && ok; ++kt) {
-            for (int hh = 0; hh < NQH; ++hh) {
-                if (kt >= tiles_h[hh])
-                    continue;
-                if (!(ok = wait(&p_full[hh], (uint32_t)(kt & 1)) &&
-                           wait(&v_full[kt % NSLOT], (uint32_t)((kt / NSLOT) & 1))))
-                    break;
-                tc_fence_after();
-                issue_pv(hh, kt);
-                if (kt + 1 < tiles_h[hh]) {
-                    if (!(ok = wait(&k_full[(kt + 1) % NSLOT], (uint32_t)(((kt + 1) / NSLOT) & 1))))
+                if (it.tiles_h[hh] > 0)
+                    issue_s(hh, gt);
+            for (int kt = 0; kt < it.ntiles && ok; ++kt) {
+                const int g = gt + kt;
+                for (int hh = 0; hh < NQH; ++hh) {
+                    if (kt >= it.tiles_h[hh])
+                        continue;
+                    if (!(ok = wait(&p_full[hh], pc[hh] & 1) &&
+                               wait(&v_full[g % NSLOT], (uint32_t)((g / NSLOT) & 1))))
                         break;
+                    ++pc[hh];
+                    if (kt == 0 && o_used[hh]) {   // the softmax warps have read O_h out
+                        if (!(ok = wait(&o_free[hh], ofc[hh] & 1)))
+                            break;
+                        ++ofc[hh];
+                    }
                     tc_fence_after();
-                    issue_s(hh, kt + 1);
-                } else {
-                    umma_commit(&o_done[hh]);
+                    issue_pv(hh, g, kt);
+                    if (kt + 1 < it.tiles_h[hh]) {
+                        if (!(ok = wait(&k_full[(g + 1) % NSLOT], (uint32_t)(((g + 1) / NSLOT) & 1))))
+                            break;
+                        tc_fence_after();
+                        issue_s(hh, g + 1);
+                    } else {
+                        umma_commit(&o_done[hh]);
+                        o_used[hh] = true;
+                    }
                 }
             }
+            gt += it.ntiles;
         }
         // every issued MMA has finished before tensor memory is released
         umma_commit(drain);
@@ -631,9 +711,18 @@ int launch_prefill_t(const pkv_pool *pool, const PrefillParams &prm, int max_q_l
             return PKV_ERR_CUDA;
         configured = true;
     }
-    constexpr int QT = NQH * TBQ;
-    const dim3 grid((unsigned)((max_q_len + QT - 1) / QT), (unsigned)prm.num_q_heads,
-                    (unsigned)prm.batch);
+    // one CTA per SM, each walking the items c, c + grid, ...
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms < 1)
+            return PKV_ERR_CUDA;
+    }
+    (void)max_q_len;
+    const int64_t nitems = (int64_t)prm.nqt * prm.num_q_heads * prm.batch;
+    const dim3 grid((unsigned)(nitems < sms ? nitems : sms));
     if (launch_pdl(paged_prefill_tc_kernel<D, T>, grid, dim3(TNT), (size_t)C::SMEM_BYTES, s,
                    prm) != cudaSuccess)
         return PKV_ERR_CUDA;
@@ -702,6 +791,10 @@ int launch_prefill(const pkv_pool *pool, const void *q, int num_q_heads, const v
     prm.num_blocks = pool->num_blocks;
     prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
     prm.box_rows = pool->block_size < TBK ? pool->block_size : TBK;
+    constexpr int QT = NQH * TBQ;
+    prm.nqt = (max_q_len + QT - 1) / QT;
+    if ((int64_t)prm.nqt * num_q_heads * batch >= ((int64_t)1 << 31))
+        return PKV_ERR_UNSUPPORTED;
     if (!encode_cache_map(&prm.tm_k, pool, k_cache, prm.box_rows) ||
         !encode_cache_map(&prm.tm_v, pool, v_cache, prm.box_rows))
         return PKV_ERR_CUDA;
