@@ -276,6 +276,16 @@ __device__ __forceinline__ Item make_item(const PrefillParams &p, int i)
     return it;
 }
 
+// This CTA's item in round rnd (-1: none): items are numbered longest
+// first, and the rounds alternate direction over the CTAs so that every CTA
+// gets a mix of long and short items.
+__device__ __forceinline__ int item_of(int rnd, int nitems)
+{
+    const int c = (rnd & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    const int i = rnd * (int)gridDim.x + c;
+    return i < nitems ? i : -1;
+}
+
 template <int D, typename T>
 __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_constant__ PrefillParams p)
 {
@@ -354,7 +364,10 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
         const uint32_t t_s = tmem + hh * C::HALF_COLS + ((uint32_t)(quad * 32) << 16);
         const uint32_t t_o = t_s + TBK;
         uint32_t sc = 0, od = 0;                   // phases used of s_full[hh], o_done[hh]
-        for (int i = blockIdx.x; i < nitems; i += gridDim.x) {
+        for (int rnd = 0; rnd * (int)gridDim.x < nitems; ++rnd) {
+            const int i = item_of(rnd, nitems);
+            if (i < 0)
+                continue;
             const Item it = make_item(p, i);
             const int rows = it.rows_h[hh], my_tiles = it.tiles_h[hh];
             if (my_tiles == 0)
@@ -496,7 +509,10 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
         const int oob = p.num_blocks * p.num_kv_heads;   // a block index past the end: zero fill
         int gt = 0;                                // the CTA's tiles so far
         uint32_t qc = 0;                           // items so far
-        for (int i = blockIdx.x; i < nitems; i += gridDim.x) {
+        for (int rnd = 0; rnd * (int)gridDim.x < nitems; ++rnd) {
+            const int i = item_of(rnd, nitems);
+            if (i < 0)
+                continue;
             const Item it = make_item(p, i);
             if (!it.live)
                 continue;
@@ -604,7 +620,10 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
         uint32_t qc = 0, pc[NQH] = {0, 0}, ofc[NQH] = {0, 0};
         bool o_used[NQH] = {false, false};         // O_h holds an earlier item's result
         bool ok = true;
-        for (int i = blockIdx.x; i < nitems && ok; i += gridDim.x) {
+        for (int rnd = 0; rnd * (int)gridDim.x < nitems && ok; ++rnd) {
+            const int i = item_of(rnd, nitems);
+            if (i < 0)
+                continue;
             const Item it = make_item(p, i);
             if (it.bad_len)
                 atomicOr(p.err, PKV_EBIT_SEQLEN);
