@@ -104,7 +104,9 @@ template <int D>
 struct TcCfg {
     static constexpr int Q_BYTES = TBQ * D * 2;          // one half
     static constexpr int KV_BYTES = TBK * D * 2;          // one K or V tile
-    static constexpr int BAR_OFF = NQH * Q_BYTES + 2 * NSLOT * KV_BYTES;
+    // output staging: 32 rows x 32 fp32 per softmax warp
+    static constexpr int STG_OFF = NQH * Q_BYTES + 2 * NSLOT * KV_BYTES;
+    static constexpr int BAR_OFF = STG_OFF + SOFT_WARPS * 32 * 32 * 4;
     static constexpr int NBARS = 4 * NSLOT + 4 * NQH + 3;
     static constexpr int SMEM_BYTES = BAR_OFF + NBARS * 8 + 16;
     static constexpr int TMEM_COLS = 512;
@@ -297,6 +299,7 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
     unsigned char *sQ = smem_raw;                              // NQH halves
     unsigned char *sK = sQ + NQH * C::Q_BYTES;                 // NSLOT K tiles
     unsigned char *sV = sK + NSLOT * C::KV_BYTES;              // NSLOT V tiles
+    float4 *stg_all = reinterpret_cast<float4 *>(smem_raw + C::STG_OFF);
     uint64_t *k_full = reinterpret_cast<uint64_t *>(smem_raw + C::BAR_OFF);
     uint64_t *k_empty = k_full + NSLOT;
     uint64_t *v_full = k_empty + NSLOT;
@@ -467,19 +470,31 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
             ++od;
             tc_fence_after();
             {
+                // 32 columns at a time through the warp's staging rows (16-byte
+                // slot j of row x at j xor (x mod 8): conflict-free both
+                // ways), then out as 128-byte row segments, four rows a store
                 const float inv = 1.0f / l_run;
-                float *dst = p.out + ((int64_t)(it.q0 + it.qt * QT + hh * TBQ +
-                                                min(r, max(rows, 1) - 1)) * p.num_q_heads + it.h) * D;
+                const int lane = tid & 31;
+                float4 *stg = stg_all + warp * 32 * 8;
+                const int xr = lane >> 3, xj = lane & 7;   // store: rows xr, xr + 4, ...
+                const int64_t row0 = (int64_t)it.q0 + it.qt * QT + hh * TBQ + quad * 32;
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     float o[32];
                     tmem_ld32(t_o + c0, o);
-                    if (r < rows) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(dst + c0 + j) = make_float4(
-                                o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
+                    for (int j = 0; j < 8; ++j)
+                        stg[lane * 8 + (j ^ (lane & 7))] = make_float4(
+                            o[4 * j] * inv, o[4 * j + 1] * inv, o[4 * j + 2] * inv, o[4 * j + 3] * inv);
+                    __syncwarp();
+#pragma unroll
+                    for (int x = xr; x < 32; x += 4) {
+                        const float4 v = stg[x * 8 + (xj ^ (x & 7))];
+                        if (quad * 32 + x < rows)
+                            *reinterpret_cast<float4 *>(p.out + ((row0 + x) * p.num_q_heads + it.h) * D +
+                                                        c0 + 4 * xj) = v;
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
