@@ -181,6 +181,32 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
                  : "memory");
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// (a0, a1) = (a0, a1) * s + c as one packed fp32x2 FMA.
+__device__ __forceinline__ void fma2_bc(float &a0, float &a1, float s, float c)
+{
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %2};\n\t"
+        "mov.b64 z, {%3, %3};\n\tfma.rn.f32x2 x, x, y, z;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(s), "f"(c));
+}
+
+// (a0, a1) += (b0, b1) as one packed fp32x2 add.
+__device__ __forceinline__ void add2(float &a0, float &a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+        "add.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
 // 2^x with the hardware approximation (-inf -> +0).
 __device__ __forceinline__ float ex2_approx(float x)
 {
@@ -399,12 +425,14 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
                             if (c0 + j > lim)
                                 v[j] = -INFINITY;
                     }
+                    // three-input maxima: 32 -> 11 -> 4 -> 1
+                    float t[11];
 #pragma unroll
-                    for (int w = 16; w > 0; w >>= 1)   // tree: 5 dependent steps
-#pragma unroll
-                        for (int j = 0; j < w; ++j)
-                            v[j] = fmaxf(v[j], v[j + w]);
-                    mx = fmaxf(mx, v[0]);
+                    for (int j = 0; j < 10; ++j)
+                        t[j] = max3f(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+                    t[10] = fmaxf(v[30], v[31]);
+                    mx = max3f(mx, max3f(t[0], t[1], t[2]), max3f(t[3], t[4], t[5]));
+                    mx = max3f(mx, max3f(t[6], t[7], t[8]), fmaxf(t[9], t[10]));
                 }
                 mx *= p.scale_log2;                // scale > 0: the maximum commutes
                 // The running maximum moves only when a score exceeds it by
@@ -444,19 +472,22 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
                                 v[j] = -INFINITY;
                     }
 #pragma unroll
+                    for (int j = 0; j < 32; j += 2)        // the exponent, two a step
+                        fma2_bc(v[j], v[j + 1], p.scale_log2, -m_new);
+#pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        v[j] = ex2_approx(fmaf(v[j], p.scale_log2, -m_new));
+                        v[j] = ex2_approx(v[j]);
                     uint32_t w[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         w[j] = pack2<T>(v[2 * j], v[2 * j + 1]);
                     tmem_st16(t_s + c0 / 2, w);
 #pragma unroll
-                    for (int k = 16; k > 0; k >>= 1)   // tree sum
+                    for (int k = 16; k > 1; k >>= 1)       // tree sum over pairs
 #pragma unroll
-                        for (int j = 0; j < k; ++j)
-                            v[j] += v[j + k];
-                    sum += v[0];
+                        for (int j = 0; j < k; j += 2)
+                            add2(v[j], v[j + 1], v[j + k], v[j + k + 1]);
+                    sum += v[0] + v[1];
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 l_run = l_run * corr + sum;
