@@ -164,6 +164,10 @@ def _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, seed):
     ("f16", 128, 8, 8, 16, [1], [1]),
     ("bf16", 64, 8, 4, 8, [300, 513, 256], [17, 0, 40]),
     ("bf16", 128, 4, 2, 256, [700, 3], [300, 509]),
+    # more work items (256-query tiles x heads) than SMs: each CTA runs
+    # several, some of them empty
+    ("bf16", 128, 32, 8, 16, [700, 300, 900, 50], [0, 100, 0, 500]),
+    ("f16", 64, 32, 4, 8, [513, 1, 260], [10, 0, 3]),
 ])
 def test_gpu_prefill_matches_oracle(dt, D, Hq, Hkv, bs, news, cached):
     from paged_kv_cache_273_gb300 import pkv
