@@ -175,3 +175,56 @@ def test_gpu_prefill_matches_oracle(dt, D, Hq, Hkv, bs, news, cached):
     assert same_cache and intact
     assert status == pkv.PKV_OK
     assert err <= PREFILL_TOL[dt], err
+
+
+@pytest.mark.gpu
+def test_gpu_prefill_full_size_sampled():
+    """The timed prefill workload (4 prompts x 4096 new tokens, 32 q / 8 KV
+    heads, d 128, bf16, block size 16, one launch as the bench makes it);
+    sampled outputs checked one by one: the attention of new token i is the
+    decode oracle over the first i + 1 cached rows."""
+    import torch
+    from paged_kv_cache_273_gb300 import pkv
+    import parity_harness as PH
+    from paged_kv_cache_273_gb300 import workloads as W
+    code, B, n, Hq, Hkv, D, bs = W.BF16, 4, 4096, 32, 8, 128, 16
+    rng = np.random.default_rng(90)
+    dev = torch.device("cuda", 0)
+    nb = n // bs
+    NB = B * nb + 3
+    tables = rng.permutation(NB)[:B * nb].astype(np.int32).reshape(B, nb)
+    pool = pkv.kv_block_pool_init(NB, bs, Hkv, D, code)
+    kc = torch.zeros((NB, Hkv, bs, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    ok = np.zeros((NB, Hkv, bs, D), np.uint16)
+    ov = np.zeros_like(ok)
+    lens = np.full(B, n, np.int32)
+    rows_k = W._values(rng, (B * n, Hkv, D), code)
+    rows_v = W._values(rng, (B * n, Hkv, D), code)
+    slots = pkv.kv_slot_mapping(tables, bs, np.zeros(B, np.int32), lens)
+    pkv.kv_append(pool, PH.to_device(rows_k, code), PH.to_device(rows_v, code),
+                  torch.from_numpy(slots).to(dev), kc, vc)
+    O.append(rows_k, rows_v, code, slots, bs, ok, ov)
+    qs = np.arange(0, (B + 1) * n, n, dtype=np.int32)
+    q = W._values(rng, (B * n, Hq, D), code)
+    out = torch.full((B * n, Hq, D), float("nan"), dtype=torch.float32, device=dev)
+    scale = 1.0 / np.sqrt(D)
+    pkv.paged_prefill_attention(pool, PH.to_device(q, code), kc, vc,
+                                torch.from_numpy(tables).to(dev), torch.from_numpy(qs).to(dev),
+                                torch.from_numpy(lens).to(dev), scale, out, n)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_error(pool) == pkv.PKV_OK
+    got = out.cpu().numpy()
+    assert not np.isnan(got).any()                  # every output row was written
+    assert np.array_equal(PH.to_raw(kc, code), ok) and np.array_equal(PH.to_raw(vc, code), ov)
+    picks = [(b, i, h) for b in range(B) for i in (0, 1, 255, 256, 4095)
+             for h in (0, 31)] + [tuple(x) for x in
+                                  zip(rng.integers(0, B, 40), rng.integers(0, n, 40),
+                                      rng.integers(0, Hq, 40))]
+    err = 0.0
+    for b, i, h in picks:
+        qrow = q[qs[b] + i][None, :, :]
+        want = O.paged_decode_attention(qrow, code, ok, ov, code, tables[b:b + 1],
+                                        np.array([i + 1], np.int32), float(np.float32(scale)))
+        err = max(err, float(np.max(np.abs(got[qs[b] + i, h] - want[0, h]))))
+    assert err <= PREFILL_TOL["bf16"], err
