@@ -228,3 +228,46 @@ def test_gpu_prefill_full_size_sampled():
                                         np.array([i + 1], np.int32), float(np.float32(scale)))
         err = max(err, float(np.max(np.abs(got[qs[b] + i, h] - want[0, h]))))
     assert err <= PREFILL_TOL["bf16"], err
+
+
+def _prefill_error_case(bad: str):
+    """A small bf16 prefill whose inputs are wrong in one way; returns the
+    pool's status and whether the caches' canaries are intact."""
+    import torch
+    from paged_kv_cache_273_gb300 import pkv
+    import parity_harness as PH
+    from paged_kv_cache_273_gb300 import workloads as W
+    code, D, Hq, Hkv, bs = W.BF16, 128, 8, 2, 16
+    rng = np.random.default_rng(91)
+    dev = torch.device("cuda", 0)
+    news, cached = [300, 40], [20, 0]
+    lens = np.array([c + n for c, n in zip(cached, news)], np.int32)
+    maxb = max(-(-int(L) // bs) for L in lens)
+    NB = 2 * maxb + 2
+    tables = rng.permutation(NB)[:2 * maxb].astype(np.int32).reshape(2, maxb)
+    pool = pkv.kv_block_pool_init(NB, bs, Hkv, D, code)
+    gk = PH.Guarded((NB, Hkv, bs, D), torch.bfloat16)
+    gv = PH.Guarded((NB, Hkv, bs, D), torch.bfloat16)
+    qs = np.array([0, news[0], news[0] + news[1]], np.int32)
+    q = W._values(rng, (int(qs[-1]), Hq, D), code)
+    if bad == "block":
+        tables[0, 5] = NB + 7                      # an id past the pool, inside the prefix
+    elif bad == "length":
+        lens[1] = news[1] - 1                      # fewer cached rows than new tokens
+    out = torch.full((int(qs[-1]), Hq, D), float("nan"), dtype=torch.float32, device=dev)
+    pkv.paged_prefill_attention(pool, PH.to_device(q, code), gk.tensor, gv.tensor,
+                                torch.from_numpy(tables).to(dev), torch.from_numpy(qs).to(dev),
+                                torch.from_numpy(lens).to(dev), 1.0 / np.sqrt(D), out, max(news))
+    torch.cuda.synchronize()
+    return pkv.pkv_check_error(pool), gk.intact() and gv.intact(), out
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("bad", ["block", "length"])
+def test_gpu_prefill_reports_bad_inputs(bad):
+    from paged_kv_cache_273_gb300 import pkv
+    status, intact, out = _prefill_error_case(bad)
+    assert status == pkv.PKV_ERR_BAD_INDEX
+    assert intact
+    if bad == "length":                            # the other sequence is still computed
+        assert not out[:300].isnan().any()
