@@ -112,7 +112,7 @@ def test_chunked_prefill_equals_prefill_at_once():
 PREFILL_TOL = {"f16": 2e-3, "bf16": 1e-2}
 
 
-def _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, seed):
+def _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, seed, k_growth=0.0, with_vmax=False):
     import torch
     from paged_kv_cache_273_gb300 import pkv
     import parity_harness as PH
@@ -133,6 +133,14 @@ def _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, seed):
     total = int(lens.sum())
     rows_k = W._values(rng, (total, Hkv, D), code)
     rows_v = W._values(rng, (total, Hkv, D), code)
+    if k_growth > 0.0:
+        # K rows grow with their position in the sequence, so that each new
+        # key tile holds larger scores than every earlier one
+        pos = np.concatenate([np.arange(int(L)) for L in lens]).astype(np.float32)
+        kf = rng.standard_normal((total, Hkv, D), dtype=np.float32) * \
+            (1.0 + k_growth * pos)[:, None, None]
+        rows_k = (kf.view(np.uint32) >> 16).astype(np.uint16) if code == W.BF16 else \
+            kf.astype(np.float16).view(np.uint16)
     slots = pkv.kv_slot_mapping(tables, bs, np.zeros(B, np.int32), lens)
     pkv.kv_append(pool, PH.to_device(rows_k, code), PH.to_device(rows_v, code),
                   torch.from_numpy(slots).to(dev), gk.tensor, gv.tensor)
@@ -151,8 +159,11 @@ def _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, seed):
                                      float(np.float32(scale)))
     same_cache = np.array_equal(PH.to_raw(gk.tensor, code), ok) and \
         np.array_equal(PH.to_raw(gv.tensor, code), ov)
-    return float(np.max(np.abs(got - want))), pkv.pkv_check_error(pool), same_cache, \
-        gk.intact() and gv.intact()
+    res = (float(np.max(np.abs(got - want))), pkv.pkv_check_error(pool), same_cache,
+           gk.intact() and gv.intact())
+    if with_vmax:
+        res += (float(np.max(np.abs(O.decode(rows_v, code)))),)
+    return res
 
 
 @pytest.mark.gpu
@@ -271,3 +282,21 @@ def test_gpu_prefill_reports_bad_inputs(bad):
     assert intact
     if bad == "length":                            # the other sequence is still computed
         assert not out[:300].isnan().any()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_gpu_prefill_rising_scores(dt):
+    """Scores that keep rising along the keys move each row's running offset
+    inside most tiles (the rare path: P already written in the tile, the sums
+    and O are rescaled)."""
+    from paged_kv_cache_273_gb300 import pkv
+    err, status, same_cache, intact, vmax = _gpu_prefill_case(
+        dt, 128, 8, 2, 16, [600, 130], [100, 0], 81, k_growth=1.0 / 32, with_vmax=True)
+    assert same_cache and intact
+    assert status == pkv.PKV_OK
+    # With one or two keys carrying nearly all the weight the rounding errors
+    # of P do not average out: the bound is the worst case, half an ulp of
+    # the weight type (2^-8 bf16, 2^-11 fp16) times max |v|, plus fp32 slack.
+    tol = (2.0 ** -8 if dt == "bf16" else 2.0 ** -11) * vmax + 1e-4
+    assert err <= tol, (err, tol)
