@@ -66,34 +66,40 @@ struct PrefillParams {
     float scale_log2;
 };
 
-// ---- tcgen05: 2 x 128 queries x 128 keys per step, warp-specialised
+// ---- tcgen05: 2 x 128 queries x 128 keys per step, warp-specialised,
+// persistent
 //
-// A CTA takes 256 queries of one (sequence, query head) as two 128-row
-// halves A and B that share every K/V tile (one CTA per SM), with three
-// roles:
-//  * four producer warps copy a quarter of Q each with 16-byte cp.async
-//    copies into the tensor cores' core-matrix layout (8 rows x 16 bytes per
-//    128-byte core matrix, no swizzle); then warps 0, 1 bring K tiles and
-//    warps 2, 3 V tiles into two-slot rings, 128-byte swizzled (row r of a
-//    64-column panel at 128 r, its 16-byte chunks permuted by r mod 8):
-//    one tensor-memory-access copy per cache block and panel (lane j takes
-//    the j-th block of the tile), 16-byte cp.async copies for blocks of 4
-//    rows and for the block where the sequence ends;
+// One CTA per SM walks work items: 256 queries of one (sequence, query head)
+// as two 128-row halves A and B that share every K/V tile.  Items are
+// numbered longest first and dealt to the CTAs in an order that alternates
+// direction each round.  Three roles:
+//  * four producer warps copy a quarter of each item's Q with 16-byte
+//    cp.async copies into the tensor cores' core-matrix layout (8 rows x 16
+//    bytes per 128-byte core matrix, no swizzle); then warps 0, 1 bring K
+//    tiles and warps 2, 3 V tiles into two-slot rings, 128-byte swizzled
+//    (row r of a 64-column panel at 128 r, its 16-byte chunks permuted by
+//    r mod 8): one tensor-memory-access copy per cache block and panel (lane
+//    j takes the j-th block of the tile), 16-byte cp.async copies for blocks
+//    of 4 rows and for the block where the sequence ends;
 //  * one thread issues the tcgen05.mma: S = Q K^T (M 128, N 128, K = D, both
 //    operands in shared memory) and O += P V (M 128, N = D, K 128, P read
 //    from tensor memory) per half, fp32 accumulators in tensor memory (half
 //    h: S in columns [256 h, 256 h + 128), O in the next D);
 //  * one warpgroup per half, one thread per query row, reads its S row with
 //    tcgen05.ld, does the online softmax, writes P as fp16/bf16 pairs over
-//    the S columns it has read, and rescales its O row in tensor memory when
-//    the row maximum moved by more than 2^8.
+//    the S columns it has read, rescales its O row in tensor memory when the
+//    row maximum moved by more than 2^8, and at the end of an item writes
+//    O / l out through shared-memory staging.
 // The issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) lets one half's
 // softmax run while the tensor cores work on the other half; tcgen05.mma
 // runs in issue order, so S_h(j+1) overwrites P_h(j) only after P_h(j) V
-// has read it.  mbarriers hand the tiles over: k_full / k_empty and v_full /
-// v_empty per slot, s_full (tcgen05.commit after S_h, which also covers the
-// P V issued before it, so O_h is idle), p_full (the half's 128 softmax
-// threads) and o_done (after the last P V).
+// has read it.  mbarriers hand the work over: k_full / k_empty and v_full /
+// v_empty per slot (tiles counted across items), s_full (tcgen05.commit
+// after S_h, which also covers the P V issued before it, so O_h is idle),
+// p_full (the half's 128 softmax threads), o_done (after an item's last
+// P V), o_free (the softmax threads have read O out: the next item's first
+// P V may overwrite it) and q_full / q_empty (the next item's Q loads once
+// the current item's last S has read Q).
 
 constexpr int TBQ = 128, TBK = 128, NQH = 2, NSLOT = 2;
 constexpr int SOFT_WARPS = 4 * NQH, PROD_WARPS = 2 * NSLOT;   // K slots, then V slots
