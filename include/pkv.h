@@ -340,10 +340,16 @@ int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype
  *
  * Runs on the fifth-generation tensor cores (tcgen05.mma, fp16/bf16 inputs,
  * fp32 accumulators in tensor memory; the softmax weights are rounded to the
- * input type for the P.V product).  Head dim 64 or 128.
- * fp32 and quantized pools return PKV_ERR_UNSUPPORTED.  Lengths or block ids
- * out of range set PKV_ERR_BAD_INDEX in the error word (those rows are
- * skipped).  No workspace.
+ * input type for the P.V product), one persistent CTA per SM; K and V are
+ * read through tensor maps built on the host for this call's k_cache and
+ * v_cache (so both must stay valid until the kernel has run, as for any
+ * stream-ordered call).  Head dim 64 or 128.
+ * fp32 and quantized pools return PKV_ERR_UNSUPPORTED, and so do shapes
+ * whose (256-query tiles x heads x batch) count reaches 2^31; PKV_ERR_CUDA
+ * if a tensor map cannot be encoded.  A length out of range sets
+ * PKV_ERR_BAD_INDEX in the error word and that sequence is skipped; a block
+ * id out of range sets it too and its rows are read as zeros (the
+ * sequence's output is unspecified).  No workspace.
  */
 int paged_prefill_attention(const pkv_pool *pool, const void *q, int num_q_heads,
                             const void *k_cache, const void *v_cache,
