@@ -772,25 +772,18 @@ template <int D, typename T>
 int launch_prefill_t(const pkv_pool *pool, const PrefillParams &prm, int max_q_len,
                      cudaStream_t s)
 {
-    (void)pool;
     using C = TcCfg<D>;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(paged_prefill_tc_kernel<D, T>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM_BYTES) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        configured = true;
-    }
-    // one CTA per SM, each walking the items c, c + grid, ...
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            sms < 1)
-            return PKV_ERR_CUDA;
-    }
+    // Set per call (for the current device, from any host thread): a few
+    // microseconds against a kernel of hundreds.
+    if (cudaFuncSetAttribute(paged_prefill_tc_kernel<D, T>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    // one CTA per SM (of the pool's device), each walking the items c,
+    // c + grid, ...
+    const int sms = pool->num_sms;
+    if (sms < 1)
+        return PKV_ERR_CUDA;
     (void)max_q_len;
     const int64_t nitems = (int64_t)prm.nqt * prm.num_q_heads * prm.batch;
     const dim3 grid((unsigned)(nitems < sms ? nitems : sms));
