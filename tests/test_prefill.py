@@ -179,6 +179,10 @@ def _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, seed, k_growth=0.0, with
     # several, some of them empty
     ("bf16", 128, 32, 8, 16, [700, 300, 900, 50], [0, 100, 0, 500]),
     ("f16", 64, 32, 4, 8, [513, 1, 260], [10, 0, 3]),
+    # d 128 with the smallest blocks (4 rows: 16-byte copies) and 8-row
+    # tensor copies
+    ("bf16", 128, 8, 4, 4, [150, 20], [30, 7]),
+    ("f16", 128, 4, 4, 8, [300], [9]),
 ])
 def test_gpu_prefill_matches_oracle(dt, D, Hq, Hkv, bs, news, cached):
     from paged_kv_cache_273_gb300 import pkv
