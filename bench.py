@@ -23,6 +23,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -101,7 +102,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+        # raw samples (the JSON line carries their summary); PKV_CLOCKS_DIR
+        # keeps them somewhere else than the temporary directory
+        out_dir = os.environ.get("PKV_CLOCKS_DIR", tempfile.gettempdir())
+        self.path = os.path.join(out_dir, "clocks_bench_%d.csv" % os.getpid())
 
     def start(self):
         try:
