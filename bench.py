@@ -339,6 +339,28 @@ def time_prefill(dev, stream, peak_tflops: float, B=4, n=4096, reps=10) -> dict:
                     "peak = measured bf16 burst"}
 
 
+# ------------------------------------------------------------------ ranks
+def whole_job(units_per_rank: float, seconds: float, world: int, reduce_max=None):
+    """Whole-job throughput of a weak-scaling run: every rank processed
+    units_per_rank in `seconds` of its own; the job lasted as long as the
+    slowest rank, and all ranks' units count.  reduce_max(x) returns the
+    maximum of x over the ranks (needed when world > 1).  Returns (units per
+    second, the job's seconds)."""
+    t = reduce_max(seconds) if world > 1 else seconds
+    return units_per_rank * world / t, t
+
+
+def dist_max(dist, device):
+    """reduce_max for whole_job over a torch.distributed process group (NCCL
+    with a CUDA device, gloo with the CPU)."""
+    def reduce_max(x: float) -> float:
+        import torch
+        tt = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
+    return reduce_max
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_gpu(args):
     import torch
@@ -430,12 +452,10 @@ def run_gpu(args):
         raise RuntimeError("device error in timed region: %s" % pkv.status_string(status))
 
     step_bytes = sum(bytes_attn[k % S] + bytes_app for k in range(args.steps))
-    t_max = total_ms
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
-    value = step_bytes * world / (t_max / 1e3) / 1e9
+    rmax = dist_max(dist, dev) if world > 1 else None
+    rate, t_max_s = whole_job(step_bytes, total_ms / 1e3, world, rmax)
+    t_max = t_max_s * 1e3
+    value = rate / 1e9
     tok_s = B * args.steps * world / (t_max / 1e3)
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     sampled = [bytes_attn[k % S] for k in range(0, args.steps, EVENT_EVERY)]
@@ -480,11 +500,7 @@ def run_gpu(args):
         e2e_step(k % S)
     e2e_s = time.perf_counter() - t0
     e2e_bytes = sum(bytes_attn[k % S] + bytes_app for k in range(e2e_steps))
-    e2e_val = e2e_bytes / e2e_s / 1e9
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_val = e2e_bytes * world / float(tt.item()) / 1e9
+    e2e_val = whole_job(e2e_bytes, e2e_s, world, rmax)[0] / 1e9
 
     # ---- measured peak
     peaks = {}
