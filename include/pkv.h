@@ -391,6 +391,18 @@ int paged_decode_attention_noalloc(const pkv_pool *pool, const void *q, pkv_dtyp
                                    float scale, float *out, pkv_stream_t stream);
 
 /*
+ * pkv_selftest_wait_timeout — a check of the failure path of the library's
+ * bounded device waits (not part of the method).  Launches one kernel whose
+ * single waiting thread waits, the way every mbarrier wait in this library
+ * does, on a phase that nothing completes; after the wait's time limit
+ * (about one second) it records a timeout in the pool's error word and
+ * returns.  The next pkv_check_error() then returns PKV_ERR_TIMEOUT and the
+ * device stays usable.  Returns PKV_OK when the kernel was launched,
+ * PKV_ERR_INVALID for a null pool, PKV_ERR_CUDA without a device.
+ */
+int pkv_selftest_wait_timeout(const pkv_pool *pool, pkv_stream_t stream);
+
+/*
  * pkv_check_error — synchronise the stream, read and clear the pool's device
  * error word.  Returns PKV_OK, PKV_ERR_BAD_INDEX, PKV_ERR_TIMEOUT (a bounded
  * wait inside a kernel gave up; the kernel returned without finishing), or

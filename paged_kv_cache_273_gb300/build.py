@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
 
 CUDA_SOURCES = ["append.cu", "decode.cu", "decode_f32.cu", "decode_f16.cu", "decode_bf16.cu",
-                "decode_i8.cu", "decode_i4.cu", "decode_noalloc.cu", "prefill.cu"]
+                "decode_i8.cu", "decode_i4.cu", "decode_noalloc.cu", "prefill.cu", "selftest.cu"]
 HOST_SOURCES = ["pool.cpp"]
 HEADERS = ["pkv_internal.h", "device_common.cuh", "decode_kernel.cuh"]
 

@@ -63,6 +63,7 @@ int launch_prefill(const pkv_pool *pool, const void *q, int num_q_heads, const v
                    const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
                    const int32_t *q_start, const int32_t *seq_lens, int batch, int max_q_len,
                    float scale, float *out, pkv_stream_t stream);
+int launch_selftest_wait_timeout(const pkv_pool *pool, pkv_stream_t stream);
 int launch_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, int n,
                       void *k_cache, void *v_cache, void *k_scales, void *v_scales,
                       pkv_stream_t stream);

@@ -475,6 +475,15 @@ int paged_prefill_attention(const pkv_pool *pool, const void *q, int num_q_heads
                                out, stream);
 }
 
+int pkv_selftest_wait_timeout(const pkv_pool *pool, pkv_stream_t stream)
+{
+    if (!pool)
+        return PKV_ERR_INVALID;
+    if (!pool->has_device)
+        return PKV_ERR_CUDA;
+    return pkv::launch_selftest_wait_timeout(pool, stream);
+}
+
 int pkv_check_error(const pkv_pool *pool, pkv_stream_t stream)
 {
     if (!pool)

@@ -44,7 +44,7 @@ SYMBOLS = ("pkv_status_string", "kv_block_pool_init", "kv_block_pool_destroy", "
            "kv_block_share", "kv_block_free", "kv_reserve_slots", "kv_reserve_slots_cow",
            "kv_slot_mapping", "kv_append", "kv_block_copy", "paged_decode_workspace_bytes", "paged_decode_attention",
            "paged_decode_attention_window", "paged_prefill_attention",
-           "paged_decode_attention_noalloc", "pkv_check_error")
+           "paged_decode_attention_noalloc", "pkv_selftest_wait_timeout", "pkv_check_error")
 
 
 class PkvError(RuntimeError):
@@ -113,6 +113,8 @@ def load() -> ctypes.CDLL:
         lib.paged_decode_attention_noalloc.argtypes = [P, P, I, I, P, P, P, P, P, I, P, I, I, F,
                                                        P, P]
         lib.paged_decode_attention_noalloc.restype = I
+        lib.pkv_selftest_wait_timeout.argtypes = [P, P]
+        lib.pkv_selftest_wait_timeout.restype = I
         lib.pkv_check_error.argtypes = [P, P]
         lib.pkv_check_error.restype = I
         _lib = lib
@@ -387,6 +389,13 @@ def paged_decode_attention_noalloc(pool: Pool, q, k_cache, v_cache, block_tables
         _dptr(k_scales), _dptr(v_scales), _dptr(block_tables), block_tables.shape[1],
         _dptr(seq_lens), B, int(max_seq_len), float(scale), _dptr(out), _stream(stream)),
         "paged_decode_attention_noalloc")
+
+
+def pkv_selftest_wait_timeout(pool: Pool, stream=None) -> None:
+    """Launch a kernel whose bounded wait runs out (about a second); the next
+    pkv_check_error() returns PKV_ERR_TIMEOUT."""
+    _check(load().pkv_selftest_wait_timeout(pool.handle, _stream(stream)),
+           "pkv_selftest_wait_timeout")
 
 
 def pkv_check_error(pool: Pool, stream=None) -> int:

@@ -244,3 +244,19 @@ def test_reserve_slots_drives_a_decode_loop():
         want = O.paged_decode_attention(qb, O.BF16, ok, ov, O.BF16, tables, lens, D ** -0.5)
         assert np.max(np.abs(out.cpu().numpy() - want)) <= 2e-3
     assert pkv.pkv_check_error(pool) == pkv.PKV_OK
+
+
+@pytest.mark.gpu
+def test_gpu_bounded_wait_reports_timeout_and_device_stays_usable():
+    """A kernel waits on an mbarrier phase that nothing completes; the bounded
+    wait gives up (about a second), the error word says PKV_ERR_TIMEOUT, and
+    the next attention call on the same device runs and matches the oracle."""
+    import time
+    pool = pkv.kv_block_pool_init(4, 16, 1, 64, W.F16)
+    t0 = time.perf_counter()
+    pkv.pkv_selftest_wait_timeout(pool)
+    assert pkv.pkv_check_error(pool) == pkv.PKV_ERR_TIMEOUT
+    assert time.perf_counter() - t0 < 30.0
+    assert pkv.pkv_check_error(pool) == pkv.PKV_OK     # the word was cleared
+    r = run(W.make_inputs("tiny"))
+    assert r["max_err"] <= r["tol"] and r["error_word"] == pkv.PKV_OK
