@@ -1,18 +1,25 @@
 """Benchmark: decode steps of paged attention on the Llama-3-8B-shaped layer.
 
-One step = the whole hot path over one batch: slot mapping of the new tokens
-(host), kv_append of the 16 new K/V rows, and paged_decode_attention of
-16 sequences x 32 query heads over 4097..4160 cached tokens (bf16 K/V,
-8 KV heads, d 128, block size 16).  Steps cycle through the workload's 64
-consecutive decode steps.
+One step = the whole hot path over one batch: kv_append of the 16 new K/V
+rows and paged_decode_attention of 16 sequences x 32 query heads over
+4097..4160 cached tokens (bf16 K/V, 8 KV heads, d 128, block size 16).
+Steps cycle through the workload's 64 consecutive decode steps.  In the
+device-timed loop the slot mapping of every step is computed on the host
+before the timed region (it is host bookkeeping, not device work); the
+end-to-end loop computes it on the host inside every step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+    python bench.py --profile NAME      # a few calls of one kernel, for ncu
 
 Prints one JSON line.  `value` is achieved GB/s of algorithmic bytes over
-the whole step with inputs resident in HBM; `e2e` repeats the measurement
-through the C ABI with host buffers (host->device copies of the step's
-inputs and the device->host copy of its output inside the timed region).
-The reference arm (--impl reference) times the fp64 CPU oracle.
+the whole step with inputs resident in HBM; the device is kept busy (a GPU
+sleep) while the host queues the timed steps, so host launch latency is not
+part of the device time.  `roofline` times the attention kernel alone in its
+own loop of back-to-back launches.  `e2e` repeats the measurement through the
+C ABI with host buffers: every step computes its slot mapping on the host,
+copies its inputs from one pinned buffer to the device in one copy and its
+output back, and the host reads the result (two steps in flight).  The
+reference arm (--impl reference) times the fp64 CPU oracle.
 """
 from __future__ import annotations
 
@@ -35,9 +42,7 @@ sys.path.insert(0, ROOT)
 from paged_kv_cache_273_gb300 import workloads as W  # noqa: E402
 
 WORKLOAD = "llama3_8b"
-EVENT_EVERY = 10          # timed steps that carry per-launch attention events
 METRIC = "paged decode-attn achieved HBM GB/s (% of GB300 peak) and decode tokens/s/layer"
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_llama3_8b_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_273_gb300", "csrc", f)
                   for f in ("decode_kernel.cuh", "device_common.cuh")]
 
@@ -87,10 +92,96 @@ def attention_bytes_window(wl: W.Workload, lens: np.ndarray, window: int) -> int
     return kv + q + out + table + wl.batch * 4
 
 
+def attention_bytes_unique(wl: W.Workload, lens: np.ndarray, tables: np.ndarray) -> int:
+    """attention_bytes with every cached row counted once, however many
+    sequences' tables point at its block (shared prefix blocks)."""
+    L = lens.astype(np.int64)
+    bs = wl.block_size
+    rows_of = {}                        # block id -> rows read from it (the most any sequence reads)
+    for b in range(len(L)):
+        n = int(-(-L[b] // bs))
+        for j in range(n):
+            r = int(min(bs, L[b] - j * bs))
+            bid = int(tables[b, j])
+            if r > rows_of.get(bid, 0):
+                rows_of[bid] = r
+    rows = sum(rows_of.values())
+    kv = rows * wl.num_kv_heads * row_bytes(wl.kv_dtype, wl.head_dim) * 2
+    if wl.kv_dtype in (W.I8, W.I4):
+        kv += rows * wl.num_kv_heads * 2 * 2
+    return attention_bytes(wl, lens) - attention_kv_bytes(wl, lens) + kv
+
+
+def attention_kv_bytes(wl: W.Workload, lens: np.ndarray) -> int:
+    """The K/V (and scale) part of attention_bytes."""
+    L = int(lens.astype(np.int64).sum())
+    kv = L * wl.num_kv_heads * row_bytes(wl.kv_dtype, wl.head_dim) * 2
+    if wl.kv_dtype in (W.I8, W.I4):
+        kv += L * wl.num_kv_heads * 2 * 2
+    return kv
+
+
 def append_bytes(wl: W.Workload, ntok: int) -> int:
     """New K/V rows read and written once, plus the slot mapping."""
     row = wl.num_kv_heads * wl.head_dim
     return ntok * row * (eb(wl.src_dtype) + eb(wl.kv_dtype)) * 2 + ntok * 4
+
+
+# ------------------------------------------------------------------ device timing helpers
+SLEEP_CYCLES_PER_US = 2000        # the GPU sleep counts SM clocks (about 2 GHz)
+
+
+def sleep_ahead(us: float) -> None:
+    """Queue a GPU sleep of about `us` microseconds on the current stream, so
+    that the host can queue the launches of a timed loop before the device
+    reaches them (the loop's device time then holds no host launch latency)."""
+    import torch
+    torch.cuda._sleep(int(max(us, 10.0) * SLEEP_CYCLES_PER_US))
+
+
+def timed_loop(stream, body, n: int, host_us: float, repeats: int = 3) -> list:
+    """Device time (ms) of n back-to-back calls of body(i), `repeats` times,
+    each timed by one event pair on `stream` after a sleep that covers the
+    host's queueing of the n calls."""
+    import torch
+    out = []
+    for _ in range(repeats):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sleep_ahead(min(n * host_us * 1.5 + 100.0, 500e3))
+        e0.record(stream)
+        for i in range(n):
+            body(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
+def host_queue_us(body, n: int = 20) -> float:
+    """Host microseconds to queue one call of body(i) (measured over n calls,
+    then drained)."""
+    import torch
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n):
+        body(i)
+    t = (time.perf_counter() - t0) / n * 1e6
+    torch.cuda.synchronize()
+    return t
+
+
+def traffic_record(name: str):
+    """DRAM bytes per launch of a kernel from profiles/, while the kernel
+    source it was taken on is unchanged; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_%s_traffic.json" % name)
+    try:
+        with open(path) as f:
+            tr = json.load(f)
+        if tr.get("kernel_source_sha256") == kernel_source_hash():
+            return tr.get("traffic_bytes_per_launch")
+    except Exception:
+        pass
+    return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -163,9 +254,11 @@ def oracle_state(inp: W.Inputs):
     return ok, ov
 
 
-def time_oracle(inp: W.Inputs, ok, ov, seqs, step: int, budget_s: float, max_reps=None):
+def time_oracle(inp: W.Inputs, ok, ov, seqs, step: int, budget_s: float, max_reps=None,
+                nthreads: int = 0):
     """Run the oracle's decode attention for the given sequences until the
-    budget is used; returns (seconds per call, algorithmic bytes per call)."""
+    budget is used; returns (seconds per call, algorithmic bytes per call).
+    nthreads > 0 sets the oracle's thread count (it stays set)."""
     from oracle import oracle as O
     wl = inp.workload
     lens = inp.lens_after_step(step)[seqs]
@@ -176,7 +269,7 @@ def time_oracle(inp: W.Inputs, ok, ov, seqs, step: int, budget_s: float, max_rep
     reps, t0 = 0, time.perf_counter()
     while True:
         O.paged_decode_attention(q, wl.q_dtype, ok, ov, wl.kv_dtype, tables, lens,
-                                 1.0 / np.sqrt(wl.head_dim))
+                                 1.0 / np.sqrt(wl.head_dim), nthreads=nthreads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_reps is not None and reps >= max_reps):
@@ -236,10 +329,10 @@ def config_block(wl, l2_note):
 
 
 # ------------------------------------------------------------------ other workload shapes
-def time_workload(name: str, dev, stream, peak: float, reps: int = 20) -> dict:
-    """Attention on another workload's shape (lengths, tables, dtypes): the
-    caches are filled with random codes / values on the device (timing only;
-    parity is the tests' job).  Back-to-back calls, caches larger than L2."""
+def build_device_workload(name: str, dev):
+    """Pool, caches and call arguments of a workload's decode attention, with
+    the caches filled with random codes / values on the device (timing only;
+    parity is the tests' job)."""
     import torch
     from paged_kv_cache_273_gb300 import pkv
     inp = W.make_inputs(name, values=False)
@@ -265,34 +358,51 @@ def time_workload(name: str, dev, stream, peak: float, reps: int = 20) -> dict:
     out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
     ws = pkv.alloc_workspace(pool, B, Hq, dev)
     max_len = int(lens_h.max())
+    return dict(inp=inp, wl=wl, pool=pool, kc=kc, vc=vc, ks=ks, vs=vs, q=q, lens=lens,
+                lens_h=lens_h, tables=tables, out=out, ws=ws, max_len=max_len)
 
-    def call():
-        pkv.paged_decode_attention(pool, q, kc, vc, tables, lens, 1.0 / np.sqrt(D), out, ws,
-                                   max_len, ks, vs, stream=stream)
+
+def kernel_name(wl) -> str:
+    return "paged_decode_kernel<%d,%d,%s>" % (wl.head_dim, wl.group,
+                                               {W.F32: "f32", W.F16: "f16", W.BF16: "bf16",
+                                                W.I8: "i8", W.I4: "i4"}[wl.kv_dtype])
+
+
+def time_workload(name: str, dev, stream, peak: float, reps: int = 20) -> dict:
+    """Attention on another workload's shape (lengths, tables, dtypes), on
+    device-filled caches: `reps` back-to-back calls, three times, median."""
+    from paged_kv_cache_273_gb300 import pkv
+    d = build_device_workload(name, dev)
+    wl = d["wl"]
+
+    def call(i=0):
+        pkv.paged_decode_attention(d["pool"], d["q"], d["kc"], d["vc"], d["tables"], d["lens"],
+                                   1.0 / np.sqrt(wl.head_dim), d["out"], d["ws"], d["max_len"],
+                                   d["ks"], d["vs"], stream=stream)
 
     for _ in range(3):
         call()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if pkv.pkv_check_error(pool) != pkv.PKV_OK:
+    host_us = host_queue_us(call, 5)
+    ms = statistics.median(timed_loop(stream, call, reps, host_us))
+    if pkv.pkv_check_error(d["pool"]) != pkv.PKV_OK:
         raise RuntimeError("device error timing workload %s" % name)
-    us = e0.elapsed_time(e1) / reps * 1e3
-    nbytes = attention_bytes(wl, lens_h)
-    cache_mb = 2 * kc.numel() * kc.element_size() / 1e6
-    del kc, vc, ks, vs, ws
-    return {"value": nbytes / (us / 1e6) / 1e9, "unit": "GB/s",
-            "frac": nbytes / (us / 1e6) / 1e9 / peak, "launch_us": us,
-            "bytes_per_launch": nbytes, "cache_mb": cache_mb,
-            "kernel": "paged_decode_kernel<%d,%d,%s>" % (D, wl.group,
-                                                         {W.F32: "f32", W.F16: "f16",
-                                                          W.BF16: "bf16", W.I8: "i8",
-                                                          W.I4: "i4"}[wl.kv_dtype]),
-            "note": "back to back, %d calls; logical bytes (shared prefix rows counted per "
-                    "sequence)" % reps}
+    us = ms / reps * 1e3
+    nbytes = attention_bytes(wl, d["lens_h"])
+    res = {"value": nbytes / (us / 1e6) / 1e9, "unit": "GB/s",
+           "frac": nbytes / (us / 1e6) / 1e9 / peak, "launch_us": us,
+           "bytes_per_launch": nbytes,
+           "cache_mb": 2 * d["kc"].numel() * d["kc"].element_size() / 1e6,
+           "kernel": kernel_name(wl), "traffic": traffic_record(name),
+           "note": "back to back, %d calls, median of 3; logical bytes (a shared prefix row "
+                   "counted once per sequence that reads it)" % reps}
+    if wl.shared_prefix_tokens > 0:
+        ub = attention_bytes_unique(wl, d["lens_h"], d["inp"].block_tables)
+        res["unique"] = {"value": ub / (us / 1e6) / 1e9, "unit": "GB/s",
+                         "frac": ub / (us / 1e6) / 1e9 / peak, "bytes_per_launch": ub,
+                         "note": "every cached row counted once (the shared prefix blocks "
+                                 "once for all sequences that share them)"}
+    del d
+    return res
 
 
 def time_prefill(dev, stream, peak_tflops: float, B=4, n=4096, reps=10) -> dict:
@@ -320,15 +430,11 @@ def time_prefill(dev, stream, peak_tflops: float, B=4, n=4096, reps=10) -> dict:
 
     for _ in range(3):
         call()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    host_us = host_queue_us(lambda i: call(), 3)
+    ms = statistics.median(timed_loop(stream, lambda i: call(), reps, host_us))
     if pkv.pkv_check_error(pool) != pkv.PKV_OK:
         raise RuntimeError("device error in the prefill measurement")
-    us = e0.elapsed_time(e1) / reps * 1e3
+    us = ms / reps * 1e3
     flops = 4.0 * B * (n * (n + 1) / 2) * D * Hq          # QK^T and PV over the causal half
     tf = flops / (us / 1e6) / 1e12
     return {"value": tf, "unit": "TFLOP/s", "bound": "tensor", "frac": tf / peak_tflops,
@@ -336,7 +442,7 @@ def time_prefill(dev, stream, peak_tflops: float, B=4, n=4096, reps=10) -> dict:
             "config": "%d prompts x %d tokens, causal, 32 q / 8 KV heads, d 128, bf16, "
                       "block size 16" % (B, n),
             "note": "tcgen05.mma kind::f16, bf16 in, fp32 accumulators in tensor memory; "
-                    "peak = measured bf16 burst"}
+                    "%d calls back to back, median of 3; peak = measured bf16 burst" % reps}
 
 
 # ------------------------------------------------------------------ ranks
@@ -362,6 +468,96 @@ def dist_max(dist, device):
 
 
 # ------------------------------------------------------------------ GPU arm
+ROOF_LAUNCHES = 256       # attention launches per repeat of the roofline loop
+E2E_MIN_STEPS = 256       # end-to-end steps timed whatever --steps is
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def run_e2e(pool, inp, kc, vc, tables, ws, scale, max_len, steps, dev, stream, bytes_attn,
+            bytes_app, world, rmax):
+    """The metric end to end through the C ABI with host buffers.  Every
+    step: the host computes the step's slot mapping into a pinned staging
+    buffer that already holds the step's k, v, q and lengths; one copy moves
+    the buffer to the device; kv_append and paged_decode_attention read their
+    inputs from slices of it; the output is copied back to pinned memory and
+    the host reads it.  Two steps are in flight: the host prepares step k
+    while the device runs step k - 1, and reads step k - 2's output."""
+    import torch
+    from paged_kv_cache_273_gb300 import pkv
+    wl = inp.workload
+    B, Hq, Hkv, D, bs = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
+    S = wl.decode_steps
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    nk, nq = B * Hkv * D * 2, B * Hq * D * 2
+    o_k, o_v, o_q = 0, al(nk), 2 * al(nk)
+    o_slot = o_q + al(nq)
+    o_len = o_slot + al(B * 4)
+    total = o_len + al(B * 4)
+    stage = []
+    for st in range(S):
+        h = torch.empty(total, dtype=torch.uint8).pin_memory()
+        hn = h.numpy()
+        hn[o_k:o_k + nk] = inp.step_k[st].view(np.uint8).reshape(-1)
+        hn[o_v:o_v + nk] = inp.step_v[st].view(np.uint8).reshape(-1)
+        hn[o_q:o_q + nq] = inp.step_q[st].view(np.uint8).reshape(-1)
+        hn[o_len:o_len + B * 4] = inp.lens_after_step(st).view(np.uint8)
+        stage.append(h)
+    d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
+    e_k = d_stage[o_k:o_k + nk].view(torch.bfloat16).view(B, Hkv, D)
+    e_v = d_stage[o_v:o_v + nk].view(torch.bfloat16).view(B, Hkv, D)
+    e_q = d_stage[o_q:o_q + nq].view(torch.bfloat16).view(B, Hq, D)
+    e_slot = d_stage[o_slot:o_slot + B * 4].view(torch.int32)
+    e_lens = d_stage[o_len:o_len + B * 4].view(torch.int32)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    h_out = [torch.empty((B, Hq, D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    checksum = [0.0]
+
+    def host_read(k):
+        done[k % 2].synchronize()
+        checksum[0] += float(h_out[k % 2].numpy()[0, 0, 0])
+
+    def e2e_step(k):
+        s = k % S
+        if k >= 2:
+            host_read(k - 2)
+        slots = stage[s].numpy()[o_slot:o_slot + B * 4].view(np.int32)
+        slots[:] = pkv.kv_slot_mapping(inp.block_tables, bs, (inp.prefix_lens + s).astype(np.int32))
+        d_stage.copy_(stage[s], non_blocking=True)
+        pkv.kv_append(pool, e_k, e_v, e_slot, kc, vc, stream=stream)
+        pkv.paged_decode_attention(pool, e_q, kc, vc, tables, e_lens, scale, out, ws, max_len,
+                                   stream=stream)
+        h_out[k % 2].copy_(out, non_blocking=True)
+        done[k % 2].record(stream)
+
+    for w in range(4):
+        e2e_step(w)
+    host_read(2)
+    host_read(3)
+    torch.cuda.synchronize()
+    n = max(E2E_MIN_STEPS, min(steps, 2000))
+    t0 = time.perf_counter()
+    for k in range(n):
+        e2e_step(k)
+    host_read(n - 2)
+    host_read(n - 1)
+    e2e_s = time.perf_counter() - t0
+    e2e_bytes = sum(bytes_attn[k % S] + bytes_app for k in range(n))
+    value = whole_job(e2e_bytes, e2e_s, world, rmax)[0] / 1e9
+    return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": total,
+            "d2h_bytes_per_step": out.numel() * 4, "steps": n,
+            "note": "one pinned-to-device copy of the step's inputs (k, v, q, slot mapping, "
+                    "lengths), slot mapping on the host in the step, output copied back and "
+                    "read by the host; two steps in flight"}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -408,25 +604,24 @@ def run_gpu(args):
     max_len = int(inp.final_lens.max())
     torch.cuda.synchronize()
 
-    def step(s, ev=None):
-        pkv.kv_append(pool, d_k[s], d_v[s], d_slots[s], kc, vc, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
+    def attend(s):
         pkv.paged_decode_attention(pool, d_q[s], kc, vc, tables, d_lens[s], scale, out, ws,
                                    max_len, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
+
+    def step(k):
+        s = k % S
+        pkv.kv_append(pool, d_k[s], d_v[s], d_slots[s], kc, vc, stream=stream)
+        attend(s)
 
     for w in range(args.warmup):
-        step(w % S)
+        step(w)
     torch.cuda.synchronize()
     if pkv.pkv_check_error(pool) != pkv.PKV_OK:
         raise RuntimeError("device error during warm-up")
+    host_us = host_queue_us(step, 20)
 
     bytes_attn = [attention_bytes(wl, lens_h[s]) for s in range(S)]
     bytes_app = append_bytes(wl, B)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           if k % EVENT_EVERY == 0 else None for k in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if world > 1:
@@ -434,19 +629,18 @@ def run_gpu(args):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)                     # let the sampler take its first reading
+    # The device sleeps while the host queues the first steps (up to the
+    # launch queue's depth), so the timed region holds device work only.
+    sleep_ahead(min(args.steps, 2000) * host_us * 1.5 + 100.0)
     t_start.record(stream)
-    # Events between the append and the attention end the programmatic overlap
-    # of the two launches (~8 us a step), so only every EVENT_EVERY-th step
-    # carries them; the attention time is averaged over those launches.
     for k in range(args.steps):
-        step(k % S, evs[k] if k % EVENT_EVERY == 0 else None)
+        step(k)
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
-    attn_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(0, args.steps, EVENT_EVERY)]
     status = pkv.pkv_check_error(pool)
     if status != pkv.PKV_OK:
         raise RuntimeError("device error in timed region: %s" % pkv.status_string(status))
@@ -457,58 +651,36 @@ def run_gpu(args):
     t_max = t_max_s * 1e3
     value = rate / 1e9
     tok_s = B * args.steps * world / (t_max / 1e3)
-    attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    sampled = [bytes_attn[k % S] for k in range(0, args.steps, EVENT_EVERY)]
-    achieved = sum(sampled) / len(sampled) / (attn_avg_ms / 1e3) / 1e9
+
+    # ---- the attention kernel alone: ROOF_LAUNCHES back-to-back launches
+    # over the 64 decode steps' inputs (same caches), one event pair around
+    # the loop, three repeats, median
+    attn_host_us = host_queue_us(attend, 20)
+    roof_ms = timed_loop(stream, lambda i: attend(i % S), ROOF_LAUNCHES, attn_host_us)
+    launch_ms = statistics.median(roof_ms) / ROOF_LAUNCHES
+    roof_bytes = sum(bytes_attn[i % S] for i in range(ROOF_LAUNCHES)) / ROOF_LAUNCHES
+    achieved = roof_bytes / (launch_ms / 1e3) / 1e9
+    # secondary: the attention launch between appends, events around it (an
+    # event between the two launches ends their overlap, so this is longer)
+    pairs = []
+    for k in range(64):
+        s = k % S
+        pkv.kv_append(pool, d_k[s], d_v[s], d_slots[s], kc, vc, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        attend(s)
+        e1.record(stream)
+        pairs.append((e0, e1))
+    torch.cuda.synchronize()
+    in_step_us = statistics.median(a.elapsed_time(b) for a, b in pairs) * 1e3
+    if pkv.pkv_check_error(pool) != pkv.PKV_OK:
+        raise RuntimeError("device error in the attention loop")
 
     # ---- end to end through the C ABI with host buffers
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_k = [pin(inp.step_k[s].view(np.int16)) for s in range(S)]
-    h_v = [pin(inp.step_v[s].view(np.int16)) for s in range(S)]
-    h_q = [pin(inp.step_q[s].view(np.int16)) for s in range(S)]
-    h_lens = [pin(lens_h[s]) for s in range(S)]
-    h_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
-    h_slot = torch.empty(B, dtype=torch.int32).pin_memory()
-    e_k = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
-    e_v = torch.empty_like(e_k)
-    e_q = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
-    e_slot = torch.empty(B, dtype=torch.int32, device=dev)
-    e_lens = torch.empty(B, dtype=torch.int32, device=dev)
-    h2d = (e_k.numel() * 2 * 2 + e_q.numel() * 2 + B * 4 * 2)
-    d2h = h_out.numel() * 4
-    e2e_steps = min(args.steps, 2000)
+    e2e = run_e2e(pool, inp, kc, vc, tables, ws, scale, max_len, args.steps, dev, stream,
+                  bytes_attn, bytes_app, world, rmax)
 
-    def e2e_step(s):
-        start = (inp.prefix_lens + s).astype(np.int32)
-        h_slot.numpy()[:] = pkv.kv_slot_mapping(inp.block_tables, bs, start)    # host a1
-        e_k.copy_(h_k[s].view(torch.bfloat16), non_blocking=True)
-        e_v.copy_(h_v[s].view(torch.bfloat16), non_blocking=True)
-        e_q.copy_(h_q[s].view(torch.bfloat16), non_blocking=True)
-        e_slot.copy_(h_slot, non_blocking=True)
-        e_lens.copy_(h_lens[s], non_blocking=True)
-        pkv.kv_append(pool, e_k, e_v, e_slot, kc, vc, stream=stream)
-        pkv.paged_decode_attention(pool, e_q, kc, vc, tables, e_lens, scale, out, ws, max_len,
-                                   stream=stream)
-        h_out.copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()     # the host reads the step's result
-
-    for w in range(3):
-        e2e_step(w % S)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for k in range(e2e_steps):
-        e2e_step(k % S)
-    e2e_s = time.perf_counter() - t0
-    e2e_bytes = sum(bytes_attn[k % S] + bytes_app for k in range(e2e_steps))
-    e2e_val = whole_job(e2e_bytes, e2e_s, world, rmax)[0] / 1e9
-
-    # ---- measured peak
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except Exception:
-        pass
+    peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_note = "measured"
     if not peak:
@@ -523,16 +695,14 @@ def run_gpu(args):
     c_src = torch.from_numpy(perm[:cow_blocks // 2].copy()).to(dev)
     c_dst = torch.from_numpy(perm[cow_blocks // 2:].copy()).to(dev)
     cow_bytes = (cow_blocks // 2) * Hkv * bs * D * eb(wl.kv_dtype) * 2 * 2   # K+V, read+write
+
+    def cow(i=0):
+        pkv.kv_block_copy(cow_pool, c_src, c_dst, ck, cv, stream=stream)
+
     for _ in range(3):
-        pkv.kv_block_copy(cow_pool, c_src, c_dst, ck, cv, stream=stream)
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cow()
     cow_reps = 50
-    c0.record(stream)
-    for _ in range(cow_reps):
-        pkv.kv_block_copy(cow_pool, c_src, c_dst, ck, cv, stream=stream)
-    c1.record(stream)
-    torch.cuda.synchronize()
-    cow_ms = c0.elapsed_time(c1) / cow_reps
+    cow_ms = statistics.median(timed_loop(stream, cow, cow_reps, host_queue_us(cow, 5))) / cow_reps
     if pkv.pkv_check_error(cow_pool) != pkv.PKV_OK:
         raise RuntimeError("device error in the block-copy measurement")
     del ck, cv
@@ -540,9 +710,9 @@ def run_gpu(args):
     # ---- sliding-window attention (window 1024) on the same caches.  The
     # window's 67 MB fit in L2, so before every call L2 is refilled with
     # other data (a 256 MB read, clean lines: nothing to write back).  The
-    # flushes and calls run back to back with no host wait in between, and
-    # the time of the flushes alone is subtracted, so neither host launch
-    # latency nor the flush counts.
+    # refills and calls run back to back with no host wait in between, and
+    # the time of the refills alone is subtracted, so neither host launch
+    # latency nor the refill counts.
     win = 1024
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev).fill_(1.0)
     win_bytes = attention_bytes_window(wl, lens_h[0], win)
@@ -555,19 +725,9 @@ def run_gpu(args):
         flush.sum()
         win_call()
     win_reps = 50
-    pairs = []
-    for with_call in (True, False, True, False, True, False):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(win_reps):
-            flush.sum()
-            if with_call:
-                win_call()
-        e1.record(stream)
-        pairs.append((with_call, e0, e1))
-    torch.cuda.synchronize()
-    t_with = sorted(a.elapsed_time(b) for w, a, b in pairs if w)[1]
-    t_flush = sorted(a.elapsed_time(b) for w, a, b in pairs if not w)[1]
+    t_with = statistics.median(timed_loop(stream, lambda i: (flush.sum(), win_call()), win_reps,
+                                          60.0))
+    t_flush = statistics.median(timed_loop(stream, lambda i: flush.sum(), win_reps, 30.0))
     win_ms = (t_with - t_flush) / win_reps
     if pkv.pkv_check_error(pool) != pkv.PKV_OK:
         raise RuntimeError("device error in the sliding-window measurement")
@@ -581,27 +741,23 @@ def run_gpu(args):
     bf16_peak = peaks.get("bf16_tflops") or 1900.0
     prefill = time_prefill(dev, stream, bf16_peak) if world == 1 else None
 
-    traffic = None
-    try:
-        with open(TRAFFIC_FILE) as f:
-            tr = json.load(f)
-        if tr.get("kernel_source_sha256") == kernel_source_hash():
-            traffic = tr.get("traffic_bytes_per_launch")
-    except Exception:
-        pass
-
     if rank == 0:
         cpu = None
         if world == 1:
             from oracle import oracle as O
             O.build()
             ok, ov = oracle_state(inp)
-            seqs = list(range(B))
-            t_call, b_call = time_oracle(inp, ok, ov, seqs, 0, 10.0)
-            cpu = {"value": b_call / t_call / 1e9, "unit": "GB/s", "cores": O.max_threads(),
+            cores = O.max_threads()
+            t_call, b_call = time_oracle(inp, ok, ov, list(range(B)), 0, 10.0, nthreads=cores)
+            t1, b1 = time_oracle(inp, ok, ov, [0], 0, 8.0, nthreads=1)
+            time_oracle(inp, ok, ov, [0], 0, 0.0, max_reps=1, nthreads=cores)   # restore
+            cpu = {"value": b_call / t_call / 1e9, "unit": "GB/s", "cores": cores,
                    "kind": "oracle",
                    "sample": "full decode-step attention (16 seq x 32 heads, 4097 tokens) "
-                             "repeated for ~10 s, fp64 C oracle, OpenMP"}
+                             "repeated for ~10 s, fp64 C oracle, OpenMP",
+                   "one_core": {"value": b1 / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                                "sample": "attention of 1 of the 16 sequences (32 heads, "
+                                          "4097 tokens) repeated for ~8 s on one thread"}}
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
@@ -612,13 +768,17 @@ def run_gpu(args):
             "tokens_per_s_per_layer": tok_s,
             "pct_of_hbm_peak": 100.0 * value / peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "paged_decode_kernel<128,4,bf16>",
-                         "launch_us": attn_avg_ms * 1e3, "launches_timed": len(attn_ms),
-                         "peak_source": peak_note},
+                         "frac": achieved / peak, "traffic": traffic_record(WORKLOAD),
+                         "kernel": kernel_name(wl), "launch_us": launch_ms * 1e3,
+                         "launches_timed": ROOF_LAUNCHES, "repeats": len(roof_ms),
+                         "bytes_per_launch": roof_bytes, "in_step_launch_us": in_step_us,
+                         "peak_source": peak_note,
+                         "note": "%d back-to-back launches over the 64 decode steps' inputs, "
+                                 "one event pair, median of %d; in_step_launch_us: events "
+                                 "around the launch between appends (median of 64)"
+                                 % (ROOF_LAUNCHES, len(roof_ms))},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "e2e": e2e,
             "gpu_launches": 2 * args.steps,
             "extra_kernels": {
                 "kv_block_copy": {"value": cow_bytes / (cow_ms / 1e3) / 1e9, "unit": "GB/s",
@@ -644,13 +804,41 @@ def run_gpu(args):
     return 0
 
 
+def run_profile(name: str) -> int:
+    """A few calls of one kernel on its timing workload, for ncu captures
+    (no timing, no JSON line): NAME is a workload (its decode attention) or
+    'prefill'."""
+    import torch
+    from paged_kv_cache_273_gb300 import pkv
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    if name == "prefill":
+        time_prefill(dev, stream, 1900.0, reps=1)
+        return 0
+    d = build_device_workload(name, dev)
+    wl = d["wl"]
+    for _ in range(4):
+        pkv.paged_decode_attention(d["pool"], d["q"], d["kc"], d["vc"], d["tables"], d["lens"],
+                                   1.0 / np.sqrt(wl.head_dim), d["out"], d["ws"], d["max_len"],
+                                   d["ks"], d["vs"], stream=stream)
+    torch.cuda.synchronize()
+    if pkv.pkv_check_error(d["pool"]) != pkv.PKV_OK:
+        raise RuntimeError("device error profiling %s" % name)
+    print("profiled %s: 4 calls of %s" % (name, kernel_name(wl)))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--profile", default=None,
+                    choices=["gpt2", "llama3_8b", "llama2_70b", "int8", "int4", "prefill"])
     args = ap.parse_args()
+    if args.profile:
+        return run_profile(args.profile)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

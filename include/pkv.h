@@ -136,7 +136,8 @@ int kv_block_alloc(pkv_pool *pool, int n, int32_t *out_ids);
 /*
  * kv_block_share — add one reference to each of ids[0..n), so that another
  * request can point at the same blocks ([VIS] "PagedAttention: the cache in
- * blocks": requests with the same prompt prefix point at the same blocks).
+ * blocks": sequences that begin with the same prompt tokens can reference a
+ * single stored copy of those tokens' blocks).
  * All-or-nothing: PKV_ERR_INVALID if any id is out of range or free.
  */
 int kv_block_share(pkv_pool *pool, const int32_t *ids, int n);
@@ -152,9 +153,10 @@ int kv_block_free(pkv_pool *pool, const int32_t *ids, int n);
  * kv_reserve_slots — host bookkeeping of one append step (prefill or decode).
  * For each sequence b with seq_lens[b] tokens already cached and num_new[b]
  * new tokens (num_new == NULL means 1 each), allocate a new block whenever a
- * new token's position starts a block ([VIS] "PagedAttention…": a request
- * takes a new block only when its last block is full, so at most one block per
- * request is partly empty), record it in the host array block_tables
+ * new token's position starts a block (allocation on demand, [VIS]
+ * "PagedAttention: the cache in blocks": blocks are handed out as a sequence
+ * grows, so each sequence has at most one partly filled block), record it in
+ * the host array block_tables
  * ([B][max_blocks_per_seq], updated in place), and write the slot of every
  * new token to slot_mapping (sequence-major, sum(num_new) entries).
  * All-or-nothing: PKV_ERR_NO_BLOCKS if the pool cannot cover the step,
@@ -166,9 +168,10 @@ int kv_reserve_slots(pkv_pool *pool, int batch, const int32_t *seq_lens, const i
 
 /*
  * kv_reserve_slots_cow — kv_reserve_slots for tables that may point at shared
- * blocks.  [VIS] "PagedAttention: the cache in blocks": requests with the same
- * prefix point at the same blocks, and a block is copied only when one of
- * them writes to it.  The only existing block an append step writes into is a
+ * blocks.  [VIS] "PagedAttention: the cache in blocks": sequences that start
+ * with the same tokens may reference one physical copy of those blocks, and a
+ * private copy is made only at the moment a sharer must modify one.  The only
+ * existing block an append step writes into is a
  * sequence's last, partly filled one (at position seq_lens[b] when
  * seq_lens[b] % bs != 0 and num_new[b] > 0); if its reference count is above
  * one, the sequence gets a private copy first: a fresh block is allocated,
@@ -372,7 +375,9 @@ int paged_prefill_attention(const pkv_pool *pool, const void *q, int num_q_heads
  *
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the rest of the
+ *    process: after a cudaDeviceReset (which unloads the array with the
+ *    library's device image) do not call this entry point on that device.
  *  - Each call clears the part of the array it uses (cudaMemsetAsync on
  *    `stream`), then runs the same kernel as paged_decode_attention.  It
  *    calls no cudaMalloc/cudaFree and no allocating library routine.

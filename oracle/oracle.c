@@ -205,10 +205,10 @@ void orc_append(const void *k_new, const void *v_new, int dtype, const int32_t *
 }
 
 /* ------------------------------------------------------------------ */
-/* Copy-on-write: [VIS] "PagedAttention: the cache in blocks".  Requests */
-/* with the same prefix point at the same blocks, and a block is copied  */
-/* only when one of them writes to it; the writer then holds a private   */
-/* block with the same rows.  So every element (head, offset, i) of      */
+/* Copy-on-write: [VIS] "PagedAttention: the cache in blocks".  Sequences */
+/* that begin alike may reference one physical copy of their first blocks; */
+/* a sharer that must modify such a block first gets a private block with */
+/* the same rows.  So every element (head, offset, i) of      */
 /* block src[j] is copied to the same place in block dst[j].  One call   */
 /* handles one array: a K or V cache (row = head_dim elements), or the   */
 /* int8 scales (row = 1 element of 2 bytes).                             */
@@ -554,8 +554,8 @@ int orc_paged_decode_attention(const void *q, int q_dtype, int num_q_heads, cons
 }
 
 /* ------------------------------------------------------------------ */
-/* Prefill attention ([VIS] "Prefill and decode feel different": prefill */
-/* handles all prompt tokens at once; [GUIDE] "How the cache turns the   */
+/* Prefill attention ([VIS] "Prefill and decode feel different": the    */
+/* prompt is processed as one batch of tokens; [GUIDE] "How the cache turns the */
 /* loop cheap": prefill computes K and V for the whole prompt and stores */
 /* them).  Sequence b has n_b new tokens, the last n_b of its seq_lens[b] */
 /* cached rows (already appended); new token i sits at position          */

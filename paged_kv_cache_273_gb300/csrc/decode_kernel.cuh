@@ -36,7 +36,6 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
-#include <mutex>
 #include <type_traits>
 
 #include "device_common.cuh"
@@ -1206,18 +1205,12 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
     prm.nst = nst;
     const Layout lay = make_layout<D, G, KV>(nst, batch);
 
-    static int configured_smem = 0;   // per instantiation
-    static std::mutex mu;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (lay.total > configured_smem) {
-            if (cudaFuncSetAttribute(paged_decode_kernel<D, G, KV>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     lay.total) != cudaSuccess)
-                return PKV_ERR_CUDA;
-            configured_smem = lay.total;
-        }
-    }
+    // The dynamic shared-memory limit is an attribute of the kernel in the
+    // current device's context (a context that a device reset replaces), so
+    // it is set on every call rather than remembered by the process.
+    if (cudaFuncSetAttribute(paged_decode_kernel<D, G, KV>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) != cudaSuccess)
+        return PKV_ERR_CUDA;
     const int64_t max_tiles =
         (int64_t)batch * pool->num_kv_heads * ((max_seq_len + TILE - 1) / TILE);
     int64_t P = pool->num_sms;

@@ -15,7 +15,10 @@
 // calls on a device share it.  Host code cannot use the array's name as a
 // device address, so the address is looked up once per device with
 // cudaGetSymbolAddress (the first call on a device does this; make that call
-// before any stream capture) and passed to the unchanged decode path.
+// before any stream capture) and passed to the unchanged decode path.  The
+// address stays valid for the life of the device's context: cudaDeviceReset
+// unloads the library's device image with the array, so a process that
+// resets a device must not call this entry point on it again.
 
 #include <cuda_runtime.h>
 

@@ -1,9 +1,10 @@
 // paged_prefill_attention: causal attention of a batch of new tokens over the
 // paged cache (the new tokens' K and V already appended).
 //
-// KV cache visualization page, "Prefill and decode feel different": prefill
-// handles all prompt tokens at once and is bound by arithmetic, not by bytes,
-// so it runs on the fifth-generation tensor cores.  Token i of the n_b new
+// KV cache visualization page, "Prefill and decode feel different": the
+// prompt's tokens are processed together in one pass, which makes the work
+// limited by arithmetic rather than by memory traffic, so it runs on the
+// fifth-generation tensor cores.  Token i of the n_b new
 // tokens of sequence b sits at position p = seq_lens[b] - n_b + i and attends
 // over positions 0..p ("KV cache: the engine behind fast LLM inference",
 // "Concept"), in FlashAttention-style tiles that never hold the whole score

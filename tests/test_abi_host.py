@@ -98,8 +98,8 @@ def test_reserve_slots_matches_oracle_and_wastes_at_most_one_block():
             assert np.array_equal(slots, want)
             lens = lens + n_new
             blocks = -(-lens // bs)
-            # a request takes a new block only when its last one is full:
-            # at most one partly filled block per request
+            # blocks are allocated on demand: each sequence ends with at
+            # most one block that is not full
             waste = blocks * bs - lens
             assert np.all((waste >= 0) & (waste < bs))
             assert NB - pkv.kv_num_free_blocks(p) == int(blocks.sum())

@@ -1,8 +1,8 @@
 """Copy-on-write of shared blocks, on the CPU.
 
-[VIS] "PagedAttention: the cache in blocks": requests with the same prefix
-point at the same blocks, and a block is copied only when one of them
-writes to it.  These tests pin the oracle's block copy and the CoW semantics
+[VIS] "PagedAttention: the cache in blocks": sequences that begin with the
+same tokens can reference one physical copy of those blocks, and a sharer gets
+its own copy of a block only when it has to modify it.  These tests pin the oracle's block copy and the CoW semantics
 (each request keeps seeing exactly its own rows), and check the library's
 host bookkeeping (kv_reserve_slots_cow) against a model written here.
 """

@@ -1,8 +1,8 @@
 """Copy-on-write on the GPU, through the C ABI, against the oracle.
 
-[VIS] "PagedAttention: the cache in blocks": requests with the same prefix
-point at the same blocks, and a block is copied only when one of them writes
-to it.  kv_block_copy must be a bit copy of whole blocks; a fork of one
+[VIS] "PagedAttention: the cache in blocks": sequences that begin alike may
+reference one physical copy of their first blocks, and a sharer gets a private
+copy of a block only when it must modify it.  kv_block_copy must be a bit copy of whole blocks; a fork of one
 prompt into several requests, each appending its own tokens with
 kv_reserve_slots_cow + kv_block_copy + kv_append, must leave every request
 seeing exactly the prompt followed by its own rows, and attention over them

@@ -1,7 +1,7 @@
 """Prefill attention over the paged cache: oracle pins (CPU) and GPU parity.
 
-[VIS] "Prefill and decode feel different": prefill handles all prompt tokens
-at once.  Each new token attends causally over the cached rows up to its own
+[VIS] "Prefill and decode feel different": the prompt is processed as one
+batch of tokens, not one token per step.  Each new token attends causally over the cached rows up to its own
 position, with the softmax of [NOTES] "Concept"; the new tokens' K and V are
 already in the cache (kv_append with T > 1).
 """

@@ -4,9 +4,11 @@ paged_decode_attention_noalloc serves callers that cannot allocate device
 memory when they call (for example from an allocator hook, or in a serving
 loop that must not allocate after start-up): instead of a caller workspace it
 uses a fixed scratch array in the library's device image.  These tests call it
-through the C ABI and check it against the workspace entry point.  The file
-is collected last so that a failure here stops a `-x` run only after every
-other test has run; it also passes on its own in a fresh process.
+through the C ABI and check it against the workspace entry point (the same
+deterministic kernel, so the outputs must be bit-identical) and against the
+fp64 oracle.  The file is collected last so that a failure here stops a `-x`
+run only after every other test has run; it also passes on its own in a fresh
+process.
 """
 import numpy as np
 import pytest
@@ -15,36 +17,69 @@ import torch
 from paged_kv_cache_273_gb300 import pkv
 from paged_kv_cache_273_gb300 import workloads as W
 
-from parity_harness import TOL, append_step, attend_gpu, build, to_device
+from parity_harness import TOL, append_step, attend_gpu, attend_oracle, build, to_device
 
 pytestmark = pytest.mark.gpu
 
 
-def _noalloc(case, s):
-    wl = case.wl
-    lens = case.inp.lens_after_step(s)
-    q = to_device(case.inp.step_q[s], wl.q_dtype)
-    out = torch.full((wl.batch, wl.num_q_heads, wl.head_dim), float("nan"), dtype=torch.float32,
-                     device="cuda")
-    pkv.paged_decode_attention_noalloc(case.pool, q, case.gk.tensor, case.gv.tensor, case.tables_d,
-                                       torch.from_numpy(lens).cuda(), 1.0 / np.sqrt(wl.head_dim),
-                                       out, int(lens.max()))
-    torch.cuda.synchronize()
-    return out.cpu().numpy()
+class _Call:
+    """Device buffers of one no-alloc call, made once so that repeated calls
+    allocate nothing on the torch side either."""
+
+    def __init__(self, case, s):
+        wl = case.wl
+        self.case = case
+        self.lens_h = case.inp.lens_after_step(s)
+        self.q = to_device(case.inp.step_q[s], wl.q_dtype)
+        self.lens = torch.from_numpy(self.lens_h).cuda()
+        self.out = torch.empty((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.float32,
+                               device="cuda")
+
+    def __call__(self):
+        c, wl = self.case, self.case.wl
+        self.out.fill_(float("nan"))
+        pkv.paged_decode_attention_noalloc(
+            c.pool, self.q, c.gk.tensor, c.gv.tensor, c.tables_d, self.lens,
+            1.0 / np.sqrt(wl.head_dim), self.out, int(self.lens_h.max()),
+            None if c.gks is None else c.gks.tensor, None if c.gvs is None else c.gvs.tensor)
+        torch.cuda.synchronize()
+        return self.out.cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["llama2_70b", "gpt2"])
+@pytest.mark.parametrize("name", ["llama2_70b", "gpt2", "int8"])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(name):
     # llama2_70b splits long sequences over many CTAs, so the shared counters
-    # and partials in the scratch array are exercised; gpt2 has many pieces.
+    # and partials in the scratch array are exercised; gpt2 has many pieces;
+    # int8 passes the scale arrays through.
     case = build(W.make_inputs(name))
     append_step(case, 0)
     want = attend_gpu(case, 0)
+    ref = attend_oracle(case, 0)
+    call = _Call(case, 0)
     for _ in range(2):
-        got = _noalloc(case, 0)
-        assert np.all(np.isfinite(got))
-        assert np.max(np.abs(got - want)) <= TOL[case.wl.kv_dtype]
+        got = call()
+        # the same kernel with the same inputs and merge order: bit-identical
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+        assert np.max(np.abs(got - ref)) <= TOL[case.wl.kv_dtype]
     assert pkv.pkv_check_error(case.pool) == pkv.PKV_OK
+
+
+def test_noalloc_calls_leave_free_device_memory_unchanged():
+    # After one warm call (which may load the library's device image, and
+    # with it the scratch array), further calls must not change the device's
+    # free memory: they allocate nothing.
+    case = build(W.make_inputs("llama2_70b"))
+    append_step(case, 0)
+    call = _Call(case, 0)
+    first = call()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        got = call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert np.array_equal(got.view(np.uint32), first.view(np.uint32))
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch():
