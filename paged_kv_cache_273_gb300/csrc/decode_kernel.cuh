@@ -10,16 +10,22 @@
 // How (GB300 design; the pages give no kernel):
 //  * Decode reads the whole cache once per step and does little arithmetic
 //    per byte (KV cache visualization, "Prefill and decode feel different"),
-//    so the kernel is built to stream K/V at HBM bandwidth.  CUDA cores, no
-//    tensor cores: G query heads per K/V byte is far below the tensor ridge.
+//    so the kernel is built to stream K/V at HBM bandwidth.  G query heads
+//    per K/V byte is far below the tensor ridge, but the instructions per
+//    byte are not: with G >= 2 the grouped heads make each 16-token tile a
+//    small dense contraction (16 tokens x G heads x d), done as warp-level
+//    MMAs that serve all heads of the group from one read of the tile, which
+//    cuts the instructions per tile several-fold (fp32 caches and G = 1 stay
+//    on the CUDA cores).
 //  * The batch's work is a list of 16-token tiles, ordered by (sequence,
 //    KV head, tile).  A persistent grid of one CTA per SM takes an equal,
 //    contiguous share of that list (split-K across the sequence axis,
 //    balanced to +-1 tile whatever the length mix).
 //  * In each CTA one producer warp issues bulk async copies (cp.async.bulk)
 //    of whole K and V tiles, located through the block table, into a ring of
-//    shared-memory stages guarded by mbarriers; 15 (or 11) consumer warps take
-//    tiles round-robin, each keeping its own online-softmax state (the
+//    shared-memory stages guarded by mbarriers (the int8 / int4 scales ride
+//    along as 16-byte cp.async copies); 11 consumer warps take tiles
+//    round-robin, each keeping its own online-softmax state (the
 //    FlashAttention idea of never materialising the score row, from the
 //    guide's "Flash attention: don't build the giant matrix").
 //  * At the end of each (sequence, KV head) piece the consumer warps merge
@@ -46,27 +52,35 @@ namespace kern {
 using namespace dev;
 
 constexpr int TILE = 16;        // tokens per pipeline stage
-constexpr int MAX_STAGES = 32;
+constexpr int MAX_STAGES = 64;
 // misc ints in shared memory: [0] abort flag, [2] a constant zero, [4..6)
-// "merge the partials of the first / last piece" flags, [8..8+warps) scan scratch, [32..32+MAX_STAGES) last
-// issued round per stage (+1; 0 = never), [64..66) q copies issued per slot,
-// [66] number of q copies issued so far (they go out in piece order).
-constexpr int MISC_INTS = 72;
+// "merge the partials of the first / last piece" flags, [8..8+warps) scan
+// scratch, [32..32+MAX_STAGES) last issued round per stage (+1; 0 = never),
+// [96..98) q copies issued per slot, [98] number of q copies issued so far
+// (they go out in piece order).
 constexpr int MISC_ISSUED = 32;
-constexpr int MISC_QISSUED = 64;
-constexpr int MISC_QCOUNT = 66;
+constexpr int MISC_QISSUED = MISC_ISSUED + MAX_STAGES;
+constexpr int MISC_QCOUNT = MISC_QISSUED + 2;
+constexpr int MISC_INTS = MISC_QCOUNT + 6;
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// Consumer warps per CTA.  With G = 2 the tile math of 16-bit or int8 K/V
-// (including the tile's V columns held in registers) fits in 128 registers,
-// so 15 consumer warps + the producer fill 16 warps per SM; larger groups
-// need up to 168 registers: 11 + 1.  With G = 1 the pieces (sequence, head)
-// are many and short, and 11 warps merge each piece's state faster than 15
-// (gpt2 shape: 68.6 against 71.5 us; 7 warps: 71.3 us).
+// Tile math: with G >= 2 query heads per KV head and a 16-bit, 8-bit or
+// 4-bit cache, on the tensor cores (warp-level MMA, all heads of the group
+// from one read of the tile); with G = 1 (the MMA's head dimension would be
+// 1/8 used, and its dependent chain per tile outlasts the CUDA cores' on
+// short pieces: 80 against 68 us on the GPT-2-small shape) or an fp32 cache
+// (no exact tensor-core type), on the CUDA cores.
+__host__ __device__ constexpr bool mma_path(int KV, int G) { return KV != PKV_F32 && G >= 2; }
+
+// Consumer warps per CTA: 11 + the producer.  (The tensor-core tile math
+// fits in 128 registers, so 15 consumer warps would fit; measured on the
+// workload shapes, 11 are as fast or faster: 52.4 against 56.5 us on the
+// Llama-3-8B shape, 120 against 139 us on the Llama-2-70B shape.  The
+// CUDA-core tile math takes up to 168 registers.)
 __host__ __device__ constexpr int consumer_warps(int G, int KV)
 {
-    return (KV != PKV_F32 && G == 2) ? 15 : 11;
+    return 11;
 }
 
 // Bits of one cached element.
@@ -83,6 +97,7 @@ __host__ __device__ constexpr bool quantized(int KV) { return KV == PKV_I8 || KV
 
 template <int D, int G, int KV>
 struct Cfg {
+    static constexpr bool MMA = mma_path(KV, G);
     static constexpr int W = consumer_warps(G, KV);
     static constexpr int NTHREADS = (W + 1) * 32;
     static constexpr int ROWB = D * KvBits<KV>::v / 8;   // bytes of one cached row
@@ -94,13 +109,14 @@ struct Cfg {
     static constexpr int NP = TPL * G;             // partial dots per lane
     static constexpr int NF = G >= 2 ? G / 2 : 1;  // scores per lane after reduction
     static constexpr int VE = D / 32;              // V elements per lane
-    static constexpr int KV_BYTES = TILE * ROWB;
+    static constexpr int KV_BYTES = TILE * ROWB;   // one tile of K (or V)
     static constexpr int SC_BYTES = quantized(KV) ? TILE * 2 : 0;
     static constexpr int STAGE_BYTES = round_up(2 * KV_BYTES + 2 * SC_BYTES, 128);
     static constexpr int QSLOT = round_up(G * D * 4, 128);   // fits any q dtype
     static constexpr int MERGE_FLOATS = W * G * (D + 2);
-    // per warp: {p, p} pairs of the tile ([TILE][G] float2) + G rescale factors
-    static constexpr int PSW = round_up(TILE * 2 * G + G, 4);
+    // per warp (CUDA-core tile math only): {p, p} pairs of the tile
+    // ([TILE][G] float2) + G rescale factors
+    static constexpr int PSW = mma_path(KV, G) ? 0 : round_up(TILE * 2 * G + G, 4);
     static constexpr int PS_FLOATS = W * PSW;
     static_assert(NCH >= 4 && (NCH % DS) == 0, "row must split into 16-byte chunks");
     static_assert(TPL * TQ == TILE, "tile split");
@@ -489,9 +505,380 @@ __device__ __forceinline__ float exp2_approx(float x)
     return y;
 }
 
+// ---- tile math on the tensor cores (warp-level MMA) --------------------------
+//
+// For 16-bit, 8-bit and 4-bit caches a warp does a tile's two products as
+// m16n8k16 MMAs with fp32 accumulation (the scores and outputs of all G <= 8
+// heads of the group at once):
+//   S^T = K q^T:   M = the tile's 16 tokens, N = the heads (padded to 8),
+//                  K = 16 elements of d per MMA;
+//   O^T += V^T P^T: M = 16 output elements, N = the heads, K = the 16 tokens.
+// Fragment layout (PTX m16n8k16, .row.col): with gid = lane / 4 and
+// tig = lane % 4, A holds (row gid | gid+8, k 2tig..2tig+1 | 2tig+8..2tig+9),
+// B holds (k 2tig..2tig+1 | 2tig+8..2tig+9, column gid), C holds (row gid |
+// gid+8, columns 2tig, 2tig+1).  Two freedoms keep the shared-memory reads
+// plain 16-byte loads of the rows as the bulk copies left them:
+//  * the order of d inside q.K is free (the same permutation on both
+//    operands): lane tig takes a contiguous quarter of every K row and of q;
+//  * the output elements a row of O^T stands for are free: lane gid owns the
+//    contiguous eighth [gid D/8, (gid+1) D/8) of d, m-tile j's rows gid and
+//    gid+8 being elements gid D/8 + 2j and + 2j + 1.
+// S^T comes out with a lane holding two tokens x two heads; one 8x8
+// transpose (movmatrix) per half tile turns the packed weights into the B
+// fragment of P^T.  Weights are split into a high and a low part of the MMA
+// type (p = hi + lo to ~2^-16 relative) and both are multiplied, so that the
+// weights' rounding stays far inside the error budget; for the same reason a
+// q whose type differs from the cache's is split the same way.  The products
+// of 16-bit (or exactly converted int8 / int4) operands are exact in fp32.
+
+// The MMA operand type of a cache: bf16 for bf16 caches, else fp16 (int8 and
+// int4 codes are exact in fp16).
+template <int KV>
+struct MmaBf16 { static constexpr bool v = KV == PKV_BF16; };
+
+template <bool BF>
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    if constexpr (BF)
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+                     "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+                     "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held one pair per lane (lane
+// holds row lane/4, columns 2(lane%4), +1), in the same layout.
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// (x, y) -> packed pairs hi and lo of the MMA type with hi + lo = (x, y) up to
+// the rounding of lo (relative 2^-16 for bf16, 2^-22 for fp16).
+template <bool BF>
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint32_t &lo)
+{
+    if constexpr (BF) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(x - __low2float(h), y - __high2float(h));
+        hi = *reinterpret_cast<const uint32_t *>(&h);
+        lo = *reinterpret_cast<const uint32_t *>(&l);
+    } else {
+        const __half2 h = __floats2half2_rn(x, y);
+        const __half2 l = __floats2half2_rn(x - __low2float(h), y - __high2float(h));
+        hi = *reinterpret_cast<const uint32_t *>(&h);
+        lo = *reinterpret_cast<const uint32_t *>(&l);
+    }
+}
+
+// Two biased int8 codes (code ^ 0x80) picked by SEL from a word -> an exact
+// fp16 pair: the biased byte becomes the low mantissa bits of 1024 (0x64 in
+// the high byte) and 1152 = 1024 + 128 (0x6480) is subtracted.  SEL 0x4140
+// takes bytes 0, 1; 0x4342 bytes 2, 3.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t i8pair_to_half2(uint32_t biased)
+{
+    const uint32_t t = __byte_perm(biased, 0x64646464u, SEL);
+    uint32_t h;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(t), "r"(0x64806480u));
+    return h;
+}
+
+template <int D, int KV>
+struct MmaCfg {
+    static constexpr int ROWB = D * KvBits<KV>::v / 8;   // bytes of one cached row
+    static constexpr int KQB = ROWB / 4;                  // a lane's quarter of a K row
+    static constexpr int KCH = KQB / 16;                  // its 16-byte chunks
+    static constexpr int KS = D / 16;                     // k-steps of q.K (16 elements each)
+    static constexpr int VB = ROWB / 8;                   // a lane's eighth of a V row
+    static constexpr int MT = D / 16;                     // m-tiles of O^T
+    // 16-bit rows of d = 128 are read in a chunk order rotated by lane pairs,
+    // which spreads a quarter-warp's 16-byte reads over all banks but the
+    // two tokens' (2-way conflict instead of 4-way)
+    static constexpr bool ROTATE = KvBits<KV>::v == 16 && KCH == 4;
+    static_assert(KCH >= 1 || KV == PKV_I4, "K quarter rows are whole 16-byte chunks");
+};
+
+// Element of d (within the lane's quarter of the row, offset tig * D / 4)
+// that element u of half h of the q B fragment of k-step ks stands for; the
+// same element the K A fragment's pair holds.
+template <int D, int KV>
+__device__ __forceinline__ int q_elem_index(int ks, int h, int u, int rot)
+{
+    if constexpr (KvBits<KV>::v == 16) {
+        // chunk slot ks / 2 (holding chunk (ks / 2 + rot) mod KCH); words
+        // 2 (ks % 2) + h of it
+        constexpr int KCH = MmaCfg<D, KV>::KCH;
+        const int chunk = ((ks >> 1) + rot) & (KCH - 1);
+        return 8 * chunk + 4 * (ks & 1) + 2 * h + u;
+    } else if constexpr (KV == PKV_I8) {
+        return 4 * ks + 2 * h + u;                       // word ks, bytes 2h + u
+    } else {
+        // 4-bit: word w = ks / 2 holds codes 8w..8w+7; pair k = 2 (ks % 2) + h
+        // is codes (8w + k, 8w + k + 4)
+        return 8 * (ks >> 1) + 2 * (ks & 1) + h + 4 * u;
+    }
+}
+
+template <int D, int G, int KV, bool QS>
+struct MmaState {
+    uint32_t qh[D / 16][2];                 // q B fragments (high part)
+    uint32_t ql[QS ? D / 16 : 1][2];        // low part (q of another type only)
+    float acc[D / 16][4];                   // O^T C fragments
+    float m[2], l[2];                       // heads 2 tig, 2 tig + 1 (l: this lane's tokens)
+};
+
+// q of the piece's G heads (in shared memory, q_dtype) -> B fragments.
+template <int D, int G, int KV, bool QS>
+__device__ __forceinline__ void load_q_mma(MmaState<D, G, KV, QS> &st, const unsigned char *qs,
+                                           int q_dtype, int lane)
+{
+    constexpr bool BF = MmaBf16<KV>::v;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int rot = MmaCfg<D, KV>::ROTATE ? (tig >> 1) * 2 : 0;
+    const int base = gid * D + tig * (D / 4);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float x0 = 0.0f, x1 = 0.0f;
+            if (gid < G) {
+                x0 = q_elem(qs, base + q_elem_index<D, KV>(ks, h, 0, rot), q_dtype);
+                x1 = q_elem(qs, base + q_elem_index<D, KV>(ks, h, 1, rot), q_dtype);
+            }
+            uint32_t hi, lo;
+            split_pair<BF>(x0, x1, hi, lo);
+            st.qh[ks][h] = hi;
+            if constexpr (QS)
+                st.ql[ks][h] = lo;
+        }
+}
+
+// One 16-token tile: scores, online softmax, weighted V.  nvalid: tokens of
+// the tile inside the sequence; tlo: first token inside the window.  The
+// stage is released (empty barrier) as soon as its last byte has been read.
+template <int D, int G, int KV, bool QS>
+__device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsigned char *sK,
+                                         const unsigned char *sV, const __half *sKS,
+                                         const __half *sVS, int nvalid, int tlo, float scale_log2,
+                                         int lane, uint64_t *empty_bar)
+{
+    using M = MmaCfg<D, KV>;
+    constexpr bool BF = MmaBf16<KV>::v;
+    constexpr int ROWB = M::ROWB;
+    const int gid = lane >> 2, tig = lane & 3;
+
+    // ---- S^T = K q^T (rows gid, gid + 8 of the tile; the lane's quarter of d)
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    {
+        const unsigned char *r0 = sK + gid * ROWB + tig * M::KQB;
+        const unsigned char *r1 = r0 + 8 * ROWB;
+        if constexpr (KvBits<KV>::v == 16) {
+            const int rot = M::ROTATE ? (tig >> 1) * 2 : 0;
+#pragma unroll
+            for (int c = 0; c < M::KCH; ++c) {
+                const int ch = (c + rot) & (M::KCH - 1);
+                const uint4 x = *reinterpret_cast<const uint4 *>(r0 + ch * 16);
+                const uint4 y = *reinterpret_cast<const uint4 *>(r1 + ch * 16);
+                mma_16816<BF>(s, x.x, y.x, x.y, y.y, st.qh[2 * c][0], st.qh[2 * c][1]);
+                mma_16816<BF>(s, x.z, y.z, x.w, y.w, st.qh[2 * c + 1][0], st.qh[2 * c + 1][1]);
+                if constexpr (QS) {
+                    mma_16816<BF>(s, x.x, y.x, x.y, y.y, st.ql[2 * c][0], st.ql[2 * c][1]);
+                    mma_16816<BF>(s, x.z, y.z, x.w, y.w, st.ql[2 * c + 1][0],
+                                  st.ql[2 * c + 1][1]);
+                }
+            }
+        } else if constexpr (KV == PKV_I8) {
+#pragma unroll
+            for (int c = 0; c < M::KCH; ++c) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(r0 + c * 16);
+                const uint4 y = *reinterpret_cast<const uint4 *>(r1 + c * 16);
+                const uint32_t xw[4] = {x.x ^ 0x80808080u, x.y ^ 0x80808080u, x.z ^ 0x80808080u,
+                                        x.w ^ 0x80808080u};
+                const uint32_t yw[4] = {y.x ^ 0x80808080u, y.y ^ 0x80808080u, y.z ^ 0x80808080u,
+                                        y.w ^ 0x80808080u};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int ks = 4 * c + i;
+                    const uint32_t a0 = i8pair_to_half2<0x4140u>(xw[i]);
+                    const uint32_t a2 = i8pair_to_half2<0x4342u>(xw[i]);
+                    const uint32_t a1 = i8pair_to_half2<0x4140u>(yw[i]);
+                    const uint32_t a3 = i8pair_to_half2<0x4342u>(yw[i]);
+                    mma_16816<BF>(s, a0, a1, a2, a3, st.qh[ks][0], st.qh[ks][1]);
+                    if constexpr (QS)
+                        mma_16816<BF>(s, a0, a1, a2, a3, st.ql[ks][0], st.ql[ks][1]);
+                }
+            }
+        } else {
+            static_assert(KV == PKV_I4 && D == 128, "4-bit rows are d = 128");
+            const uint4 x = *reinterpret_cast<const uint4 *>(r0);
+            const uint4 y = *reinterpret_cast<const uint4 *>(r1);
+            const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+            const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int w = ks >> 1, k0 = 2 * (ks & 1);
+                const uint32_t a0 = i4pair_to_half2(xw[w], k0);
+                const uint32_t a2 = i4pair_to_half2(xw[w], k0 + 1);
+                const uint32_t a1 = i4pair_to_half2(yw[w], k0);
+                const uint32_t a3 = i4pair_to_half2(yw[w], k0 + 1);
+                mma_16816<BF>(s, a0, a1, a2, a3, st.qh[ks][0], st.qh[ks][1]);
+                if constexpr (QS)
+                    mma_16816<BF>(s, a0, a1, a2, a3, st.ql[ks][0], st.ql[ks][1]);
+            }
+        }
+    }
+
+    // ---- the lane's eighth of the V rows of tokens 2tig, 2tig+1, 2tig+8,
+    // 2tig+9, and the scales; then the stage goes back to the producer
+    constexpr int VW = (M::VB + 3) / 4;           // 32-bit words per token (>= 2)
+    uint32_t vw[4][VW];
+    {
+        const int toks[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const unsigned char *p = sV + toks[i] * ROWB + gid * M::VB;
+            if constexpr (M::VB >= 16) {
+#pragma unroll
+                for (int c = 0; c < M::VB / 16; ++c) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(p + 16 * c);
+                    vw[i][4 * c] = x.x; vw[i][4 * c + 1] = x.y;
+                    vw[i][4 * c + 2] = x.z; vw[i][4 * c + 3] = x.w;
+                }
+            } else {
+                const uint2 x = *reinterpret_cast<const uint2 *>(p);
+                vw[i][0] = x.x; vw[i][1] = x.y;
+            }
+        }
+        if constexpr (KvBits<KV>::v == 16) {
+            // rows past the sequence end may hold anything (0 * NaN is NaN)
+            if (nvalid < TILE) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (toks[i] >= nvalid)
+#pragma unroll
+                        for (int u = 0; u < VW; ++u)
+                            vw[i][u] = 0u;
+            }
+        }
+    }
+    float ks0 = 1.0f, ks1 = 1.0f, vs0 = 1.0f, vs1 = 1.0f;
+    if constexpr (quantized(KV)) {
+        ks0 = __half2float(sKS[gid]);
+        ks1 = __half2float(sKS[gid + 8]);
+        vs0 = __half2float(sVS[gid]);
+        vs1 = __half2float(sVS[gid + 8]);
+    }
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(empty_bar);
+
+    // ---- online softmax (log2 domain) of heads 2tig, 2tig+1 over tokens
+    // gid, gid+8 of this lane; the other lanes of the head differ in gid
+    const bool v0 = gid < nvalid && gid >= tlo;
+    const bool v1 = gid + 8 < nvalid && gid + 8 >= tlo;
+    const float sc0 = scale_log2 * ks0, sc1 = scale_log2 * ks1;
+    const float x0 = v0 ? s[0] * sc0 : -INFINITY;   // token gid, head 2tig
+    const float x1 = v0 ? s[1] * sc0 : -INFINITY;   // token gid, head 2tig + 1
+    const float x2 = v1 ? s[2] * sc1 : -INFINITY;   // token gid + 8, head 2tig
+    const float x3 = v1 ? s[3] * sc1 : -INFINITY;   // token gid + 8, head 2tig + 1
+    const bool above = fmaxf(x0, x2) > st.m[0] || fmaxf(x1, x3) > st.m[1];
+    if (__any_sync(FULL_MASK, above)) {
+        // the running maxima move (softmax is shift invariant: any running
+        // value that is one of the scores seen is exact)
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int mask = 4; mask < 32; mask <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, mask));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, mask));
+        }
+        const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
+        const float c0 = exp2_approx(st.m[0] - n0), c1 = exp2_approx(st.m[1] - n1);
+        st.m[0] = n0;
+        st.m[1] = n1;
+        st.l[0] *= c0;
+        st.l[1] *= c1;
+#pragma unroll
+        for (int j = 0; j < M::MT; ++j) {
+            st.acc[j][0] *= c0;
+            st.acc[j][2] *= c0;
+            st.acc[j][1] *= c1;
+            st.acc[j][3] *= c1;
+        }
+    }
+    float p0 = exp2_approx(x0 - st.m[0]), p1 = exp2_approx(x1 - st.m[1]);
+    float p2 = exp2_approx(x2 - st.m[0]), p3 = exp2_approx(x3 - st.m[1]);
+    st.l[0] += p0 + p2;
+    st.l[1] += p1 + p3;
+    if constexpr (quantized(KV)) {
+        // V codes are dequantized through the weights: p * s_v of the token
+        p0 = v0 ? p0 * vs0 : 0.0f;
+        p1 = v0 ? p1 * vs0 : 0.0f;
+        p2 = v1 ? p2 * vs1 : 0.0f;
+        p3 = v1 ? p3 * vs1 : 0.0f;
+    }
+    // P^T as the B fragment: (token gid | gid+8, heads 2tig, 2tig+1) pairs,
+    // transposed to (tokens 2tig, 2tig+1 | +8, head gid)
+    uint32_t ph0, pl0, ph1, pl1;
+    split_pair<BF>(p0, p1, ph0, pl0);
+    split_pair<BF>(p2, p3, ph1, pl1);
+    const uint32_t bh0 = transpose8x8(ph0), bh1 = transpose8x8(ph1);
+    const uint32_t bl0 = transpose8x8(pl0), bl1 = transpose8x8(pl1);
+
+    // ---- O^T += V^T P^T, m-tile j: rows gid, gid+8 = elements 2j, 2j+1 of
+    // the lane's eighth of d
+#pragma unroll
+    for (int j = 0; j < M::MT; ++j) {
+        uint32_t a0, a1, a2, a3;
+        if constexpr (KvBits<KV>::v == 16) {
+            a0 = __byte_perm(vw[0][j], vw[1][j], 0x5410u);
+            a1 = __byte_perm(vw[0][j], vw[1][j], 0x7632u);
+            a2 = __byte_perm(vw[2][j], vw[3][j], 0x5410u);
+            a3 = __byte_perm(vw[2][j], vw[3][j], 0x7632u);
+        } else if constexpr (KV == PKV_I8) {
+            // bytes 2j, 2j+1 of the token's eighth: word j / 2
+            const int w = j >> 1;
+            const uint32_t xa = vw[0][w] ^ 0x80808080u, xb = vw[1][w] ^ 0x80808080u;
+            const uint32_t xc = vw[2][w] ^ 0x80808080u, xd = vw[3][w] ^ 0x80808080u;
+            // interleave the two tokens' bytes: (A.b, B.b, A.b', B.b')
+            const uint32_t tab = (j & 1) ? __byte_perm(xa, xb, 0x7362u) : __byte_perm(xa, xb, 0x5140u);
+            const uint32_t tcd = (j & 1) ? __byte_perm(xc, xd, 0x7362u) : __byte_perm(xc, xd, 0x5140u);
+            a0 = i8pair_to_half2<0x4140u>(tab);
+            a1 = i8pair_to_half2<0x4342u>(tab);
+            a2 = i8pair_to_half2<0x4140u>(tcd);
+            a3 = i8pair_to_half2<0x4342u>(tcd);
+        } else {
+            // codes 2j, 2j+1 of the token's eighth (16 codes in two words):
+            // interleave the two tokens' bytes so that a half holds one
+            // token's four codes, then one nibble pair per half-word
+            const int w = j >> 2, k = (2 * j) & 3;
+            const uint32_t tab = (j & 2) ? __byte_perm(vw[0][w], vw[1][w], 0x7632u)
+                                         : __byte_perm(vw[0][w], vw[1][w], 0x5410u);
+            const uint32_t tcd = (j & 2) ? __byte_perm(vw[2][w], vw[3][w], 0x7632u)
+                                         : __byte_perm(vw[2][w], vw[3][w], 0x5410u);
+            a0 = i4pair_to_half2(tab, k);
+            a1 = i4pair_to_half2(tab, k + 1);
+            a2 = i4pair_to_half2(tcd, k);
+            a3 = i4pair_to_half2(tcd, k + 1);
+        }
+        mma_16816<BF>(st.acc[j], a0, a1, a2, a3, bh0, bh1);
+        mma_16816<BF>(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+    }
+}
+
 // ---- the kernel ---------------------------------------------------------------
 
-template <int D, int G, int KV>
+// QS: q's type differs from the MMA operand type, so q is split into a high
+// and a low part (tensor-core tile math only).
+template <int D, int G, int KV, bool QS>
 __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kernel(const Params p)
 {
     using C = Cfg<D, G, KV>;
@@ -522,8 +909,10 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     const int B = p.batch;
 
     if (tid == 0) {
+        // full: the producer's expect-tx arrival, plus (quantized caches) the
+        // arrival that tracks the scales' cp.async copies
         for (int s = 0; s < p.nst; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], quantized(KV) ? 2 : 1);
             mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -555,12 +944,14 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     // Tiles of sequence b: from the one holding its first attended row to the
     // one holding its last.
     auto seq_tiles = [&](int b) { return (s_len[b] + TILE - 1) / TILE - s_lo[b] / TILE; };
-    {
+    // Exclusive prefix over the sequences of value(b), written to out[0..B];
+    // thread t takes a contiguous run of sequences, then warp and block scans.
+    auto block_scan = [&](auto value, int *out) {
         const int per = (B + NTHREADS - 1) / NTHREADS;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         int sum = 0;
         for (int b = b0; b < b1; ++b)
-            sum += seq_tiles(b) * Hkv;
+            sum += value(b);
         int incl = sum;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -586,13 +977,15 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         __syncthreads();
         int base = (warp > 0 ? wsum[warp - 1] : 0) + incl - sum;
         for (int b = b0; b < b1; ++b) {
-            s_tstart[b] = base;
-            base += seq_tiles(b) * Hkv;
+            out[b] = base;
+            base += value(b);
         }
         if (tid == 0)
-            s_tstart[B] = wsum[NTHREADS / 32 - 1];
-    }
-    __syncthreads();
+            out[B] = wsum[NTHREADS / 32 - 1];
+        __syncthreads();
+    };
+    // the prefix of tiles
+    block_scan([&](int b) { return seq_tiles(b) * Hkv; }, s_tstart);
 
     // The T tiles are split over P = min(grid, T) CTAs, so that every CTA
     // that takes part owns at least one tile and the CTAs holding pieces of
@@ -695,15 +1088,15 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     unsigned char *sVS = sKS + C::SC_BYTES;
                     const int rows_per_copy = bs >= TILE ? TILE : bs;
                     const uint32_t kv_copy = (uint32_t)(rows_per_copy * C::ROWB);
-                    const uint32_t sc_copy = (uint32_t)(rows_per_copy * 2);
-                    // Count the bytes of the copies that will be issued.
+                    const int sc_copy = rows_per_copy * 2;
+                    // Count the bytes of the bulk copies that will be issued.
                     uint32_t total = 0;
                     bool bad = false;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         if (u < cur.nblk) {
                             if (cur.id[u] >= 0 && cur.id[u] < p.num_blocks)
-                                total += 2 * kv_copy + (quantized(KV) ? 2 * sc_copy : 0);
+                                total += 2 * kv_copy;
                             else
                                 bad = true;
                         }
@@ -725,11 +1118,30 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                             bulk_g2s_hint(sV + dst_row * C::ROWB, p.v_cache + row0 * C::ROWB,
                                           kv_copy, &full[st], policy);
                             if constexpr (quantized(KV)) {
-                                bulk_g2s(sKS + dst_row * 2, p.k_scales + row0, sc_copy, &full[st]);
-                                bulk_g2s(sVS + dst_row * 2, p.v_scales + row0, sc_copy, &full[st]);
+                                // The scales (32 bytes of each array per 16
+                                // rows) go by 16-byte (8-byte for 4-row
+                                // blocks) cp.async copies: as two more bulk
+                                // copies they would double the tile's copy
+                                // count, and small tiles are bound by the
+                                // bulk-copy unit's rate per copy, not bytes.
+                                const unsigned char *ksrc =
+                                    reinterpret_cast<const unsigned char *>(p.k_scales + row0);
+                                const unsigned char *vsrc =
+                                    reinterpret_cast<const unsigned char *>(p.v_scales + row0);
+                                if (sc_copy >= 16) {
+                                    for (int o = 0; o < sc_copy; o += 16) {
+                                        cp_async_16b(sKS + dst_row * 2 + o, ksrc + o);
+                                        cp_async_16b(sVS + dst_row * 2 + o, vsrc + o);
+                                    }
+                                } else {
+                                    cp_async_8b(sKS + dst_row * 2, ksrc);
+                                    cp_async_8b(sVS + dst_row * 2, vsrc);
+                                }
                             }
                         }
                     }
+                    if constexpr (quantized(KV))
+                        cp_async_mbar_arrive(&full[st]);
                         t_done = true;
                     }
                     if (__all_sync(FULL_MASK, q_done && t_done))
@@ -846,14 +1258,18 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             const int lo = s_lo[b];
 
             // q of this (sequence, KV head) group.
-            QRegs<D, G, KV> qr;
+            QRegs<D, G, KV> qr;             // CUDA-core tile math
+            MmaState<D, G, KV, QS> mst;     // tensor-core tile math
             {
                 const int slot = qn & 1;
                 if (!mbar_wait_bounded(&qfull[slot], (qn >> 1) & 1, abort_flag) && !*abort_flag) {
                     *abort_flag = 1;
                     atomicOr(p.err, PKV_EBIT_TIMEOUT);
                 }
-                load_q<D, G, KV>(qr, qring + slot * C::QSLOT, ds, p.q_dtype);
+                if constexpr (C::MMA)
+                    load_q_mma<D, G, KV, QS>(mst, qring + slot * C::QSLOT, p.q_dtype, lane);
+                else
+                    load_q<D, G, KV>(qr, qring + slot * C::QSLOT, ds, p.q_dtype);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&qempty[slot]);
@@ -872,11 +1288,24 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
 #pragma unroll
                 for (int e = 0; e < C::VE; ++e)
                     acc[g][e] = 0.0f;
+            if constexpr (C::MMA) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    mst.m[r] = -INFINITY;
+                    mst.l[r] = 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        mst.acc[j][u] = 0.0f;
+            }
 
             const int kfirst = k0 + (w - k0 % W + W) % W;
-            int st = kfirst % p.nst;                 // stage and ring round of tile kfirst
-            int rnd = kfirst / p.nst;
             for (int k = kfirst; k < k1; k += W) {
+                // tile k sits in ring stage st = k mod nst, round rnd = k / nst
+                const int rnd = k / p.nst;
+                const int st = k - rnd * p.nst;
                 const int ti = ti0 + (k - k0);
                 const int nvalid = min(TILE, L - TILE * ti);
                 const int tlo = lo - TILE * ti;          // > 0 only in the window's first tile
@@ -898,166 +1327,191 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 const unsigned char *sV = sK + C::KV_BYTES;
                 const __half *sKS = reinterpret_cast<const __half *>(sV + C::KV_BYTES);
                 const __half *sVS = sKS + TILE;
-                // After the reduction below the lane holds token t, heads g0 + r.
-                const int t = tq + C::TQ * (ds >> 1);
-                const int g0 = G >= 2 ? (G / 2) * (ds & 1) : 0;
+                if constexpr (C::MMA) {
+                    mma_tile<D, G, KV, QS>(mst, sK, sV, sKS, sVS, nvalid, tlo, p.scale_log2,
+                                           lane, &empty[st]);
+                } else {
+                    // After the reduction below the lane holds token t, heads g0 + r.
+                    const int t = tq + C::TQ * (ds >> 1);
+                    const int g0 = G >= 2 ? (G / 2) * (ds & 1) : 0;
 
-                // ---- take this lane's part of the tile into registers and hand
-                // the stage back at once, so that the next copy into it starts
-                // while this warp computes
-                uint4 kr[C::TPL][C::CPL];
-                load_k<D, G, KV>(kr, sK, tq, ds);
-                float ks_t = 1.0f, vs_t = 1.0f;
-                if constexpr (quantized(KV)) {
-                    ks_t = __half2float(sKS[t]);
-                    vs_t = __half2float(sVS[t]);
-                }
-                // (with G = 8 the heads' accumulators need the registers; V is
-                // then read from the stage, which is released after P.V)
-                constexpr bool VREG = VRaw<D, KV>::IN_REGS && G <= 4;
-                typename VRaw<D, KV>::type vr[TILE];
-                if constexpr (VREG) {
-#pragma unroll
-                    for (int tt = 0; tt < TILE; ++tt)
-                        vr[tt] = load_v_raw<D, KV>(sV, tt, lane);
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&empty[st]);
-                }
+                    // ---- take this lane's part of the tile into registers and hand
+                    // the stage back at once, so that the next copy into it starts
+                    // while this warp computes
+                    uint4 kr[C::TPL][C::CPL];
+                    load_k<D, G, KV>(kr, sK, tq, ds);
+                    float ks_t = 1.0f, vs_t = 1.0f;
+                    if constexpr (quantized(KV)) {
+                        ks_t = __half2float(sKS[t]);
+                        vs_t = __half2float(sVS[t]);
+                    }
+                    // (with G = 8 the heads' accumulators need the registers; V is
+                    // then read from the stage, which is released after P.V)
+                    constexpr bool VREG = VRaw<D, KV>::IN_REGS && G <= 4;
+                    typename VRaw<D, KV>::type vr[TILE];
+                    if constexpr (VREG) {
+    #pragma unroll
+                        for (int tt = 0; tt < TILE; ++tt)
+                            vr[tt] = load_v_raw<D, KV>(sV, tt, lane);
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&empty[st]);
+                    }
 
-                // ---- scores: partial dots, then reduce-scatter over the DS lanes
-                float part[C::NP];
-#pragma unroll
-                for (int j = 0; j < C::NP; ++j)
-                    part[j] = 0.0f;
-                qk_tile<D, G, KV>(part, qr, kr);
-                reduce_scatter<C::NP, C::DS / 2>(part, ds);
-                float s[C::NF];
-                float kscale = p.scale_log2;
-                if constexpr (quantized(KV))
-                    kscale *= ks_t;
-                bool above = false;
-#pragma unroll
-                for (int r = 0; r < C::NF; ++r) {
-                    s[r] = (t < nvalid && t >= tlo) ? part[r] * kscale : -INFINITY;
-                    above |= s[r] > m_run[r];
-                }
-                // The running maximum only needs to move when some score
-                // exceeds it (softmax is shift invariant, so any running value
-                // that is one of the scores seen is exact); most tiles skip
-                // the per-head maximum and the rescale.
-                const bool moved = __any_sync(FULL_MASK, above);
-                float corr[C::NF];
-                if (moved) {
-#pragma unroll
+                    // ---- scores: partial dots, then reduce-scatter over the DS lanes
+                    float part[C::NP];
+    #pragma unroll
+                    for (int j = 0; j < C::NP; ++j)
+                        part[j] = 0.0f;
+                    qk_tile<D, G, KV>(part, qr, kr);
+                    reduce_scatter<C::NP, C::DS / 2>(part, ds);
+                    float s[C::NF];
+                    float kscale = p.scale_log2;
+                    if constexpr (quantized(KV))
+                        kscale *= ks_t;
+                    bool above = false;
+    #pragma unroll
                     for (int r = 0; r < C::NF; ++r) {
-                        float mx = s[r];
-#pragma unroll
-                        for (int mask = 2; mask < 32; mask <<= 1)
-                            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, mask));
-                        const float mnew = fmaxf(m_run[r], mx);   // finite: a valid token
-                        corr[r] = exp2_approx(m_run[r] - mnew);
-                        l_run[r] *= corr[r];
-                        m_run[r] = mnew;
+                        s[r] = (t < nvalid && t >= tlo) ? part[r] * kscale : -INFINITY;
+                        above |= s[r] > m_run[r];
                     }
-                }
-                float pr[C::NF];
-#pragma unroll
-                for (int r = 0; r < C::NF; ++r) {
-                    pr[r] = exp2_approx(s[r] - m_run[r]);
-                    l_run[r] += pr[r];
-                }
-                // Publish {p, p} pairs (p times the V scale for int8) and, when
-                // the maximum moved, the rescale factors.
-                if (G >= 2 || (ds & 1) == 0) {
-                    const float vsc = vs_t;
-                    float2 *pp = reinterpret_cast<float2 *>(ps + t * 2 * G) + g0;
-#pragma unroll
-                    for (int r = 0; r < C::NF; ++r) {
-                        const float v = pr[r] * vsc;
-                        pp[r] = make_float2(v, v);
-                    }
-                    if (moved && tq == 0 && (ds >> 1) == 0) {
-#pragma unroll
-                        for (int r = 0; r < C::NF; ++r)
-                            ps[TILE * 2 * G + g0 + r] = corr[r];
-                    }
-                }
-                __syncwarp();
-
-                // ---- weighted V
-                if (moved) {
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float cg = ps[TILE * 2 * G + g];
-#pragma unroll
-                        for (int e = 0; e < C::VE; ++e)
-                            acc[g][e] *= cg;
-                    }
-                }
-                auto pv_token = [&](int tt) {
-                    float v[C::VE];
-                    if constexpr (VREG)
-                        unpack_v<D, KV>(v, vr[tt]);
-                    else
-                        load_v<D, KV>(v, sV, tt, lane);
-                    const float *pt = ps + tt * 2 * G;
-                    if constexpr (G == 1) {
-                        const float2 w2 = *reinterpret_cast<const float2 *>(pt);
-#pragma unroll
-                        for (int e = 0; e < C::VE; e += 2)
-                            fma2(acc[0][e], acc[0][e + 1], w2.x, w2.y, v[e], v[e + 1]);
-                    } else {
-#pragma unroll
-                        for (int g = 0; g < G; g += 2) {
-                            const float4 w4 = *reinterpret_cast<const float4 *>(pt + 2 * g);
-#pragma unroll
-                            for (int e = 0; e < C::VE; e += 2) {
-                                fma2(acc[g][e], acc[g][e + 1], w4.x, w4.y, v[e], v[e + 1]);
-                                fma2(acc[g + 1][e], acc[g + 1][e + 1], w4.z, w4.w, v[e], v[e + 1]);
-                            }
+                    // The running maximum only needs to move when some score
+                    // exceeds it (softmax is shift invariant, so any running value
+                    // that is one of the scores seen is exact); most tiles skip
+                    // the per-head maximum and the rescale.
+                    const bool moved = __any_sync(FULL_MASK, above);
+                    float corr[C::NF];
+                    if (moved) {
+    #pragma unroll
+                        for (int r = 0; r < C::NF; ++r) {
+                            float mx = s[r];
+    #pragma unroll
+                            for (int mask = 2; mask < 32; mask <<= 1)
+                                mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, mask));
+                            const float mnew = fmaxf(m_run[r], mx);   // finite: a valid token
+                            corr[r] = exp2_approx(m_run[r] - mnew);
+                            l_run[r] *= corr[r];
+                            m_run[r] = mnew;
                         }
                     }
-                };
-                if (nvalid == TILE) {
-#pragma unroll
-                    for (int tt = 0; tt < TILE; ++tt)
-                        pv_token(tt);
-                } else {
-#pragma unroll
-                    for (int tt = 0; tt < TILE; ++tt)
-                        if (tt < nvalid)
-                            pv_token(tt);
-                }
-                if constexpr (!VREG) {
+                    float pr[C::NF];
+    #pragma unroll
+                    for (int r = 0; r < C::NF; ++r) {
+                        pr[r] = exp2_approx(s[r] - m_run[r]);
+                        l_run[r] += pr[r];
+                    }
+                    // Publish {p, p} pairs (p times the V scale for int8) and, when
+                    // the maximum moved, the rescale factors.
+                    if (G >= 2 || (ds & 1) == 0) {
+                        const float vsc = vs_t;
+                        float2 *pp = reinterpret_cast<float2 *>(ps + t * 2 * G) + g0;
+    #pragma unroll
+                        for (int r = 0; r < C::NF; ++r) {
+                            const float v = pr[r] * vsc;
+                            pp[r] = make_float2(v, v);
+                        }
+                        if (moved && tq == 0 && (ds >> 1) == 0) {
+    #pragma unroll
+                            for (int r = 0; r < C::NF; ++r)
+                                ps[TILE * 2 * G + g0 + r] = corr[r];
+                        }
+                    }
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&empty[st]);
-                }
-                st += W;
-                while (st >= p.nst) {
-                    st -= p.nst;
-                    ++rnd;
+
+                    // ---- weighted V
+                    if (moved) {
+    #pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const float cg = ps[TILE * 2 * G + g];
+    #pragma unroll
+                            for (int e = 0; e < C::VE; ++e)
+                                acc[g][e] *= cg;
+                        }
+                    }
+                    auto pv_token = [&](int tt) {
+                        float v[C::VE];
+                        if constexpr (VREG)
+                            unpack_v<D, KV>(v, vr[tt]);
+                        else
+                            load_v<D, KV>(v, sV, tt, lane);
+                        const float *pt = ps + tt * 2 * G;
+                        if constexpr (G == 1) {
+                            const float2 w2 = *reinterpret_cast<const float2 *>(pt);
+    #pragma unroll
+                            for (int e = 0; e < C::VE; e += 2)
+                                fma2(acc[0][e], acc[0][e + 1], w2.x, w2.y, v[e], v[e + 1]);
+                        } else {
+    #pragma unroll
+                            for (int g = 0; g < G; g += 2) {
+                                const float4 w4 = *reinterpret_cast<const float4 *>(pt + 2 * g);
+    #pragma unroll
+                                for (int e = 0; e < C::VE; e += 2) {
+                                    fma2(acc[g][e], acc[g][e + 1], w4.x, w4.y, v[e], v[e + 1]);
+                                    fma2(acc[g + 1][e], acc[g + 1][e + 1], w4.z, w4.w, v[e], v[e + 1]);
+                                }
+                            }
+                        }
+                    };
+                    if (nvalid == TILE) {
+    #pragma unroll
+                        for (int tt = 0; tt < TILE; ++tt)
+                            pv_token(tt);
+                    } else {
+    #pragma unroll
+                        for (int tt = 0; tt < TILE; ++tt)
+                            if (tt < nvalid)
+                                pv_token(tt);
+                    }
+                    if constexpr (!VREG) {
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&empty[st]);
+                    }
                 }
             }
 
             // ---- merge the W warp states of this piece
+            if constexpr (C::MMA) {
+                // lane (gid, tig) holds heads 2tig, 2tig+1 x elements
+                // [gid D/8, (gid+1) D/8); l sums over the lane's tokens
+                const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
-            for (int r = 0; r < C::NF; ++r)
+                for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int mask = 2; mask < 32; mask <<= 1)
-                    l_run[r] += __shfl_xor_sync(FULL_MASK, l_run[r], mask);
+                    for (int mask = 4; mask < 32; mask <<= 1)
+                        mst.l[r] += __shfl_xor_sync(FULL_MASK, mst.l[r], mask);
 #pragma unroll
-            for (int g = 0; g < G; ++g)
+                for (int r = 0; r < 2; ++r) {
+                    const int h = 2 * tig + r;
+                    if (h < G) {
 #pragma unroll
-                for (int e = 0; e < C::VE; ++e)
-                    mw[g * D + lane * C::VE + e] = acc[g][e];
-            if (tq == 0 && (ds >> 1) == 0 && (G >= 2 || ds == 0)) {
-                const int g0 = G >= 2 ? (G / 2) * (ds & 1) : 0;
-#pragma unroll
-                for (int r = 0; r < C::NF; ++r) {
-                    mw[G * D + g0 + r] = m_run[r];
-                    mw[G * D + G + g0 + r] = l_run[r];
+                        for (int j = 0; j < D / 16; ++j)
+                            *reinterpret_cast<float2 *>(mw + h * D + gid * (D / 8) + 2 * j) =
+                                make_float2(mst.acc[j][r], mst.acc[j][r + 2]);
+                        if (gid == 0) {
+                            mw[G * D + h] = mst.m[r];
+                            mw[G * D + G + h] = mst.l[r];
+                        }
+                    }
+                }
+            } else {
+    #pragma unroll
+                for (int r = 0; r < C::NF; ++r)
+    #pragma unroll
+                    for (int mask = 2; mask < 32; mask <<= 1)
+                        l_run[r] += __shfl_xor_sync(FULL_MASK, l_run[r], mask);
+    #pragma unroll
+                for (int g = 0; g < G; ++g)
+    #pragma unroll
+                    for (int e = 0; e < C::VE; ++e)
+                        mw[g * D + lane * C::VE + e] = acc[g][e];
+                if (tq == 0 && (ds >> 1) == 0 && (G >= 2 || ds == 0)) {
+                    const int g0 = G >= 2 ? (G / 2) * (ds & 1) : 0;
+    #pragma unroll
+                    for (int r = 0; r < C::NF; ++r) {
+                        mw[G * D + g0 + r] = m_run[r];
+                        mw[G * D + G + g0 + r] = l_run[r];
+                    }
                 }
             }
             named_bar_sync(1, W * 32);
@@ -1189,7 +1643,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
 
 // ---- host side ---------------------------------------------------------------
 
-template <int D, int G, int KV>
+template <int D, int G, int KV, bool QS>
 int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_len,
              cudaStream_t stream)
 {
@@ -1208,7 +1662,7 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
     // The dynamic shared-memory limit is an attribute of the kernel in the
     // current device's context (a context that a device reset replaces), so
     // it is set on every call rather than remembered by the process.
-    if (cudaFuncSetAttribute(paged_decode_kernel<D, G, KV>,
+    if (cudaFuncSetAttribute(paged_decode_kernel<D, G, KV, QS>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) != cudaSuccess)
         return PKV_ERR_CUDA;
     const int64_t max_tiles =
@@ -1218,10 +1672,24 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
         P = max_tiles;
     if (P < 1)
         P = 1;
-    if (launch_pdl(paged_decode_kernel<D, G, KV>, dim3((unsigned)P), dim3(C::NTHREADS),
+    if (launch_pdl(paged_decode_kernel<D, G, KV, QS>, dim3((unsigned)P), dim3(C::NTHREADS),
                    (size_t)lay.total, stream, prm) != cudaSuccess)
         return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// The tensor-core tile math multiplies q in the cache's MMA type (bf16 for
+// bf16 caches, else fp16); a q of another type goes in as two parts.
+template <int D, int G, int KV>
+int launch_q(const pkv_pool *pool, const Params &prm, int batch, int max_seq_len,
+             cudaStream_t s)
+{
+    if constexpr (mma_path(KV, G)) {
+        const int mma_type = MmaBf16<KV>::v ? PKV_BF16 : PKV_F16;
+        if (prm.q_dtype != mma_type)
+            return launch_t<D, G, KV, true>(pool, prm, batch, max_seq_len, s);
+    }
+    return launch_t<D, G, KV, false>(pool, prm, batch, max_seq_len, s);
 }
 
 template <int D, int KV>
@@ -1229,10 +1697,10 @@ int launch_g(const pkv_pool *pool, int G, const Params &prm, int batch, int max_
              cudaStream_t s)
 {
     switch (G) {
-    case 1: return launch_t<D, 1, KV>(pool, prm, batch, max_seq_len, s);
-    case 2: return launch_t<D, 2, KV>(pool, prm, batch, max_seq_len, s);
-    case 4: return launch_t<D, 4, KV>(pool, prm, batch, max_seq_len, s);
-    case 8: return launch_t<D, 8, KV>(pool, prm, batch, max_seq_len, s);
+    case 1: return launch_q<D, 1, KV>(pool, prm, batch, max_seq_len, s);
+    case 2: return launch_q<D, 2, KV>(pool, prm, batch, max_seq_len, s);
+    case 4: return launch_q<D, 4, KV>(pool, prm, batch, max_seq_len, s);
+    case 8: return launch_q<D, 8, KV>(pool, prm, batch, max_seq_len, s);
     }
     return PKV_ERR_UNSUPPORTED;
 }

@@ -2,6 +2,7 @@
 // copies into shared memory, bounded waits, and 16-bit / 8-bit unpacking.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -189,6 +190,30 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32
         "%2, [%3], %4;" ::"r"(smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
+}
+
+// Asynchronous 16-byte (L2 only) and 8-byte copies global -> shared
+// (cp.async): addresses aligned to the size.  Their completion reaches an
+// mbarrier through cp_async_mbar_arrive.
+__device__ __forceinline__ void cp_async_16b(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_8b(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
+// One arrival on the mbarrier once every cp.async this thread issued before
+// has landed.  The arrival is not added to the barrier's pending count: the
+// barrier's expected arrival count must include it.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first()

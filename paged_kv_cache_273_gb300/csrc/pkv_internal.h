@@ -2,6 +2,9 @@
 // libpkv.  Not part of the public ABI (that is include/pkv.h).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstddef>
 #include <cstdint>
 #include <vector>
@@ -72,6 +75,10 @@ int launch_append(const pkv_pool *pool, const void *k_new, const void *v_new, pk
                   void *k_scales, void *v_scales, pkv_stream_t stream);
 
 size_t decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads);
+
+// The driver's tensor-map encoder (cuTensorMapEncodeTiled), looked up once
+// through the runtime; null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
                   const void *k_cache, const void *v_cache, const void *k_scales,

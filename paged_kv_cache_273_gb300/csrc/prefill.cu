@@ -794,21 +794,6 @@ int launch_prefill_t(const pkv_pool *pool, const PrefillParams &prm, int max_q_l
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-// The driver's tensor-map encoder, looked up once through the runtime.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }();
-    return fn;
-}
-
 // A cache [num_blocks][num_kv_heads][block_size][D] of 16-bit elements as the
 // 3-D tensor {D, block_size, num_blocks * num_kv_heads}, boxes of 64 x rows x 1.
 bool encode_cache_map(CUtensorMap *m, const pkv_pool *pool, const void *base, int rows)
