@@ -36,6 +36,18 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// A packed pair of the 16-bit type -> two floats (exact).
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t w)
+{
+    if constexpr (MmaType<T>::bf16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        const __half2 h = *reinterpret_cast<const __half2 *>(&w);
+        return __half22float2(h);
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
@@ -84,11 +96,13 @@ struct PrefillParams {
 //    of 4 rows and for the block where the sequence ends;
 //  * one thread issues the tcgen05.mma: S = Q K^T (M 128, N 128, K = D, both
 //    operands in shared memory) and O += P V (M 128, N = D, K 128, P read
-//    from tensor memory) per half, fp32 accumulators in tensor memory (half
-//    h: S in columns [256 h, 256 h + 128), O in the next D);
+//    from tensor memory, as a high and a low part: two MMAs per K step)
+//    per half, fp32 accumulators in tensor memory (half h: S in columns
+//    [256 h, 256 h + 128), O in the next D);
 //  * one warpgroup per half, one thread per query row, reads its S row with
-//    tcgen05.ld, does the online softmax, writes P as fp16/bf16 pairs over
-//    the S columns it has read, rescales its O row in tensor memory when the
+//    tcgen05.ld, does the online softmax, writes P as high and low
+//    fp16/bf16 parts (p = hi + lo to ~2^-16) over the S columns it has
+//    read, rescales its O row in tensor memory when the
 //    row maximum moved by more than 2^8, and at the end of an item writes
 //    O / l out through shared-memory staging.
 // The issue order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) lets one half's
@@ -465,7 +479,8 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
                     }
                 }
                 // pass 2: weights, their sum, and P (keys 32c..32c+31 as
-                // 16-bit pairs in columns 16c..16c+15, over S columns already
+                // 16-bit pairs, high parts in columns 32c..32c+15, low parts
+                // in 32c+16..32c+31: the S columns of this chunk, already
                 // read)
                 float sum = 0.0f;
 #pragma unroll 1
@@ -484,11 +499,20 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         v[j] = ex2_approx(v[j]);
-                    uint32_t w[16];
+                    // P in two parts of the 16-bit type, hi + lo = p to
+                    // ~2^-16 relative (rounded once, p alone would carry up
+                    // to 2^-9 (bf16) or 2^-12 (fp16) of error into P.V)
+                    uint32_t w[16], wl[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
+                    for (int j = 0; j < 16; ++j) {
                         w[j] = pack2<T>(v[2 * j], v[2 * j + 1]);
-                    tmem_st16(t_s + c0 / 2, w);
+                        const float2 h = unpack2<T>(w[j]);
+                        float r0 = v[2 * j], r1 = v[2 * j + 1];
+                        add2(r0, r1, -h.x, -h.y);
+                        wl[j] = pack2<T>(r0, r1);
+                    }
+                    tmem_st16(t_s + c0, w);
+                    tmem_st16(t_s + c0 + 16, wl);
 #pragma unroll
                     for (int k = 16; k > 1; k >>= 1)       // tree sum over pairs
 #pragma unroll
@@ -702,18 +726,24 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
                 if (--s_left == 0)
                     umma_commit(q_empty);
             };
-            // O_hh += P_hh V.  P: in tensor memory over the S columns, 16
-            // keys (a K step) per 8 columns.  V is the MN-major B in 128-byte
+            // O_hh += P_hh V.  P: in tensor memory over the S columns, keys
+            // 32c..32c+31 as 16-bit pairs: the high parts in columns 32c..
+            // 32c+15, the low parts in the next 16; a K step (16 keys) reads
+            // 8 columns of each, both MMAs accumulating into O_hh.  V is the
+            // MN-major B in 128-byte
             // swizzled panels: a key row of 64 d every 128 B, 8-key groups
             // 1024 B apart, the next 64 d a panel (TBK*128 B) on; a step of
             // 16 keys is 2048 B.
             auto issue_pv = [&](int hh, int g, int kt) {
                 const uint32_t vb = sVa + (g % NSLOT) * C::KV_BYTES;
 #pragma unroll
-                for (int ks = 0; ks < TBK / 16; ++ks)
-                    umma_f16_ta(tmem + hh * C::HALF_COLS + TBK, tmem + hh * C::HALF_COLS + ks * 8,
-                                umma_desc_sw128(vb + ks * 2048, TBK * 128, 1024), idesc_o,
+                for (int ks = 0; ks < TBK / 16; ++ks) {
+                    const uint32_t pa = tmem + hh * C::HALF_COLS + 32 * (ks >> 1) + 8 * (ks & 1);
+                    const uint64_t vd = umma_desc_sw128(vb + ks * 2048, TBK * 128, 1024);
+                    umma_f16_ta(tmem + hh * C::HALF_COLS + TBK, pa, vd, idesc_o,
                                 (kt > 0 || ks > 0) ? 1u : 0u);
+                    umma_f16_ta(tmem + hh * C::HALF_COLS + TBK, pa + 16, vd, idesc_o, 1u);
+                }
                 if (hh == last_half)
                     umma_commit(&v_empty[g % NSLOT]);
             };

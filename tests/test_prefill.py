@@ -103,13 +103,13 @@ def test_chunked_prefill_equals_prefill_at_once():
 
 
 # ------------------------------------------------------------------ GPU parity
-# Tolerance, from the arithmetic: scores are exact products summed in fp32;
-# the weights p are rounded to the input type for the P.V product, a relative
-# error of at most 2^-11 (fp16) or 2^-8 (bf16) per weight against an fp32
-# denominator, so the output can move by that fraction of max |v| (about 4
-# for N(0,1) values): ~2e-3 for fp16, ~1.6e-2 worst case for bf16, in
-# practice far less since the rounding errors do not line up.
-PREFILL_TOL = {"f16": 2e-3, "bf16": 1e-2}
+# Tolerance: 2e-3 max-abs for fp16/bf16 K/V with fp32 accumulation, as for
+# decode.  From the arithmetic: scores are exact products summed in fp32; the
+# weights p enter P.V as a high and a low part of the input type (p = hi + lo
+# up to the rounding of lo, ~2^-16 relative for bf16, ~2^-22 for fp16), so the
+# error left is fp32 accumulation and the exp2 approximation (~2^-22 relative),
+# orders of magnitude inside the bound whatever the score pattern.
+PREFILL_TOL = {"f16": 2e-3, "bf16": 2e-3}
 
 
 def _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached, seed, k_growth=0.0, with_vmax=False):
@@ -299,8 +299,8 @@ def test_gpu_prefill_rising_scores(dt):
         dt, 128, 8, 2, 16, [600, 130], [100, 0], 81, k_growth=1.0 / 32, with_vmax=True)
     assert same_cache and intact
     assert status == pkv.PKV_OK
-    # With one or two keys carrying nearly all the weight the rounding errors
-    # of P do not average out: the bound is the worst case, half an ulp of
-    # the weight type (2^-8 bf16, 2^-11 fp16) times max |v|, plus fp32 slack.
-    tol = (2.0 ** -8 if dt == "bf16" else 2.0 ** -11) * vmax + 1e-4
-    assert err <= tol, (err, tol)
+    # With one or two keys carrying nearly all the weight rounding errors of
+    # P would not average out; with P in two parts the weights' error is
+    # ~2^-16 of max |v| at worst, inside the same bound as everywhere.
+    assert vmax > 0
+    assert err <= PREFILL_TOL[dt], (err, vmax)
