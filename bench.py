@@ -401,6 +401,31 @@ def time_workload(name: str, dev, stream, peak: float, reps: int = 20) -> dict:
                          "frac": ub / (us / 1e6) / 1e9 / peak, "bytes_per_launch": ub,
                          "note": "every cached row counted once (the shared prefix blocks "
                                  "once for all sequences that share them)"}
+        # the same call with the shared prefix scored once per group
+        g = pkv.kv_prefix_groups(d["inp"].block_tables, d["lens_h"], wl.block_size)
+        gd = pkv.prefix_groups_to_device(g, dev)
+        cws = pkv.alloc_cascade_workspace(d["pool"], wl.batch, wl.num_q_heads,
+                                          g["max_prefix_len"], dev)
+
+        def ccall(i=0):
+            pkv.paged_decode_attention_cascade(d["pool"], d["q"], d["kc"], d["vc"], d["tables"],
+                                               d["lens"], 1.0 / np.sqrt(wl.head_dim), d["out"],
+                                               cws, d["max_len"], gd, stream=stream)
+
+        for _ in range(3):
+            ccall()
+        cms = statistics.median(timed_loop(stream, ccall, reps, host_queue_us(ccall, 5)))
+        if pkv.pkv_check_error(d["pool"]) != pkv.PKV_OK:
+            raise RuntimeError("device error timing the cascade on %s" % name)
+        cus = cms / reps * 1e3
+        res["cascade"] = {
+            "value": ub / (cus / 1e6) / 1e9, "unit": "GB/s", "frac": ub / (cus / 1e6) / 1e9 / peak,
+            "launch_us": cus, "bytes_per_launch": ub, "logical_value": nbytes / (cus / 1e6) / 1e9,
+            "groups": g["num_groups"], "max_group_size": g["max_group_size"],
+            "prefix_tokens": g["max_prefix_len"],
+            "note": "paged_decode_attention_cascade (prefix pass on tcgen05 + decode over each "
+                    "sequence's own rows), unique bytes; %d calls back to back, median of 3; "
+                    "logical_value counts shared rows once per sequence" % reps}
     del d
     return res
 
@@ -815,6 +840,22 @@ def run_profile(name: str) -> int:
     if name == "prefill":
         time_prefill(dev, stream, 1900.0, reps=1)
         return 0
+    if name == "llama2_70b_cascade":
+        d = build_device_workload("llama2_70b", dev)
+        wl = d["wl"]
+        g = pkv.kv_prefix_groups(d["inp"].block_tables, d["lens_h"], wl.block_size)
+        gd = pkv.prefix_groups_to_device(g, dev)
+        cws = pkv.alloc_cascade_workspace(d["pool"], wl.batch, wl.num_q_heads,
+                                          g["max_prefix_len"], dev)
+        for _ in range(4):
+            pkv.paged_decode_attention_cascade(d["pool"], d["q"], d["kc"], d["vc"], d["tables"],
+                                               d["lens"], 1.0 / np.sqrt(wl.head_dim), d["out"],
+                                               cws, d["max_len"], gd, stream=stream)
+        torch.cuda.synchronize()
+        if pkv.pkv_check_error(d["pool"]) != pkv.PKV_OK:
+            raise RuntimeError("device error profiling the cascade")
+        print("profiled the cascade on llama2_70b: 4 calls")
+        return 0
     d = build_device_workload(name, dev)
     wl = d["wl"]
     for _ in range(4):
@@ -835,7 +876,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--profile", default=None,
-                    choices=["gpt2", "llama3_8b", "llama2_70b", "int8", "int4", "prefill"])
+                    choices=["gpt2", "llama3_8b", "llama2_70b", "int8", "int4", "prefill",
+                             "llama2_70b_cascade"])
     args = ap.parse_args()
     if args.profile:
         return run_profile(args.profile)

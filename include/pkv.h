@@ -300,6 +300,80 @@ int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtyp
                            pkv_stream_t stream);
 
 /*
+ * kv_prefix_groups — host: find the groups of sequences that share a prefix
+ * of physical blocks ([VIS] "PagedAttention: the cache in blocks": sequences
+ * that begin with the same prompt tokens can reference one stored copy of
+ * those tokens' blocks).  Sequences with at least min_prefix_blocks * block
+ * _size rows are grouped by their first table entry; a group of two or more
+ * shares its members' longest common run of leading table entries, capped
+ * at the shortest member's length: group_prefix[g] tokens (P).  block_tables
+ * [B][max_blocks_per_seq] and seq_lens [B] are host arrays.  Outputs (host,
+ * caller-allocated, batch entries each, group_start batch + 1):
+ * group_start[g]..group_start[g+1] index group g's members in group_seqs
+ * (ascending sequence order; the first member's table is the one read for
+ * the prefix), group_prefix[g] = P, seq_prefix[b] = P of b's group or 0,
+ * and *num_groups, *max_group_size, *max_prefix_len.  PKV_ERR_INVALID for a
+ * null pointer, batch < 0, block_size < 1, min_prefix_blocks < 1 or a length
+ * outside its table row.
+ */
+int kv_prefix_groups(const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                     int batch, int block_size, int min_prefix_blocks, int32_t *group_start,
+                     int32_t *group_seqs, int32_t *group_prefix, int32_t *seq_prefix,
+                     int *num_groups, int *max_group_size, int *max_prefix_len);
+
+/*
+ * paged_decode_cascade_workspace_bytes — bytes of the workspace of
+ * paged_decode_attention_cascade: the decode workspace, then the prefix
+ * partials for prefixes of up to max_prefix_len tokens (fp32, [chunks][batch]
+ * [num_q_heads][head_dim + 4], at most 16 chunks of 128-key tiles; a merge
+ * step leaves the merged prefix of every row in chunk 0).  0 on bad
+ * arguments.
+ */
+size_t paged_decode_cascade_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads,
+                                            int max_prefix_len);
+
+/*
+ * paged_decode_attention_cascade — paged_decode_attention for a batch in
+ * which groups of sequences share the leading blocks of their tables ([VIS]
+ * "PagedAttention: the cache in blocks"; groups as kv_prefix_groups finds
+ * them).  The result is the same softmax of [NOTES] "Concept" over each
+ * sequence's rows; only the work is arranged differently:
+ *  1. a prefix pass (tensor cores, tcgen05) scores group g's P shared rows
+ *     once for all q heads of all its members (members x G query rows per
+ *     KV head), in key chunks, and leaves per (sequence, q head, chunk) the
+ *     unnormalised weighted sum of V, the running maximum and the sum;
+ *  2. a merge step combines each row's chunks (all SMs, one thread per row
+ *     and 4 columns);
+ *  3. the decode pass attends each sequence over its own rows [P, L) only
+ *     and folds the merged prefix into its output (a sequence with P = L
+ *     gets the prefix alone).
+ * Arguments as paged_decode_attention, without scales (fp16 / bf16 caches
+ * only; q of the cache's type, else PKV_ERR_INVALID; other caches
+ * PKV_ERR_UNSUPPORTED), plus the device arrays group_start [num_groups + 1],
+ * group_seqs, group_prefix [num_groups] and seq_prefix [batch] (seq_prefix[b]
+ * = P of b's group or 0, consistent with the groups: a sequence with
+ * seq_prefix[b] > 0 must be a member of a group with that prefix), their
+ * maxima max_group_size and max_prefix_len (<= max_seq_len), and a
+ * workspace of paged_decode_cascade_workspace_bytes(pool, batch,
+ * num_q_heads, max_prefix_len), zeroed once by the caller like
+ * paged_decode_attention's.  Every member's table must hold the same block
+ * ids for the prefix's blocks and every member's length must be >= P; the
+ * result is undefined otherwise.  seq_prefix[b] < 0 or > seq_lens[b] is
+ * recorded in the pool's error word (pkv_check_error then returns
+ * PKV_ERR_BAD_INDEX) and the sequence is attended in full.  Three kernels are
+ * launched on `stream` (one when no group is given).
+ */
+int paged_decode_attention_cascade(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
+                                   int num_q_heads, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *seq_lens, int batch, int max_seq_len,
+                                   const int32_t *group_start, const int32_t *group_seqs,
+                                   const int32_t *group_prefix, const int32_t *seq_prefix,
+                                   int num_groups, int max_group_size, int max_prefix_len,
+                                   float scale, float *out, void *workspace,
+                                   size_t workspace_bytes, pkv_stream_t stream);
+
+/*
  * paged_decode_attention_window — paged_decode_attention restricted to a
  * sliding window: sequence b attends over its last min(window,
  * seq_lens[b]) cached rows only, positions [seq_lens[b] - window,

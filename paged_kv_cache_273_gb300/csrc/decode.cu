@@ -56,7 +56,8 @@ int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int nu
                   const void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
                   const int32_t *seq_lens, int batch, int max_seq_len, int window, float scale,
                   float *out,
-                  void *workspace, size_t workspace_bytes, pkv_stream_t stream)
+                  void *workspace, size_t workspace_bytes, pkv_stream_t stream,
+                  const int32_t *seq_prefix, const float *prefix_part)
 {
     (void)workspace_bytes;
     const int Hkv = pool->num_kv_heads;
@@ -91,6 +92,8 @@ int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int nu
     const int64_t table_cap = (int64_t)max_blocks_per_seq * pool->block_size;
     prm.len_cap = (int)std::min<int64_t>(max_seq_len, table_cap);
     prm.window = window > 0 ? window : 0;
+    prm.seq_prefix = seq_prefix;
+    prm.prefix_part = prefix_part;
     prm.num_blocks = pool->num_blocks;
     prm.q_dtype = q_dtype;
     prm.q_bytes = dtype_bytes(q_dtype);

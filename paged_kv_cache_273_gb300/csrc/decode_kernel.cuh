@@ -143,6 +143,11 @@ struct Params {
     int max_seq_len;
     int len_cap;        // min(max_seq_len, max_blocks_per_seq * block_size)
     int window;         // > 0: attend over the last `window` rows only
+    // Shared-prefix (cascade) decode: sequence b attends here only over rows
+    // [seq_prefix[b], L) and folds in the partial a prefix pass left for its
+    // heads over rows [0, seq_prefix[b]) (null: no prefix)
+    const int32_t *seq_prefix;
+    const float *prefix_part;   // [batch][num_q_heads][D + 4]: O; maximum, sum at D + 2, D + 3
     int num_blocks;
     int q_dtype;
     int q_bytes;
@@ -938,12 +943,24 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             L = 0;
         }
         s_len[b] = L;
-        s_lo[b] = (p.window > 0 && L > p.window) ? L - p.window : 0;
+        int lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
+        if (p.seq_prefix) {
+            // the rows after the shared prefix (none if the prefix is all)
+            lo = __ldg(p.seq_prefix + b);
+            if (lo < 0 || lo > L) {
+                if (blockIdx.x == 0)
+                    atomicOr(p.err, PKV_EBIT_SEQLEN);
+                lo = 0;
+            }
+        }
+        s_lo[b] = lo;
     }
     __syncthreads();
     // Tiles of sequence b: from the one holding its first attended row to the
-    // one holding its last.
-    auto seq_tiles = [&](int b) { return (s_len[b] + TILE - 1) / TILE - s_lo[b] / TILE; };
+    // one holding its last (none when no row is left to attend).
+    auto seq_tiles = [&](int b) {
+        return s_len[b] > s_lo[b] ? (s_len[b] + TILE - 1) / TILE - s_lo[b] / TILE : 0;
+    };
     // Exclusive prefix over the sequences of value(b), written to out[0..B];
     // thread t takes a contiguous run of sequences, then warp and block scans.
     auto block_scan = [&](auto value, int *out) {
@@ -1186,11 +1203,29 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         float *ps = psbuf + w * C::PSW;
         float *mw = merge + w * G * (D + 2);
 
-        // Zero rows of empty sequences; sequence b is CTA (b % grid)'s job.
+        // Fold the shared-prefix partial of (sequence b, query head h,
+        // element d) into (m, num, den) (the prefix pass merged its chunks).
+        auto fold_prefix = [&](int b, int h, int d, float &m, float &num, float &den) {
+            if (p.seq_prefix == nullptr || s_lo[b] == 0)
+                return;
+            const float *row = p.prefix_part + ((int64_t)b * Hq + h) * (D + 4);
+            const float mp = __ldcg(row + D + 2), lp = __ldcg(row + D + 3), op = __ldcg(row + d);
+            const float mn = fmaxf(m, mp);
+            const float fo = exp2_approx(m - mn), fp = exp2_approx(mp - mn);
+            num = fmaf(num, fo, op * fp);
+            den = fmaf(den, fo, lp * fp);
+            m = mn;
+        };
+        // Rows of sequences with no tile here: zeros for empty sequences, the
+        // prefix alone for a sequence whose rows are all shared; sequence b
+        // is CTA (b % grid)'s job.
         for (int b = cta; b < B; b += gridDim.x) {
-            if (s_len[b] == 0)
-                for (int idx = ctid; idx < Hq * D; idx += W * 32)
-                    p.out[(int64_t)b * Hq * D + idx] = 0.0f;
+            if (seq_tiles(b) == 0)
+                for (int idx = ctid; idx < Hq * D; idx += W * 32) {
+                    float m = -INFINITY, num = 0.0f, den = 0.0f;
+                    fold_prefix(b, idx / D, idx % D, m, num, den);
+                    p.out[(int64_t)b * Hq * D + idx] = den > 0.0f ? num / den : 0.0f;
+                }
         }
 
         const int stride = G * (D + 2);   // floats of one partial
@@ -1236,6 +1271,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             for (int idx = ctid; idx < G * D; idx += W * 32) {
                 float m, num, den;
                 fold_partials(seg, sp.c_first, sp.c_last, -1, 0.0f, 0.0f, 0.0f, idx, m, num, den);
+                fold_prefix(bq, kq * G + idx / D, idx % D, m, num, den);
                 p.out[((int64_t)bq * Hq + kq * G) * D + idx] = num / den;
             }
             if (ctid == 0)
@@ -1559,8 +1595,11 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
 #pragma unroll
                 for (int j = 0; j < MO; ++j) {
                     const int idx = ctid + j * W * 32;
-                    if (idx < G * D)
-                        orow[idx] = o_num[j] / o_den[j];
+                    if (idx < G * D) {
+                        float m = o_m[j], num = o_num[j], den = o_den[j];
+                        fold_prefix(b, kvh * G + idx / D, idx % D, m, num, den);
+                        orow[idx] = num / den;
+                    }
                 }
                 named_bar_sync(1, W * 32);   // the merge buffer is free again
             } else {
@@ -1583,6 +1622,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                             float m, num, den;
                             fold_partials(seg, c_first, c_last, cta, o_m[j], o_num[j], o_den[j],
                                           idx, m, num, den);
+                            fold_prefix(b, kvh * G + idx / D, idx % D, m, num, den);
                             orow[idx] = num / den;
                         }
                     }

@@ -76,15 +76,58 @@ int launch_append(const pkv_pool *pool, const void *k_new, const void *v_new, pk
 
 size_t decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads);
 
+// Shared-prefix (cascade) decode: the prefix pass splits a prefix of up to
+// max_prefix_len tokens into at most 16 chunks of *kc_tiles 128-key tiles
+// (*nkc chunks when the prefix is that long).
+inline void prefix_chunks(int max_prefix_len, int *kc_tiles, int *nkc)
+{
+    const int tiles = (max_prefix_len + 127) / 128;
+    int kc = (tiles + 15) / 16;
+    if (kc < 1)
+        kc = 1;
+    *kc_tiles = kc;
+    *nkc = tiles > 0 ? (tiles + kc - 1) / kc : 1;
+}
+
+// Floats of one prefix partial row: O[D], running maximum, sum, 2 pad (16-byte rows).
+inline int prefix_row_floats(int head_dim) { return head_dim + 4; }
+
+// Bytes of the prefix partials [nkc][batch][num_q_heads][D + 4] fp32 (chunk 0
+// ends up holding the merged prefix of every row).
+inline size_t prefix_partials_bytes(const pkv_pool *pool, int batch, int num_q_heads,
+                                    int max_prefix_len)
+{
+    int kc = 1, nkc = 1;
+    prefix_chunks(max_prefix_len, &kc, &nkc);
+    return (size_t)nkc * batch * num_q_heads * prefix_row_floats(pool->head_dim) * sizeof(float);
+}
+
+
+// The prefix pass (tcgen05, the prefill kernel's machinery): partials of
+// every group member's q heads over its group's shared prefix.
+int launch_prefix_pass(const pkv_pool *pool, const void *q, int num_q_heads, const void *k_cache,
+                       const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *seq_lens, int batch, const int32_t *grp_start,
+                       const int32_t *grp_seqs, const int32_t *grp_len, int ngroups,
+                       int max_group_size, int max_prefix_len, float scale, float *part,
+                       int *kc_tiles, pkv_stream_t stream);
+
+// Merge the prefix pass's chunk partials of every row of a sequence with a
+// prefix into chunk 0 (O; maximum and sum at D + 2, D + 3).
+int launch_prefix_merge(const pkv_pool *pool, const int32_t *seq_prefix, float *part, int batch,
+                        int num_q_heads, int kc_tiles, pkv_stream_t stream);
+
 // The driver's tensor-map encoder (cuTensorMapEncodeTiled), looked up once
 // through the runtime; null if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// seq_prefix / prefix_part: shared-prefix decode (null: none), see Params.
 int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
                   const void *k_cache, const void *v_cache, const void *k_scales,
                   const void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
                   const int32_t *seq_lens, int batch, int max_seq_len, int window, float scale,
                   float *out,
-                  void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+                  void *workspace, size_t workspace_bytes, pkv_stream_t stream,
+                  const int32_t *seq_prefix = nullptr, const float *prefix_part = nullptr);
 
 }  // namespace pkv

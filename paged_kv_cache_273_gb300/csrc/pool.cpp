@@ -445,6 +445,155 @@ int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype
                        scale, out, workspace, workspace_bytes, stream);
 }
 
+int kv_prefix_groups(const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                     int batch, int block_size, int min_prefix_blocks, int32_t *group_start,
+                     int32_t *group_seqs, int32_t *group_prefix, int32_t *seq_prefix,
+                     int *num_groups, int *max_group_size, int *max_prefix_len)
+{
+    if (batch < 0 || max_blocks_per_seq < 0 || block_size < 1 || min_prefix_blocks < 1 ||
+        !num_groups || !max_group_size || !max_prefix_len)
+        return PKV_ERR_INVALID;
+    if (batch > 0 && (!block_tables || !seq_lens || !group_start || !group_seqs ||
+                      !group_prefix || !seq_prefix))
+        return PKV_ERR_INVALID;
+    *num_groups = 0;
+    *max_group_size = 0;
+    *max_prefix_len = 0;
+    if (batch > 0)
+        group_start[0] = 0;
+    for (int b = 0; b < batch; ++b) {
+        seq_prefix[b] = 0;
+        if (seq_lens[b] < 0 || (int64_t)seq_lens[b] > (int64_t)max_blocks_per_seq * block_size)
+            return PKV_ERR_INVALID;
+    }
+    // Candidates: sequences with at least min_prefix_blocks whole blocks,
+    // ordered by first block id (then by index, so a group lists its
+    // members in batch order).
+    std::vector<int> cand;
+    for (int b = 0; b < batch; ++b)
+        if (seq_lens[b] >= min_prefix_blocks * block_size)
+            cand.push_back(b);
+    std::stable_sort(cand.begin(), cand.end(), [&](int a, int c) {
+        return block_tables[(int64_t)a * max_blocks_per_seq] <
+               block_tables[(int64_t)c * max_blocks_per_seq];
+    });
+    int ng = 0, used = 0;
+    for (size_t i = 0; i < cand.size();) {
+        size_t j = i + 1;
+        const int32_t first = block_tables[(int64_t)cand[i] * max_blocks_per_seq];
+        while (j < cand.size() && block_tables[(int64_t)cand[j] * max_blocks_per_seq] == first)
+            ++j;
+        if (j - i >= 2) {
+            // the table entries every member shares, within every member's rows
+            const int32_t *lead = block_tables + (int64_t)cand[i] * max_blocks_per_seq;
+            int minlen = seq_lens[cand[i]];
+            for (size_t k = i; k < j; ++k)
+                minlen = std::min(minlen, (int)seq_lens[cand[k]]);
+            int common = (minlen + block_size - 1) / block_size;
+            for (size_t k = i + 1; k < j; ++k) {
+                const int32_t *row = block_tables + (int64_t)cand[k] * max_blocks_per_seq;
+                int n = 0;
+                while (n < common && row[n] == lead[n])
+                    ++n;
+                common = n;
+            }
+            const int P = std::min(common * block_size, minlen);
+            if (common >= min_prefix_blocks && P > 0) {
+                std::vector<int> mem(cand.begin() + i, cand.begin() + j);
+                std::sort(mem.begin(), mem.end());
+                for (int m : mem) {
+                    group_seqs[used++] = m;
+                    seq_prefix[m] = P;
+                }
+                group_prefix[ng] = P;
+                group_start[ng + 1] = used;
+                *max_group_size = std::max(*max_group_size, (int)mem.size());
+                *max_prefix_len = std::max(*max_prefix_len, P);
+                ++ng;
+            }
+        }
+        i = j;
+    }
+    *num_groups = ng;
+    return PKV_OK;
+}
+
+size_t paged_decode_cascade_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads,
+                                            int max_prefix_len)
+{
+    if (!pool || batch < 0 || num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0 ||
+        max_prefix_len < 0)
+        return 0;
+    const size_t dec = pkv::decode_workspace_bytes(pool, batch, num_q_heads);
+    return (dec + 255) / 256 * 256 +
+           pkv::prefix_partials_bytes(pool, batch, num_q_heads, max_prefix_len);
+}
+
+int paged_decode_attention_cascade(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
+                                   int num_q_heads, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *seq_lens, int batch, int max_seq_len,
+                                   const int32_t *group_start, const int32_t *group_seqs,
+                                   const int32_t *group_prefix, const int32_t *seq_prefix,
+                                   int num_groups, int max_group_size, int max_prefix_len,
+                                   float scale, float *out, void *workspace,
+                                   size_t workspace_bytes, pkv_stream_t stream)
+{
+    if (!pool || batch < 0 || max_blocks_per_seq < 0 || max_seq_len < 0 || num_q_heads < 1 ||
+        num_groups < 0 || max_group_size < 0 || max_prefix_len < 0)
+        return PKV_ERR_INVALID;
+    if (num_q_heads % pool->num_kv_heads != 0)
+        return PKV_ERR_INVALID;
+    const int G = num_q_heads / pool->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return PKV_ERR_UNSUPPORTED;
+    // the prefix pass multiplies q and K on the tensor cores as they are
+    if (pool->kv_dtype != PKV_F16 && pool->kv_dtype != PKV_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    if (q_dtype != pool->kv_dtype)
+        return PKV_ERR_INVALID;
+    if (batch > 4096 || max_group_size > batch || max_prefix_len > max_seq_len)
+        return batch > 4096 ? PKV_ERR_UNSUPPORTED : PKV_ERR_INVALID;
+    if (batch == 0)
+        return PKV_OK;
+    if (num_groups > 0 && (!group_start || !group_seqs || !group_prefix))
+        return PKV_ERR_INVALID;
+    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !seq_prefix || !out ||
+        !workspace)
+        return PKV_ERR_INVALID;
+    if (!pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache) ||
+        !pkv::aligned16(out) || !pkv::aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_prefix) & 3u))
+        return PKV_ERR_INVALID;
+    if (!pool->has_device)
+        return PKV_ERR_CUDA;
+    if (workspace_bytes <
+        paged_decode_cascade_workspace_bytes(pool, batch, num_q_heads, max_prefix_len))
+        return PKV_ERR_INVALID;
+    // workspace: decode's counters and partials | the prefix partials
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    const size_t dec = (pkv::decode_workspace_bytes(pool, batch, num_q_heads) + 255) / 256 * 256;
+    float *part = reinterpret_cast<float *>(ws + dec);
+    if (num_groups > batch)
+        return PKV_ERR_INVALID;
+    if (num_groups > 0 && max_group_size > 0 && max_prefix_len > 0) {
+        int kc = 1;
+        int rc = pkv::launch_prefix_pass(pool, q, num_q_heads, k_cache, v_cache, block_tables,
+                                         max_blocks_per_seq, seq_lens, batch, group_start,
+                                         group_seqs, group_prefix, num_groups, max_group_size,
+                                         max_prefix_len, scale, part, &kc, stream);
+        if (rc == PKV_OK)
+            rc = pkv::launch_prefix_merge(pool, seq_prefix, part, batch, num_q_heads, kc, stream);
+        if (rc != PKV_OK)
+            return rc;
+    }
+    return pkv::launch_decode(pool, q, q_dtype, num_q_heads, k_cache, v_cache, nullptr, nullptr,
+                              block_tables, max_blocks_per_seq, seq_lens, batch, max_seq_len, 0,
+                              scale, out, workspace, dec, stream, seq_prefix, part);
+}
+
 int paged_prefill_attention(const pkv_pool *pool, const void *q, int num_q_heads,
                             const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, int max_blocks_per_seq,

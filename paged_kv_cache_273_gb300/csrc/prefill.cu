@@ -10,6 +10,8 @@
 // "Concept"), in FlashAttention-style tiles that never hold the whole score
 // matrix ("Flash attention: don't build the giant matrix" in the guide).
 
+#include <algorithm>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -76,7 +78,20 @@ struct PrefillParams {
     int batch, num_q_heads, num_kv_heads, block_size, bs_log2, max_blocks_per_seq, num_blocks;
     int box_rows;       // min(block_size, 128)
     int nqt;            // query tiles of 256 per sequence: ceil(max_q_len / 256)
+    int nitems;         // work items (see make_item / make_prefix_item)
     float scale_log2;
+    // Shared-prefix pass (cascade): instead of a prompt's causal queries, the
+    // rows of an item are the q heads of the sequences of one group that
+    // share a prefix (member-major: row m G + g is member m's head kvh G + g),
+    // over one chunk of the prefix's keys, with no causal mask; the result is
+    // a partial (unnormalised O, running maximum, sum) per row.
+    int cascade;
+    const int32_t *grp_start;   // [ngroups + 1]: the group's members in grp_seqs
+    const int32_t *grp_seqs;    // member sequences; the first one's table is read
+    const int32_t *grp_len;     // [ngroups]: tokens of the shared prefix
+    int ngroups, group_q;       // groups; query heads per KV head
+    int kc_tiles, nkc;          // key tiles (of 128) per chunk; chunks per group at most
+    float *part;                // [nkc][batch][num_q_heads][D + 4]
 };
 
 // ---- tcgen05: 2 x 128 queries x 128 keys per step, warp-specialised,
@@ -294,14 +309,57 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[16
 struct Item {
     int b, h, qt, q0, kvh, rows_all, first_pos, last_pos, ntiles;
     int rows_h[NQH], tiles_h[NQH];
+    int kt0;         // first key tile (a prefix chunk's offset; 0 for prefill)
+    int g, c;        // prefix pass: group and key chunk
     bool live;       // has rows and valid lengths
     bool bad_len;    // has rows but its length fields are inconsistent
 };
 
-__device__ __forceinline__ Item make_item(const PrefillParams &p, int i)
+// Prefix-pass item i: (row tile qt, group g, KV head kvh, key chunk c).  The
+// rows are the group's members' q heads of kvh; the keys, tiles [kt0, kt0 +
+// ntiles) of the prefix (every row sees every prefix key: first_pos =
+// last_pos = prefix length - 1).
+__device__ __forceinline__ Item make_prefix_item(const PrefillParams &p, int i)
 {
     constexpr int QT = NQH * TBQ;
     Item it;
+    const int per = p.ngroups * p.num_kv_heads * p.nkc;
+    it.qt = i / per;
+    int rem = i - it.qt * per;
+    it.g = rem / (p.num_kv_heads * p.nkc);
+    rem -= it.g * (p.num_kv_heads * p.nkc);
+    it.kvh = rem / p.nkc;
+    it.c = rem - it.kvh * p.nkc;
+    it.h = it.kvh * p.group_q;
+    it.q0 = __ldg(p.grp_start + it.g);
+    const int members = __ldg(p.grp_start + it.g + 1) - it.q0;
+    const int P = __ldg(p.grp_len + it.g);
+    it.b = members > 0 ? __ldg(p.grp_seqs + it.q0) : 0;
+    const int L = members > 0 ? __ldg(p.seq_lens + it.b) : 0;
+    it.kt0 = it.c * p.kc_tiles;
+    const int rows_total = members * p.group_q;
+    const bool rows = it.qt * QT < rows_total && P > 0 && it.kt0 * TBK < P;
+    it.bad_len = rows && (P > L || L > p.max_blocks_per_seq * p.block_size);
+    it.live = rows && !it.bad_len;
+    it.rows_all = it.live ? min(QT, rows_total - it.qt * QT) : 0;
+    it.first_pos = P - 1;
+    it.last_pos = P - 1;
+    it.ntiles = it.live ? min(p.kc_tiles, (P + TBK - 1) / TBK - it.kt0) : 0;
+    it.rows_h[0] = min(TBQ, it.rows_all);
+    it.rows_h[1] = max(0, it.rows_all - TBQ);
+    it.tiles_h[0] = it.rows_h[0] > 0 ? it.ntiles : 0;
+    it.tiles_h[1] = it.rows_h[1] > 0 ? it.ntiles : 0;
+    return it;
+}
+
+__device__ __forceinline__ Item make_item(const PrefillParams &p, int i)
+{
+    constexpr int QT = NQH * TBQ;
+    if (p.cascade)
+        return make_prefix_item(p, i);
+    Item it;
+    it.kt0 = 0;
+    it.g = it.c = 0;
     const int per = p.num_q_heads * p.batch;
     const int qt_rev = i / per, rem = i - qt_rev * per;
     it.qt = p.nqt - 1 - qt_rev;
@@ -364,7 +422,7 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
     grid_dependency_wait();
     grid_dependents_launch();
 
-    const int nitems = p.nqt * p.num_q_heads * p.batch;
+    const int nitems = p.nitems;
     const int tid = threadIdx.x, warp = tid >> 5;
 
     if (tid == 0) {
@@ -422,7 +480,10 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
             const int rows = it.rows_h[hh], my_tiles = it.tiles_h[hh];
             if (my_tiles == 0)
                 continue;
-            const int qpos = it.first_pos + hh * TBQ + min(r, max(rows, 1) - 1);
+            // the row's position: causal rows step along the prompt; prefix
+            // rows all stand after the whole prefix
+            const int qpos = p.cascade ? it.first_pos
+                                       : it.first_pos + hh * TBQ + min(r, max(rows, 1) - 1);
             float m_run = -INFINITY, l_run = 0.0f;
             for (int kt = 0; kt < my_tiles; ++kt) {
                 if (!__all_sync(FULL_MASK, wait(&s_full[hh], sc & 1)))
@@ -431,8 +492,10 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
                 tc_fence_after();
                 // keys past this row's position (the tile crosses the
                 // diagonal) drop out
-                const bool diag = kt * TBK + TBK - 1 > it.first_pos + hh * TBQ;
-                const int lim = qpos - kt * TBK;   // last unmasked column
+                const int kpos = (it.kt0 + kt) * TBK;     // the tile's first key
+                const bool diag = kpos + TBK - 1 > (p.cascade ? it.first_pos
+                                                              : it.first_pos + hh * TBQ);
+                const int lim = qpos - kpos;       // last unmasked column
                 // pass 1: the row maximum, 32 columns at a time (chunk loops
                 // stay rolled: the three roles share the instruction cache)
                 float mx = -INFINITY;
@@ -535,11 +598,26 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
                 // 32 columns at a time through the warp's staging rows (16-byte
                 // slot j of row x at j xor (x mod 8): conflict-free both
                 // ways), then out as 128-byte row segments, four rows a store
-                const float inv = 1.0f / l_run;
+                // (prefix pass: O unnormalised, with the row's running
+                // maximum and sum beside it)
+                const float inv = p.cascade ? 1.0f : 1.0f / l_run;
                 const int lane = tid & 31;
                 float4 *stg = stg_all + warp * 32 * 8;
                 const int xr = lane >> 3, xj = lane & 7;   // store: rows xr, xr + 4, ...
                 const int64_t row0 = (int64_t)it.q0 + it.qt * QT + hh * TBQ + quad * 32;
+                // output row of the item's row x of this warp's 32
+                auto out_row = [&](int x) -> float * {
+                    if (!p.cascade)
+                        return p.out + ((row0 + x) * p.num_q_heads + it.h) * D;
+                    const int mr = it.qt * QT + hh * TBQ + quad * 32 + x;   // member row
+                    const int mem = mr / p.group_q;
+                    const int seq = __ldg(p.grp_seqs + it.q0 + mem);
+                    return p.part + (((int64_t)it.c * p.batch + seq) * p.num_q_heads +
+                                     it.kvh * p.group_q + (mr - mem * p.group_q)) * (D + 4);
+                };
+                // each lane finds its own row once; a store of row x takes
+                // lane x's pointer
+                float *const my_row = r < rows ? out_row(lane) : nullptr;
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     float o[32];
@@ -552,11 +630,16 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
 #pragma unroll
                     for (int x = xr; x < 32; x += 4) {
                         const float4 v = stg[x * 8 + (xj ^ (x & 7))];
+                        float *const rp = reinterpret_cast<float *>(__shfl_sync(
+                            0xffffffffu, reinterpret_cast<unsigned long long>(my_row), x));
                         if (quad * 32 + x < rows)
-                            *reinterpret_cast<float4 *>(p.out + ((row0 + x) * p.num_q_heads + it.h) * D +
-                                                        c0 + 4 * xj) = v;
+                            *reinterpret_cast<float4 *>(rp + c0 + 4 * xj) = v;
                     }
                     __syncwarp();
+                }
+                if (p.cascade && r < rows) {
+                    my_row[D] = m_run;
+                    my_row[D + 1] = l_run;
                 }
             }
             tc_fence_before();
@@ -600,8 +683,17 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
             for (int g = 0; g < QT / PROD_WARPS / 8; ++g) {
                 const int r = pw * (QT / PROD_WARPS) + g * 8 + rr;   // query of the item
                 const bool ok = r < it.rows_all;
-                const T *src = qg + ((int64_t)(it.q0 + it.qt * QT + (ok ? r : 0)) * p.num_q_heads +
-                                     it.h) * D;
+                const T *src;
+                if (p.cascade) {
+                    // member row: member mr / G's q head kvh G + mr % G
+                    const int mr = it.qt * QT + (ok ? r : 0);
+                    const int mem = mr / p.group_q;
+                    const int seq = __ldg(p.grp_seqs + it.q0 + mem);
+                    src = qg + ((int64_t)seq * p.num_q_heads + it.h + (mr - mem * p.group_q)) * D;
+                } else {
+                    src = qg + ((int64_t)(it.q0 + it.qt * QT + (ok ? r : 0)) * p.num_q_heads +
+                                it.h) * D;
+                }
 #pragma unroll
                 for (int c = cq; c < DCH; c += 4)
                     cp_async16(sQ + (r >> 7) * C::Q_BYTES + core_off(r & (TBQ - 1), c, DCH),
@@ -616,7 +708,7 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
                 // lane j: rows [j R, j R + R) of the tile, one cache block
                 // (block sizes are powers of two: shifts, no divisions); the
                 // block-id load overlaps the wait for the slot
-                const int pos0 = kt * TBK + lane * R;
+                const int pos0 = (it.kt0 + kt) * TBK + lane * R;
                 const bool inbox = lane < nbox;
                 const bool live = inbox && pos0 <= it.last_pos;
                 const int32_t blk = live ? __ldg(table + (pos0 >> p.bs_log2)) : 0;
@@ -656,7 +748,8 @@ __global__ void __launch_bounds__(TNT, 1) paged_prefill_tc_kernel(const __grid_c
                         const int yb = __shfl_sync(FULL_MASK, y, bx);
                         for (int idx = lane; idx < R * DCH; idx += 32) {
                             const int r = bx * R + idx / DCH, c = idx % DCH;
-                            const bool valid = zb != oob && kt * TBK + r <= it.last_pos;
+                            const bool valid =
+                                zb != oob && (it.kt0 + kt) * TBK + r <= it.last_pos;
                             const int64_t row =
                                 valid ? (int64_t)zb * p.block_size + yb + idx / DCH : 0;
                             cp_async16(ring + (c >> 3) * (TBK * 128) + r * 128 +
@@ -816,7 +909,9 @@ int launch_prefill_t(const pkv_pool *pool, const PrefillParams &prm, int max_q_l
     if (sms < 1)
         return PKV_ERR_CUDA;
     (void)max_q_len;
-    const int64_t nitems = (int64_t)prm.nqt * prm.num_q_heads * prm.batch;
+    const int nitems = prm.nitems;
+    if (nitems < 1)
+        return PKV_OK;
     const dim3 grid((unsigned)(nitems < sms ? nitems : sms));
     if (launch_pdl(paged_prefill_tc_kernel<D, T>, grid, dim3(TNT), (size_t)C::SMEM_BYTES, s,
                    prm) != cudaSuccess)
@@ -875,6 +970,7 @@ int launch_prefill(const pkv_pool *pool, const void *q, int num_q_heads, const v
     prm.nqt = (max_q_len + QT - 1) / QT;
     if ((int64_t)prm.nqt * num_q_heads * batch >= ((int64_t)1 << 31))
         return PKV_ERR_UNSUPPORTED;
+    prm.nitems = prm.nqt * num_q_heads * batch;
     if (!encode_cache_map(&prm.tm_k, pool, k_cache, prm.box_rows) ||
         !encode_cache_map(&prm.tm_v, pool, v_cache, prm.box_rows))
         return PKV_ERR_CUDA;
@@ -885,6 +981,145 @@ int launch_prefill(const pkv_pool *pool, const void *q, int num_q_heads, const v
                   : launch_prefill_t<64, __half>(pool, prm, max_q_len, s);
     return bf ? launch_prefill_t<128, __nv_bfloat16>(pool, prm, max_q_len, s)
               : launch_prefill_t<128, __half>(pool, prm, max_q_len, s);
+}
+
+namespace {
+
+// Merge each prefix row's chunk partials (left by the prefix pass) into chunk
+// 0: O in columns [0, D), the maximum and the sum in D + 2 and D + 3.  One
+// thread per (row, 4 columns), grid-stride over the sequences' q heads; rows
+// of sequences without a prefix are skipped.  The chunk loads of a unit are
+// independent, and the unit writes only columns it alone reads (chunk 0's
+// own maximum stays in D for the row's other units).
+template <int D>
+__global__ void __launch_bounds__(256) prefix_merge_kernel(const int32_t *seq_prefix,
+                                                           float *part, int batch,
+                                                           int num_q_heads, int kc_tiles)
+{
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int64_t cstride = (int64_t)batch * num_q_heads * (D + 4);
+    const int64_t units = (int64_t)batch * num_q_heads * (D / 4);
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = u / (D / 4);
+        const int d = (int)(u - row * (D / 4)) * 4;
+        const int b = (int)(row / num_q_heads);
+        const int P = __ldg(seq_prefix + b);
+        if (P <= 0)
+            continue;
+        const int nkc = ((P + TBK - 1) / TBK + kc_tiles - 1) / kc_tiles;
+        float *row0 = part + row * (D + 4);
+        float mc[16], M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            mc[c] = c < nkc ? __ldcg(row0 + c * cstride + D) : -INFINITY;
+            M = fmaxf(M, mc[c]);
+        }
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        float wsum = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            if (c < nkc) {
+                const float w = ex2_approx(mc[c] - M);
+                const float4 o = __ldcg(reinterpret_cast<const float4 *>(row0 + c * cstride + d));
+                acc.x = fmaf(w, o.x, acc.x);
+                acc.y = fmaf(w, o.y, acc.y);
+                acc.z = fmaf(w, o.z, acc.z);
+                acc.w = fmaf(w, o.w, acc.w);
+                if (d == 0)
+                    wsum = fmaf(w, __ldcg(row0 + c * cstride + D + 1), wsum);
+            }
+        }
+        *reinterpret_cast<float4 *>(row0 + d) = acc;
+        if (d == 0) {
+            row0[D + 2] = M;
+            row0[D + 3] = wsum;
+        }
+    }
+}
+
+}  // namespace
+
+int launch_prefix_merge(const pkv_pool *pool, const int32_t *seq_prefix, float *part, int batch,
+                        int num_q_heads, int kc_tiles, pkv_stream_t stream)
+{
+    const int64_t units = (int64_t)batch * num_q_heads * (pool->head_dim / 4);
+    int64_t blocks = (units + 255) / 256;
+    const int64_t cap = (int64_t)pool->num_sms * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        pool->head_dim == 64
+            ? launch_pdl(prefix_merge_kernel<64>, dim3((unsigned)blocks), dim3(256), 0, s,
+                         seq_prefix, part, batch, num_q_heads, kc_tiles)
+            : launch_pdl(prefix_merge_kernel<128>, dim3((unsigned)blocks), dim3(256), 0, s,
+                         seq_prefix, part, batch, num_q_heads, kc_tiles);
+    if (e != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int launch_prefix_pass(const pkv_pool *pool, const void *q, int num_q_heads, const void *k_cache,
+                       const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *seq_lens, int batch, const int32_t *grp_start,
+                       const int32_t *grp_seqs, const int32_t *grp_len, int ngroups,
+                       int max_group_size, int max_prefix_len, float scale, float *part,
+                       int *kc_tiles_out, pkv_stream_t stream)
+{
+    PrefillParams prm{};
+    prm.q = q;
+    prm.k_cache = k_cache;
+    prm.v_cache = v_cache;
+    prm.block_tables = block_tables;
+    prm.seq_lens = seq_lens;
+    prm.err = pool->d_err;
+    prm.batch = batch;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = pool->num_kv_heads;
+    prm.block_size = pool->block_size;
+    prm.bs_log2 = 0;
+    while ((1 << prm.bs_log2) < pool->block_size)
+        ++prm.bs_log2;
+    prm.max_blocks_per_seq = max_blocks_per_seq;
+    prm.num_blocks = pool->num_blocks;
+    prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    prm.box_rows = pool->block_size < TBK ? pool->block_size : TBK;
+    prm.cascade = 1;
+    prm.grp_start = grp_start;
+    prm.grp_seqs = grp_seqs;
+    prm.grp_len = grp_len;
+    prm.ngroups = ngroups;
+    prm.group_q = num_q_heads / pool->num_kv_heads;
+    prm.part = part;
+    constexpr int QT = NQH * TBQ;
+    prm.nqt = ((int64_t)max_group_size * prm.group_q + QT - 1) / QT;
+    // Key chunks: about one item per SM (the chunks of a row are merged at
+    // the end), at most 16 (the partials' room), at least one tile each.
+    const int tiles = (max_prefix_len + TBK - 1) / TBK;
+    const int64_t base = (int64_t)prm.nqt * ngroups * pool->num_kv_heads;
+    int want = (int)std::min<int64_t>(16, std::max<int64_t>(1, (pool->num_sms + base - 1) / base));
+    want = std::min(want, std::max(tiles, 1));
+    prm.kc_tiles = std::max(1, (tiles + want - 1) / want);
+    prm.nkc = std::max(1, (tiles + prm.kc_tiles - 1) / prm.kc_tiles);
+    *kc_tiles_out = prm.kc_tiles;
+    const int64_t nitems = (int64_t)prm.nqt * ngroups * pool->num_kv_heads * prm.nkc;
+    if (nitems >= ((int64_t)1 << 31))
+        return PKV_ERR_UNSUPPORTED;
+    prm.nitems = (int)nitems;
+    if (!encode_cache_map(&prm.tm_k, pool, k_cache, prm.box_rows) ||
+        !encode_cache_map(&prm.tm_v, pool, v_cache, prm.box_rows))
+        return PKV_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool bf = pool->kv_dtype == PKV_BF16;
+    if (pool->head_dim == 64)
+        return bf ? launch_prefill_t<64, __nv_bfloat16>(pool, prm, 0, s)
+                  : launch_prefill_t<64, __half>(pool, prm, 0, s);
+    return bf ? launch_prefill_t<128, __nv_bfloat16>(pool, prm, 0, s)
+              : launch_prefill_t<128, __half>(pool, prm, 0, s);
 }
 
 }  // namespace pkv

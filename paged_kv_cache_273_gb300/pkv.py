@@ -43,7 +43,8 @@ SYMBOLS = ("pkv_status_string", "kv_block_pool_init", "kv_block_pool_destroy", "
            "kv_scales_bytes", "kv_num_free_blocks", "kv_block_refcount", "kv_block_alloc",
            "kv_block_share", "kv_block_free", "kv_reserve_slots", "kv_reserve_slots_cow",
            "kv_slot_mapping", "kv_append", "kv_block_copy", "paged_decode_workspace_bytes", "paged_decode_attention",
-           "paged_decode_attention_window", "paged_prefill_attention",
+           "paged_decode_attention_window", "paged_prefill_attention", "kv_prefix_groups",
+           "paged_decode_cascade_workspace_bytes", "paged_decode_attention_cascade",
            "paged_decode_attention_noalloc", "pkv_selftest_wait_timeout", "pkv_check_error")
 
 
@@ -110,6 +111,15 @@ def load() -> ctypes.CDLL:
         lib.paged_decode_attention_window.restype = I
         lib.paged_prefill_attention.argtypes = [P, P, I, P, P, P, I, P, P, I, I, F, P, P]
         lib.paged_prefill_attention.restype = I
+        IP = ctypes.POINTER(I)
+        lib.kv_prefix_groups.argtypes = [I32P, I, I32P, I, I, I, I32P, I32P, I32P, I32P, IP, IP,
+                                         IP]
+        lib.kv_prefix_groups.restype = I
+        lib.paged_decode_cascade_workspace_bytes.argtypes = [P, I, I, I]
+        lib.paged_decode_cascade_workspace_bytes.restype = SZ
+        lib.paged_decode_attention_cascade.argtypes = [P, P, I, I, P, P, P, I, P, I, I, P, P, P,
+                                                       P, I, I, I, F, P, P, SZ, P]
+        lib.paged_decode_attention_cascade.restype = I
         lib.paged_decode_attention_noalloc.argtypes = [P, P, I, I, P, P, P, P, P, I, P, I, I, F,
                                                        P, P]
         lib.paged_decode_attention_noalloc.restype = I
@@ -370,6 +380,74 @@ def paged_prefill_attention(pool: Pool, q, k_cache, v_cache, block_tables, q_sta
         pool.handle, _dptr(q), q.shape[1], _dptr(k_cache), _dptr(v_cache), _dptr(block_tables),
         block_tables.shape[1], _dptr(q_start), _dptr(seq_lens), seq_lens.numel(), int(max_q_len),
         float(scale), _dptr(out), _stream(stream)), "paged_prefill_attention")
+
+
+def kv_prefix_groups(block_tables, seq_lens, block_size: int, min_prefix_blocks: int = 1) -> dict:
+    """Host: groups of sequences sharing leading blocks (see include/pkv.h).
+    Returns numpy int32 arrays group_start, group_seqs, group_prefix,
+    seq_prefix and the ints num_groups, max_group_size, max_prefix_len."""
+    bt = _i32(block_tables)
+    sl = _i32(seq_lens)
+    B = sl.size
+    gs = np.zeros(B + 1, np.int32)
+    gq = np.zeros(max(B, 1), np.int32)
+    gp = np.zeros(max(B, 1), np.int32)
+    sp = np.zeros(max(B, 1), np.int32)
+    ng, mg, mp = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().kv_prefix_groups(_i32p(bt), bt.shape[1] if bt.ndim == 2 else 0, _i32p(sl), B,
+                                   block_size, min_prefix_blocks, _i32p(gs), _i32p(gq), _i32p(gp),
+                                   _i32p(sp), ctypes.byref(ng), ctypes.byref(mg),
+                                   ctypes.byref(mp)), "kv_prefix_groups")
+    n = ng.value
+    return {"group_start": gs[:n + 1].copy(), "group_seqs": gq[:int(gs[n])].copy(),
+            "group_prefix": gp[:n].copy(), "seq_prefix": sp[:B].copy(), "num_groups": n,
+            "max_group_size": mg.value, "max_prefix_len": mp.value}
+
+
+def paged_decode_cascade_workspace_bytes(pool: Pool, batch: int, num_q_heads: int,
+                                         max_prefix_len: int) -> int:
+    return int(load().paged_decode_cascade_workspace_bytes(pool.handle, batch, num_q_heads,
+                                                           max_prefix_len))
+
+
+def alloc_cascade_workspace(pool: Pool, batch: int, num_q_heads: int, max_prefix_len: int,
+                            device="cuda") -> torch.Tensor:
+    """A zeroed workspace for paged_decode_attention_cascade."""
+    n = paged_decode_cascade_workspace_bytes(pool, batch, num_q_heads, max_prefix_len)
+    if n == 0:
+        raise PkvError(PKV_ERR_INVALID, "paged_decode_cascade_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def prefix_groups_to_device(groups: dict, device="cuda") -> dict:
+    """kv_prefix_groups' arrays as device int32 tensors (the ints unchanged)."""
+    out = dict(groups)
+    for k in ("group_start", "group_seqs", "group_prefix", "seq_prefix"):
+        a = groups[k]
+        out[k] = torch.from_numpy(a if a.size else np.zeros(1, np.int32)).to(device)
+    return out
+
+
+def paged_decode_attention_cascade(pool: Pool, q, k_cache, v_cache, block_tables, seq_lens,
+                                   scale: float, out, workspace, max_seq_len: int, groups: dict,
+                                   stream=None) -> None:
+    """paged_decode_attention with shared prefixes scored once per group;
+    groups: prefix_groups_to_device(kv_prefix_groups(...))."""
+    if q.dtype not in PKV_DTYPE:
+        raise ValueError("unsupported q dtype %s" % q.dtype)
+    if out.dtype != torch.float32:
+        raise ValueError("out must be float32")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_tables and seq_lens must be int32")
+    B, Hq, _ = q.shape
+    _check(load().paged_decode_attention_cascade(
+        pool.handle, _dptr(q), PKV_DTYPE[q.dtype], Hq, _dptr(k_cache), _dptr(v_cache),
+        _dptr(block_tables), block_tables.shape[1], _dptr(seq_lens), B, int(max_seq_len),
+        _dptr(groups["group_start"]), _dptr(groups["group_seqs"]), _dptr(groups["group_prefix"]),
+        _dptr(groups["seq_prefix"]), int(groups["num_groups"]), int(groups["max_group_size"]),
+        int(groups["max_prefix_len"]), float(scale), _dptr(out), _dptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)),
+        "paged_decode_attention_cascade")
 
 
 def paged_decode_attention_noalloc(pool: Pool, q, k_cache, v_cache, block_tables, seq_lens,
