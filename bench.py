@@ -430,6 +430,72 @@ def time_workload(name: str, dev, stream, peak: float, reps: int = 20) -> dict:
     return res
 
 
+def time_shared_prompt(dev, stream, peak: float, B=64, P=8192, reps=10) -> dict:
+    """Decode attention where all B sequences share a P-token prompt (one
+    copy of its blocks) and add private suffixes of 64..1024 tokens (seeded),
+    on the Llama-2-70B head shape (64 q / 8 KV heads, d 128, fp16, block
+    size 16): the plain call, which scores the prompt once per sequence,
+    against paged_decode_attention_cascade, which scores it once."""
+    import torch
+    from paged_kv_cache_273_gb300 import pkv
+    rng = np.random.default_rng(12)
+    Hq, Hkv, D, bs = 64, 8, 128, 16
+    suf = rng.integers(64, 1025, size=B)
+    lens = (P + suf).astype(np.int32)
+    pb = P // bs
+    nb = -(-lens // bs)
+    NB = pb + int((nb - pb).sum()) + 16
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.zeros((B, int(nb.max())), np.int32)
+    tables[:, :pb] = perm[:pb]
+    cur = pb
+    for b in range(B):
+        n = int(nb[b]) - pb
+        tables[b, pb:pb + n] = perm[cur:cur + n]
+        cur += n
+    pool = pkv.kv_block_pool_init(NB, bs, Hkv, D, pkv.PKV_F16)
+    kc, vc, _, _ = pool.alloc_cache(dev)
+    kc.normal_()
+    vc.normal_()
+    q = torch.randn((B, Hq, D), device=dev).to(torch.float16)
+    td = torch.from_numpy(tables).to(dev)
+    ld = torch.from_numpy(lens).to(dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = pkv.alloc_workspace(pool, B, Hq, dev)
+    g = pkv.kv_prefix_groups(tables, lens, bs)
+    gd = pkv.prefix_groups_to_device(g, dev)
+    cws = pkv.alloc_cascade_workspace(pool, B, Hq, g["max_prefix_len"], dev)
+    ml = int(lens.max())
+
+    def plain(i=0):
+        pkv.paged_decode_attention(pool, q, kc, vc, td, ld, D ** -0.5, out, ws, ml, stream=stream)
+
+    def casc(i=0):
+        pkv.paged_decode_attention_cascade(pool, q, kc, vc, td, ld, D ** -0.5, out, cws, ml, gd,
+                                           stream=stream)
+
+    us = {}
+    for name, f in (("plain", plain), ("cascade", casc)):
+        for _ in range(3):
+            f()
+        us[name] = statistics.median(timed_loop(stream, f, reps, host_queue_us(f, 3))) / reps * 1e3
+    if pkv.pkv_check_error(pool) != pkv.PKV_OK:
+        raise RuntimeError("device error in the shared-prompt measurement")
+    wl = W.Workload("shared_prompt", Hq, Hkv, D, bs, B, W.F16, W.F16, W.F16, 12, "fixed", P, P, 1)
+    logical = attention_bytes(wl, lens)
+    unique = attention_bytes_unique(wl, lens, tables)
+    return {"config": "%d sequences sharing a %d-token prompt + 64..1024 own tokens, 64 q / 8 "
+                      "KV heads, d 128, fp16, block size 16" % (B, P),
+            "plain_us": us["plain"], "cascade_us": us["cascade"],
+            "unique_bytes": unique, "logical_bytes": logical,
+            "plain": {"value": unique / (us["plain"] / 1e6) / 1e9, "unit": "GB/s",
+                      "frac": unique / (us["plain"] / 1e6) / 1e9 / peak},
+            "cascade": {"value": unique / (us["cascade"] / 1e6) / 1e9, "unit": "GB/s",
+                        "frac": unique / (us["cascade"] / 1e6) / 1e9 / peak},
+            "note": "unique bytes (the prompt's rows once); %d calls back to back, median of 3"
+                    % reps}
+
+
 def time_prefill(dev, stream, peak_tflops: float, B=4, n=4096, reps=10) -> dict:
     """Causal prefill of B prompts of n tokens on the Llama-3-8B head shape
     (32 q / 8 KV heads, d 128, bf16, block size 16), device-filled caches."""
@@ -763,6 +829,7 @@ def run_gpu(args):
     if world == 1:
         for name in ("gpt2", "llama2_70b", "int8", "int4"):
             others[name] = time_workload(name, dev, stream, peak)
+        others["shared_prompt_8k"] = time_shared_prompt(dev, stream, peak)
     bf16_peak = peaks.get("bf16_tflops") or 1900.0
     prefill = time_prefill(dev, stream, bf16_peak) if world == 1 else None
 
