@@ -157,11 +157,11 @@ struct Params {
 
 // Shared-memory carve-up (dynamic), identical on host and device.
 struct Layout {
-    int stages, qring, merge, ps, lens, tstart, bars, misc, total;
+    int stages, qring, merge, ps, pre, lens, tstart, bars, misc, total;
 };
 
 template <int D, int G, int KV>
-__host__ __device__ inline Layout make_layout(int nst, int batch)
+__host__ __device__ inline Layout make_layout(int nst, int batch, bool prefix)
 {
     using C = Cfg<D, G, KV>;
     Layout L;
@@ -170,6 +170,7 @@ __host__ __device__ inline Layout make_layout(int nst, int batch)
     L.qring = o; o += 2 * C::QSLOT;
     L.merge = o; o += round_up(C::MERGE_FLOATS * 4, 16);
     L.ps = o; o += C::PS_FLOATS * 4;
+    L.pre = o; o += prefix ? G * (D + 4) * 4 : 0;   // a piece's merged prefix rows
     L.lens = o; o += 2 * batch * 4;        // lengths, then window starts
     L.tstart = o; o += (batch + 1) * 4;
     o = round_up(o, 8);
@@ -890,11 +891,12 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     constexpr int W = C::W;
     constexpr int NTHREADS = C::NTHREADS;
     extern __shared__ __align__(128) unsigned char smem[];
-    const Layout lay = make_layout<D, G, KV>(p.nst, p.batch);
+    const Layout lay = make_layout<D, G, KV>(p.nst, p.batch, p.seq_prefix != nullptr);
     unsigned char *stages = smem + lay.stages;
     unsigned char *qring = smem + lay.qring;
     float *merge = reinterpret_cast<float *>(smem + lay.merge);
     float *psbuf = reinterpret_cast<float *>(smem + lay.ps);
+    float *s_pre = reinterpret_cast<float *>(smem + lay.pre);
     int *s_len = reinterpret_cast<int *>(smem + lay.lens);
     int *s_lo = s_len + p.batch;   // first attended position (sliding window)
     int *s_tstart = reinterpret_cast<int *>(smem + lay.tstart);
@@ -1216,6 +1218,18 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             den = fmaf(den, fo, lp * fp);
             m = mn;
         };
+        // The same from the piece's prefix rows staged in shared memory.
+        auto fold_prefix_staged = [&](int b, int g, int d, float &m, float &num, float &den) {
+            if (p.seq_prefix == nullptr || s_lo[b] == 0)
+                return;
+            const float *row = s_pre + g * (D + 4);
+            const float mp = row[D + 2], lp = row[D + 3], op = row[d];
+            const float mn = fmaxf(m, mp);
+            const float fo = exp2_approx(m - mn), fp = exp2_approx(mp - mn);
+            num = fmaf(num, fo, op * fp);
+            den = fmaf(den, fo, lp * fp);
+            m = mn;
+        };
         // Rows of sequences with no tile here: zeros for empty sequences, the
         // prefix alone for a sequence whose rows are all shared; sequence b
         // is CTA (b % grid)'s job.
@@ -1310,6 +1324,14 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 if (lane == 0)
                     mbar_arrive(&qempty[slot]);
                 ++qn;
+            }
+            if (p.seq_prefix != nullptr && s_lo[b] > 0) {
+                // the merged prefix rows of this piece's G heads, fetched now
+                // for its end (a load there would wait behind the streaming)
+                const float *src = p.prefix_part + ((int64_t)b * Hq + kvh * G) * (D + 4);
+                for (int i = ctid; i < G * (D + 4) / 4; i += W * 32)
+                    cp_async_16b(s_pre + 4 * i, src + 4 * i);
+                asm volatile("cp.async.commit_group;" ::: "memory");
             }
 
             float m_run[C::NF], l_run[C::NF];
@@ -1507,6 +1529,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             }
 
             // ---- merge the W warp states of this piece
+            asm volatile("cp.async.wait_all;" ::: "memory");   // this piece's prefix rows
             if constexpr (C::MMA) {
                 // lane (gid, tig) holds heads 2tig, 2tig+1 x elements
                 // [gid D/8, (gid+1) D/8); l sums over the lane's tokens
@@ -1597,7 +1620,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     const int idx = ctid + j * W * 32;
                     if (idx < G * D) {
                         float m = o_m[j], num = o_num[j], den = o_den[j];
-                        fold_prefix(b, kvh * G + idx / D, idx % D, m, num, den);
+                        fold_prefix_staged(b, idx / D, idx % D, m, num, den);
                         orow[idx] = num / den;
                     }
                 }
@@ -1622,7 +1645,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                             float m, num, den;
                             fold_partials(seg, c_first, c_last, cta, o_m[j], o_num[j], o_den[j],
                                           idx, m, num, den);
-                            fold_prefix(b, kvh * G + idx / D, idx % D, m, num, den);
+                            fold_prefix_staged(b, idx / D, idx % D, m, num, den);
                             orow[idx] = num / den;
                         }
                     }
@@ -1689,7 +1712,7 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
 {
     using C = Cfg<D, G, KV>;
     Params prm = base;
-    const Layout fixed = make_layout<D, G, KV>(0, batch);
+    const Layout fixed = make_layout<D, G, KV>(0, batch, prm.seq_prefix != nullptr);
     const int budget = pool->max_smem_optin - fixed.total - 256;
     int nst = budget / (C::STAGE_BYTES + 16);
     if (nst > MAX_STAGES)
@@ -1697,7 +1720,7 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
     if (nst < 2)
         return PKV_ERR_UNSUPPORTED;
     prm.nst = nst;
-    const Layout lay = make_layout<D, G, KV>(nst, batch);
+    const Layout lay = make_layout<D, G, KV>(nst, batch, prm.seq_prefix != nullptr);
 
     // The dynamic shared-memory limit is an attribute of the kernel in the
     // current device's context (a context that a device reset replaces), so
