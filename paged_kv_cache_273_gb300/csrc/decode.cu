@@ -42,6 +42,33 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
+bool encode_swizzled_tile_map(CUtensorMap *map, const void *base, int row_bytes,
+                              const pkv_pool *pool)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || (row_bytes != 128 && row_bytes != 256) || pool->block_size < 16)
+        return false;
+    const cuuint64_t bs = (cuuint64_t)pool->block_size;
+    const cuuint64_t nbh = (cuuint64_t)pool->num_blocks * (cuuint64_t)pool->num_kv_heads;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (row_bytes == 128) {
+        const cuuint64_t dims[3] = {128, bs, nbh};
+        const cuuint64_t strides[2] = {128, bs * 128};
+        const cuuint32_t box[3] = {128, 16, 1};
+        return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    const cuuint64_t dims[4] = {128, 2, bs, nbh};
+    const cuuint64_t strides[3] = {128, 256, bs * 256};
+    const cuuint32_t box[4] = {128, 2, 16, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads)
 {
     const int G = num_q_heads / pool->num_kv_heads;

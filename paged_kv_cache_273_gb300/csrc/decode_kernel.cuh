@@ -39,6 +39,7 @@
 
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -111,7 +112,15 @@ struct Cfg {
     static constexpr int VE = D / 32;              // V elements per lane
     static constexpr int KV_BYTES = TILE * ROWB;   // one tile of K (or V)
     static constexpr int SC_BYTES = quantized(KV) ? TILE * 2 : 0;
-    static constexpr int STAGE_BYTES = round_up(2 * KV_BYTES + 2 * SC_BYTES, 128);
+    // a stage: the tile's K then V (the scales ride in a ring of their own,
+    // so that every stage starts on a 1024-byte boundary)
+    static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+    // The tensor-core tile math reads rows of 128 or 256 bytes through the
+    // 128-byte swizzle: with blocks of >= 16 rows its K/V tiles come by
+    // tensor copies that lay them out swizzled (16-byte chunk j of a
+    // 128-byte segment s at j ^ (s mod 8)), which spreads the fragment loads
+    // over the banks.
+    static constexpr bool SWIZZLE_OK = mma_path(KV, G) && (ROWB == 128 || ROWB == 256);
     static constexpr int QSLOT = round_up(G * D * 4, 128);   // fits any q dtype
     static constexpr int MERGE_FLOATS = W * G * (D + 2);
     // per warp (CUDA-core tile math only): {p, p} pairs of the tile
@@ -123,6 +132,11 @@ struct Cfg {
 };
 
 struct Params {
+    // K and V caches as tensors of rows of 128-byte segments, for the
+    // swizzled tensor copies (see Cfg::SWIZZLE_OK): {ROWB / e, bs, NB * Hkv}
+    // for 128-byte rows, {128 / e, 2, bs, NB * Hkv} for 256-byte rows
+    CUtensorMap tm_k, tm_v;
+    int swz;            // tiles come swizzled by tensor copies
     const void *q;
     const unsigned char *k_cache;
     const unsigned char *v_cache;
@@ -157,7 +171,7 @@ struct Params {
 
 // Shared-memory carve-up (dynamic), identical on host and device.
 struct Layout {
-    int stages, qring, merge, ps, pre, lens, tstart, bars, misc, total;
+    int stages, scales, qring, merge, ps, pre, lens, tstart, bars, misc, total;
 };
 
 template <int D, int G, int KV>
@@ -167,6 +181,7 @@ __host__ __device__ inline Layout make_layout(int nst, int batch, bool prefix)
     Layout L;
     int o = 0;
     L.stages = o; o += nst * C::STAGE_BYTES;
+    L.scales = o; o += nst * 2 * C::SC_BYTES;      // K then V scales of each stage
     L.qring = o; o += 2 * C::QSLOT;
     L.merge = o; o += round_up(C::MERGE_FLOATS * 4, 16);
     L.ps = o; o += C::PS_FLOATS * 4;
@@ -511,6 +526,41 @@ __device__ __forceinline__ float exp2_approx(float x)
     return y;
 }
 
+// The 16 rows at row `y` of (block, head) `z` as one tensor copy with the
+// 128-byte swizzle into shared memory at dst (1024-byte aligned): 3-D view
+// {128-byte row, bs, NB * Hkv} for 128-byte rows, 4-D {128 bytes, 2, bs,
+// NB * Hkv} for 256-byte rows.  Completion is counted in bytes on the
+// mbarrier; `policy` is an L2 cache hint.
+template <int ROWB>
+__device__ __forceinline__ void tma_tile_swz(void *dst, const CUtensorMap *map, int y, int z,
+                                             uint64_t *bar, uint64_t policy)
+{
+    if constexpr (ROWB == 128) {
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(z), "r"(smem_addr(bar)),
+            "l"(policy)
+            : "memory");
+    } else {
+        static_assert(ROWB == 256, "swizzled tiles have rows of 128 or 256 bytes");
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(y), "r"(z),
+            "r"(smem_addr(bar)), "l"(policy)
+            : "memory");
+    }
+}
+
+// Byte offset of a 16-byte chunk inside a tile laid out by the swizzled
+// tensor copies (128-byte swizzle: chunk bits 4-6 xor segment bits 7-9), or
+// unchanged for a plain tile.
+__device__ __forceinline__ uint32_t swz_off(uint32_t off, bool swz)
+{
+    return swz ? off ^ ((off >> 3) & 0x70u) : off;
+}
+
 // ---- tile math on the tensor cores (warp-level MMA) --------------------------
 //
 // For 16-bit, 8-bit and 4-bit caches a warp does a tile's two products as
@@ -675,25 +725,30 @@ template <int D, int G, int KV, bool QS>
 __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsigned char *sK,
                                          const unsigned char *sV, const __half *sKS,
                                          const __half *sVS, int nvalid, int tlo, float scale_log2,
-                                         int lane, uint64_t *empty_bar)
+                                         int lane, uint64_t *empty_bar, int swz)
 {
     using M = MmaCfg<D, KV>;
     constexpr bool BF = MmaBf16<KV>::v;
     constexpr int ROWB = M::ROWB;
     const int gid = lane >> 2, tig = lane & 3;
 
+    // (tiles laid out by the swizzled tensor copies: chunk addresses go
+    // through swz_off)
+    constexpr bool CAN_SWZ = mma_path(KV, G) && (ROWB == 128 || ROWB == 256);
+    const bool sw = CAN_SWZ && swz != 0;
+
     // ---- S^T = K q^T (rows gid, gid + 8 of the tile; the lane's quarter of d)
     float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     {
-        const unsigned char *r0 = sK + gid * ROWB + tig * M::KQB;
-        const unsigned char *r1 = r0 + 8 * ROWB;
+        const uint32_t k0 = gid * ROWB + tig * M::KQB;
+        const uint32_t k1 = k0 + 8 * ROWB;
         if constexpr (KvBits<KV>::v == 16) {
             const int rot = M::ROTATE ? (tig >> 1) * 2 : 0;
 #pragma unroll
             for (int c = 0; c < M::KCH; ++c) {
                 const int ch = (c + rot) & (M::KCH - 1);
-                const uint4 x = *reinterpret_cast<const uint4 *>(r0 + ch * 16);
-                const uint4 y = *reinterpret_cast<const uint4 *>(r1 + ch * 16);
+                const uint4 x = *reinterpret_cast<const uint4 *>(sK + swz_off(k0 + ch * 16, sw));
+                const uint4 y = *reinterpret_cast<const uint4 *>(sK + swz_off(k1 + ch * 16, sw));
                 mma_16816<BF>(s, x.x, y.x, x.y, y.y, st.qh[2 * c][0], st.qh[2 * c][1]);
                 mma_16816<BF>(s, x.z, y.z, x.w, y.w, st.qh[2 * c + 1][0], st.qh[2 * c + 1][1]);
                 if constexpr (QS) {
@@ -705,8 +760,8 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
         } else if constexpr (KV == PKV_I8) {
 #pragma unroll
             for (int c = 0; c < M::KCH; ++c) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(r0 + c * 16);
-                const uint4 y = *reinterpret_cast<const uint4 *>(r1 + c * 16);
+                const uint4 x = *reinterpret_cast<const uint4 *>(sK + swz_off(k0 + c * 16, sw));
+                const uint4 y = *reinterpret_cast<const uint4 *>(sK + swz_off(k1 + c * 16, sw));
                 const uint32_t xw[4] = {x.x ^ 0x80808080u, x.y ^ 0x80808080u, x.z ^ 0x80808080u,
                                         x.w ^ 0x80808080u};
                 const uint32_t yw[4] = {y.x ^ 0x80808080u, y.y ^ 0x80808080u, y.z ^ 0x80808080u,
@@ -725,8 +780,8 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
             }
         } else {
             static_assert(KV == PKV_I4 && D == 128, "4-bit rows are d = 128");
-            const uint4 x = *reinterpret_cast<const uint4 *>(r0);
-            const uint4 y = *reinterpret_cast<const uint4 *>(r1);
+            const uint4 x = *reinterpret_cast<const uint4 *>(sK + k0);
+            const uint4 y = *reinterpret_cast<const uint4 *>(sK + k1);
             const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
             const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
@@ -751,11 +806,13 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
         const int toks[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const unsigned char *p = sV + toks[i] * ROWB + gid * M::VB;
+            const uint32_t v0 = toks[i] * ROWB + gid * M::VB;
+            const unsigned char *p = sV + v0;
             if constexpr (M::VB >= 16) {
 #pragma unroll
                 for (int c = 0; c < M::VB / 16; ++c) {
-                    const uint4 x = *reinterpret_cast<const uint4 *>(p + 16 * c);
+                    const uint4 x =
+                        *reinterpret_cast<const uint4 *>(sV + swz_off(v0 + 16 * c, sw));
                     vw[i][4 * c] = x.x; vw[i][4 * c + 1] = x.y;
                     vw[i][4 * c + 2] = x.z; vw[i][4 * c + 3] = x.w;
                 }
@@ -885,14 +942,15 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
 // QS: q's type differs from the MMA operand type, so q is split into a high
 // and a low part (tensor-core tile math only).
 template <int D, int G, int KV, bool QS>
-__global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kernel(const Params p)
+__global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kernel(const __grid_constant__ Params p)
 {
     using C = Cfg<D, G, KV>;
     constexpr int W = C::W;
     constexpr int NTHREADS = C::NTHREADS;
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem[];
     const Layout lay = make_layout<D, G, KV>(p.nst, p.batch, p.seq_prefix != nullptr);
     unsigned char *stages = smem + lay.stages;
+    unsigned char *scale_ring = smem + lay.scales;
     unsigned char *qring = smem + lay.qring;
     float *merge = reinterpret_cast<float *>(smem + lay.merge);
     float *psbuf = reinterpret_cast<float *>(smem + lay.ps);
@@ -906,6 +964,10 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     uint64_t *qempty = qfull + 2;
     int *misc = reinterpret_cast<int *>(smem + lay.misc);
     volatile int *abort_flag = misc + 0;  // set on any timeout
+    // The 128-byte swizzle repeats every 1024 bytes of shared address, and the
+    // tile reads assume it starts at a stage's start: without that alignment
+    // the tiles come by plain bulk copies instead.
+    const int swz = (C::SWIZZLE_OK && p.swz && (smem_addr(smem) & 1023u) == 0) ? 1 : 0;
     // misc[2]: zero word; misc[4..6): "this CTA merges the partials of its
     // first / last piece"; misc[8..]: scan scratch
 
@@ -1103,7 +1165,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     if (!t_done && !hold && mbar_test_wait(&empty[st], (uint32_t)(rnd & 1) ^ 1u)) {
                     unsigned char *sK = stages + st * C::STAGE_BYTES;
                     unsigned char *sV = sK + C::KV_BYTES;
-                    unsigned char *sKS = sV + C::KV_BYTES;
+                    unsigned char *sKS = scale_ring + st * 2 * C::SC_BYTES;
                     unsigned char *sVS = sKS + C::SC_BYTES;
                     const int rows_per_copy = bs >= TILE ? TILE : bs;
                     const uint32_t kv_copy = (uint32_t)(rows_per_copy * C::ROWB);
@@ -1132,10 +1194,29 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                             const int64_t row0 = ((int64_t)cur.id[u] * Hkv + cur.kvh) * bs +
                                                  (bs >= TILE ? in_block : 0);
                             const int dst_row = u * rows_per_copy;
-                            bulk_g2s_hint(sK + dst_row * C::ROWB, p.k_cache + row0 * C::ROWB,
-                                          kv_copy, &full[st], policy);
-                            bulk_g2s_hint(sV + dst_row * C::ROWB, p.v_cache + row0 * C::ROWB,
-                                          kv_copy, &full[st], policy);
+                            if constexpr (C::SWIZZLE_OK) {
+                                if (swz) {
+                                    // 16 rows of the (block, head) as one
+                                    // swizzled tensor copy each
+                                    const int z = cur.id[u] * Hkv + cur.kvh;
+                                    tma_tile_swz<C::ROWB>(sK, &p.tm_k, in_block, z, &full[st],
+                                                          policy);
+                                    tma_tile_swz<C::ROWB>(sV, &p.tm_v, in_block, z, &full[st],
+                                                          policy);
+                                } else {
+                                    bulk_g2s_hint(sK + dst_row * C::ROWB,
+                                                  p.k_cache + row0 * C::ROWB, kv_copy, &full[st],
+                                                  policy);
+                                    bulk_g2s_hint(sV + dst_row * C::ROWB,
+                                                  p.v_cache + row0 * C::ROWB, kv_copy, &full[st],
+                                                  policy);
+                                }
+                            } else {
+                                bulk_g2s_hint(sK + dst_row * C::ROWB, p.k_cache + row0 * C::ROWB,
+                                              kv_copy, &full[st], policy);
+                                bulk_g2s_hint(sV + dst_row * C::ROWB, p.v_cache + row0 * C::ROWB,
+                                              kv_copy, &full[st], policy);
+                            }
                             if constexpr (quantized(KV)) {
                                 // The scales (32 bytes of each array per 16
                                 // rows) go by 16-byte (8-byte for 4-row
@@ -1383,11 +1464,12 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 }
                 const unsigned char *sK = stages + st * C::STAGE_BYTES;
                 const unsigned char *sV = sK + C::KV_BYTES;
-                const __half *sKS = reinterpret_cast<const __half *>(sV + C::KV_BYTES);
+                const __half *sKS =
+                    reinterpret_cast<const __half *>(scale_ring + st * 2 * C::SC_BYTES);
                 const __half *sVS = sKS + TILE;
                 if constexpr (C::MMA) {
                     mma_tile<D, G, KV, QS>(mst, sK, sV, sKS, sVS, nvalid, tlo, p.scale_log2,
-                                           lane, &empty[st]);
+                                           lane, &empty[st], swz);
                 } else {
                     // After the reduction below the lane holds token t, heads g0 + r.
                     const int t = tq + C::TQ * (ds >> 1);
@@ -1712,9 +1794,21 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
 {
     using C = Cfg<D, G, KV>;
     Params prm = base;
+    // Tiles of the tensor-core tile math come by swizzled tensor copies when
+    // a tile is 16 rows of one block (block size >= 16).
+    prm.swz = 0;
+    if constexpr (C::SWIZZLE_OK) {
+        if (pool->block_size >= TILE) {
+            if (!encode_swizzled_tile_map(&prm.tm_k, prm.k_cache, C::ROWB, pool) ||
+                !encode_swizzled_tile_map(&prm.tm_v, prm.v_cache, C::ROWB, pool))
+                return PKV_ERR_CUDA;
+            prm.swz = 1;
+        }
+    }
     const Layout fixed = make_layout<D, G, KV>(0, batch, prm.seq_prefix != nullptr);
     const int budget = pool->max_smem_optin - fixed.total - 256;
-    int nst = budget / (C::STAGE_BYTES + 16);
+    // a stage: its K and V tiles, their scales and two barriers
+    int nst = budget / (C::STAGE_BYTES + 2 * C::SC_BYTES + 16);
     if (nst > MAX_STAGES)
         nst = MAX_STAGES;
     if (nst < 2)

@@ -121,6 +121,13 @@ int launch_prefix_merge(const pkv_pool *pool, const int32_t *seq_prefix, float *
 // through the runtime; null if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// A cache [NB][Hkv][bs][row_bytes] (row_bytes 128 or 256) as the tensor the
+// decode kernel's swizzled tile copies read: bytes in 128-byte segments,
+// {128, bs, NB * Hkv} or {128, 2, bs, NB * Hkv}, boxes of 16 rows, 128-byte
+// swizzle.  False if the encoder is unavailable or refuses.
+bool encode_swizzled_tile_map(CUtensorMap *map, const void *base, int row_bytes,
+                              const pkv_pool *pool);
+
 // seq_prefix / prefix_part: shared-prefix decode (null: none), see Params.
 int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
                   const void *k_cache, const void *v_cache, const void *k_scales,
