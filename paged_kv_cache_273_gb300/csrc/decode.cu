@@ -89,8 +89,10 @@ int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int nu
     (void)workspace_bytes;
     const int Hkv = pool->num_kv_heads;
     const int G = num_q_heads / Hkv;
+    // tiles, and their cost for the split over CTAs, must count in 31 bits
     const int64_t tiles_bound =
-        (int64_t)batch * Hkv * (((int64_t)max_seq_len + kern::TILE - 1) / kern::TILE);
+        (int64_t)batch * Hkv *
+        (((int64_t)max_seq_len + kern::TILE - 1) / kern::TILE + kern::piece_cost(G));
     if (tiles_bound >= ((int64_t)1 << 31))
         return PKV_ERR_UNSUPPORTED;
     kern::Params prm{};

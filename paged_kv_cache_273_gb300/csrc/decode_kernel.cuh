@@ -42,6 +42,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <type_traits>
 
@@ -55,7 +56,7 @@ using namespace dev;
 constexpr int TILE = 16;        // tokens per pipeline stage
 constexpr int MAX_STAGES = 64;
 // misc ints in shared memory: [0] abort flag, [2] a constant zero, [4..6)
-// "merge the partials of the first / last piece" flags, [8..8+warps) scan
+// "merge the partials of the first / last piece" flags, [8..32) scan
 // scratch, [32..32+MAX_STAGES) last issued round per stage (+1; 0 = never),
 // [96..98) q copies issued per slot, [98] number of q copies issued so far
 // (they go out in piece order).
@@ -171,7 +172,7 @@ struct Params {
 
 // Shared-memory carve-up (dynamic), identical on host and device.
 struct Layout {
-    int stages, scales, qring, merge, ps, pre, lens, tstart, bars, misc, total;
+    int stages, scales, qring, merge, ps, pre, lens, tstart, cstart, bars, misc, total;
 };
 
 template <int D, int G, int KV>
@@ -183,17 +184,27 @@ __host__ __device__ inline Layout make_layout(int nst, int batch, bool prefix)
     L.stages = o; o += nst * C::STAGE_BYTES;
     L.scales = o; o += nst * 2 * C::SC_BYTES;      // K then V scales of each stage
     L.qring = o; o += 2 * C::QSLOT;
+    // (every region from here on starts on a 16-byte boundary: the ps and
+    // prefix-row regions take 16-byte accesses)
     L.merge = o; o += round_up(C::MERGE_FLOATS * 4, 16);
-    L.ps = o; o += C::PS_FLOATS * 4;
-    L.pre = o; o += prefix ? G * (D + 4) * 4 : 0;   // a piece's merged prefix rows
+    L.ps = o; o += round_up(C::PS_FLOATS * 4, 16);
+    L.pre = o; o += prefix ? round_up(G * (D + 4) * 4, 16) : 0;   // a piece's merged prefix rows
     L.lens = o; o += 2 * batch * 4;        // lengths, then window starts
     L.tstart = o; o += (batch + 1) * 4;
+    L.cstart = o; o += (batch + 1) * 4;
     o = round_up(o, 8);
     L.bars = o; o += (2 * nst + 4) * 8;
     L.misc = o; o += MISC_INTS * 4;
     L.total = round_up(o, 128);
     return L;
 }
+
+// The end of a piece (its warps' states merged, the result written) costs
+// about as much as this many tiles, the more the more heads it merges
+// (measured on GB300: about 1.4 us a piece at G = 4 and 3 us at G = 8,
+// against 0.15-0.17 us a tile).  The split over CTAs charges it, so that a
+// CTA whose share holds many short sequences gets fewer tiles.
+__host__ __device__ constexpr int piece_cost(int G) { return 2 + 2 * G; }
 
 // Owner CTA of global tile x when T tiles are split evenly over P CTAs:
 // CTA c owns [floor(c*T/P), floor((c+1)*T/P)).
@@ -786,11 +797,15 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
             const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const int w = ks >> 1, k0 = 2 * (ks & 1);
-                const uint32_t a0 = i4pair_to_half2(xw[w], k0);
-                const uint32_t a2 = i4pair_to_half2(xw[w], k0 + 1);
-                const uint32_t a1 = i4pair_to_half2(yw[w], k0);
-                const uint32_t a3 = i4pair_to_half2(yw[w], k0 + 1);
+                // pair k of word w (codes k, k + 4): k = 0, 1 from the word,
+                // k = 2, 3 from the word shifted down a byte
+                const int w = ks >> 1;
+                const uint32_t xs = (ks & 1) ? xw[w] >> 8 : xw[w];
+                const uint32_t ys = (ks & 1) ? yw[w] >> 8 : yw[w];
+                const uint32_t a0 = i4pair_lo_to_half2(xs);
+                const uint32_t a2 = i4pair_hi_to_half2(xs);
+                const uint32_t a1 = i4pair_lo_to_half2(ys);
+                const uint32_t a3 = i4pair_hi_to_half2(ys);
                 mma_16816<BF>(s, a0, a1, a2, a3, st.qh[ks][0], st.qh[ks][1]);
                 if constexpr (QS)
                     mma_16816<BF>(s, a0, a1, a2, a3, st.ql[ks][0], st.ql[ks][1]);
@@ -919,18 +934,17 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
             a2 = i8pair_to_half2<0x4140u>(tcd);
             a3 = i8pair_to_half2<0x4342u>(tcd);
         } else {
-            // codes 2j, 2j+1 of the token's eighth (16 codes in two words):
-            // interleave the two tokens' bytes so that a half holds one
-            // token's four codes, then one nibble pair per half-word
-            const int w = j >> 2, k = (2 * j) & 3;
-            const uint32_t tab = (j & 2) ? __byte_perm(vw[0][w], vw[1][w], 0x7632u)
-                                         : __byte_perm(vw[0][w], vw[1][w], 0x5410u);
-            const uint32_t tcd = (j & 2) ? __byte_perm(vw[2][w], vw[3][w], 0x7632u)
-                                         : __byte_perm(vw[2][w], vw[3][w], 0x5410u);
-            a0 = i4pair_to_half2(tab, k);
-            a1 = i4pair_to_half2(tab, k + 1);
-            a2 = i4pair_to_half2(tcd, k);
-            a3 = i4pair_to_half2(tcd, k + 1);
+            // codes 2j, 2j+1 of the token's eighth (16 codes in two words)
+            // are byte j of it: that byte of the two tokens goes to bytes 0
+            // and 2 of one word (low nibbles: code 2j; high: code 2j + 1)
+            const int w = j >> 2, b = j & 3;
+            const uint32_t sel = (uint32_t)b | ((uint32_t)(b + 4) << 8);
+            const uint32_t tab = __byte_perm(vw[0][w], vw[1][w], sel);
+            const uint32_t tcd = __byte_perm(vw[2][w], vw[3][w], sel);
+            a0 = i4pair_lo_to_half2(tab);
+            a1 = i4pair_hi_to_half2(tab);
+            a2 = i4pair_lo_to_half2(tcd);
+            a3 = i4pair_hi_to_half2(tcd);
         }
         mma_16816<BF>(st.acc[j], a0, a1, a2, a3, bh0, bh1);
         mma_16816<BF>(st.acc[j], a0, a1, a2, a3, bl0, bl1);
@@ -958,6 +972,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     int *s_len = reinterpret_cast<int *>(smem + lay.lens);
     int *s_lo = s_len + p.batch;   // first attended position (sliding window)
     int *s_tstart = reinterpret_cast<int *>(smem + lay.tstart);
+    int *s_cstart = reinterpret_cast<int *>(smem + lay.cstart);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
     uint64_t *empty = full + p.nst;
     uint64_t *qfull = empty + p.nst;
@@ -1025,57 +1040,110 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     auto seq_tiles = [&](int b) {
         return s_len[b] > s_lo[b] ? (s_len[b] + TILE - 1) / TILE - s_lo[b] / TILE : 0;
     };
-    // Exclusive prefix over the sequences of value(b), written to out[0..B];
-    // thread t takes a contiguous run of sequences, then warp and block scans.
-    auto block_scan = [&](auto value, int *out) {
+    // One pass over the sequences (thread t takes a contiguous run, then
+    // warp and block scans): the exclusive prefixes of tiles (s_tstart) and
+    // of cost (s_cstart), where each (sequence, KV head) segment costs PC
+    // units for its piece end, then one per tile; and this CTA's tiles.
+    //
+    // The cost is split evenly over P = min(grid, cost) CTAs; a CTA owns
+    // the tiles whose cost position (segment start + PC + tile) falls in
+    // its share.  The CTAs holding pieces of one sequence/head are
+    // consecutive, and each CTA between the owners of a segment's first and
+    // last tile owns a tile of it (tile positions are consecutive there), as
+    // the merge counts on.
+    constexpr int PC = piece_cost(G);
+    constexpr int NW = NTHREADS / 32;
+    static_assert(NW <= 12, "scan scratch: misc[8, 32)");
+    int *s_range = reinterpret_cast<int *>(smem + lay.merge);   // free until the first merge
+    {
         const int per = (B + NTHREADS - 1) / NTHREADS;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
-        int sum = 0;
-        for (int b = b0; b < b1; ++b)
-            sum += value(b);
-        int incl = sum;
+        int st = 0, sc = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int nt = seq_tiles(b);
+            st += nt * Hkv;
+            sc += nt > 0 ? (nt + PC) * Hkv : 0;
+        }
+        int it = st, ic = sc;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(FULL_MASK, incl, off);
-            if (lane >= off)
-                incl += y;
+            const int y = __shfl_up_sync(FULL_MASK, it, off);
+            const int z = __shfl_up_sync(FULL_MASK, ic, off);
+            if (lane >= off) {
+                it += y;
+                ic += z;
+            }
         }
-        int *wsum = misc + 8;
-        if (lane == 31)
-            wsum[warp] = incl;
+        int *wsum = misc + 8;            // [8, 8 + NW) tiles, [20, 20 + NW) cost
+        if (lane == 31) {
+            wsum[warp] = it;
+            wsum[12 + warp] = ic;
+        }
         __syncthreads();
         if (warp == 0) {
-            int v = lane < (NTHREADS / 32) ? wsum[lane] : 0;
+            int v = lane < NW ? wsum[lane] : 0;
+            int u = lane < NW ? wsum[12 + lane] : 0;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const int y = __shfl_up_sync(FULL_MASK, v, off);
-                if (lane >= off)
+                const int z = __shfl_up_sync(FULL_MASK, u, off);
+                if (lane >= off) {
                     v += y;
+                    u += z;
+                }
             }
-            if (lane < (NTHREADS / 32))
+            if (lane < NW) {
                 wsum[lane] = v;
+                wsum[12 + lane] = u;
+            }
         }
         __syncthreads();
-        int base = (warp > 0 ? wsum[warp - 1] : 0) + incl - sum;
+        int bt = (warp > 0 ? wsum[warp - 1] : 0) + it - st;
+        int bc = (warp > 0 ? wsum[12 + warp - 1] : 0) + ic - sc;
+        const int t_all = wsum[NW - 1], c_all = wsum[12 + NW - 1];
+        const int p_all = (int)min((int64_t)gridDim.x, (int64_t)c_all);
+        // the cost positions where this CTA's share begins and ends
+        const int64_t cb[2] = {
+            blockIdx.x < p_all ? (int64_t)blockIdx.x * c_all / p_all : c_all,
+            blockIdx.x < p_all ? (int64_t)(blockIdx.x + 1) * c_all / p_all : c_all};
         for (int b = b0; b < b1; ++b) {
-            out[b] = base;
-            base += value(b);
+            const int nt = seq_tiles(b);
+            const int cost = nt > 0 ? (nt + PC) * Hkv : 0;
+            s_tstart[b] = bt;
+            s_cstart[b] = bc;
+            // a share boundary inside this sequence's cost -> tiles below it
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if (cb[e] >= bc && cb[e] < bc + cost) {
+                    const int rem = (int)(cb[e] - bc);
+                    const int kvh = rem / (nt + PC);
+                    const int in = rem - kvh * (nt + PC) - PC;
+                    s_range[e] = bt + kvh * nt + (in < 0 ? 0 : (in > nt ? nt : in));
+                }
+            }
+            bt += nt * Hkv;
+            bc += cost;
         }
-        if (tid == 0)
-            out[B] = wsum[NTHREADS / 32 - 1];
+        if (tid == 0) {
+            s_tstart[B] = t_all;
+            s_cstart[B] = c_all;
+            if (cb[0] >= c_all)
+                s_range[0] = t_all;
+            if (cb[1] >= c_all)
+                s_range[1] = t_all;
+        }
         __syncthreads();
-    };
-    // the prefix of tiles
-    block_scan([&](int b) { return seq_tiles(b) * Hkv; }, s_tstart);
-
-    // The T tiles are split over P = min(grid, T) CTAs, so that every CTA
-    // that takes part owns at least one tile and the CTAs holding pieces of
-    // one sequence/head are consecutive (the merge counts on both).
+    }
     const int64_t T = s_tstart[B];
-    const int P = (int)min((int64_t)gridDim.x, T);
+    const int64_t CT = s_cstart[B];
+    const int P = (int)min((int64_t)gridDim.x, CT);
     const int cta = blockIdx.x;
-    const int64_t R0 = cta < P ? (int64_t)cta * T / P : 0;
-    const int64_t R1 = cta < P ? (int64_t)(cta + 1) * T / P : 0;
+    // cost position of tile i of segment (b, kvh)
+    auto tile_cost = [&](int b, int kvh, int i) -> int64_t {
+        return (int64_t)s_cstart[b] + (int64_t)kvh * (seq_tiles(b) + PC) + PC + i;
+    };
+    const int64_t R0 = s_range[0];
+    const int64_t R1 = s_range[1];
     const int Hq = p.num_q_heads;
 
     if (warp == W) {
@@ -1090,13 +1158,43 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         const int GRP = min(32, p.nst);
         const uint64_t policy = policy_evict_first();
         struct Desc { int b, kvh, ti, nblk; int32_t id[4]; };
-        auto describe = [&](int k0) {
+        // Tile -> (sequence, KV head, tile of the sequence) for the group's
+        // consecutive tiles at once.  bh is a sequence at or before the
+        // group's first tile; lane j holds the j-th sequence boundary after
+        // it, and each lane counts the boundaries at or below its tile by a
+        // search over the lanes (shuffles, rather than a binary search whose
+        // every step waits on a shared-memory load).  More than 31
+        // boundaries in reach (runs of empty sequences) fall back to the
+        // binary search.
+        auto describe = [&](int k0, int bh) {
             Desc d{0, 0, 0, 0, {-1, -1, -1, -1}};
+            const int x = (int)(R0 + k0) + lane;
+            const int jb = bh + 1 + lane;
+            const int tj = jb <= B ? s_tstart[jb] : INT_MAX;
+            const int t_bh = s_tstart[bh];
+            int pos = 0;
+#pragma unroll
+            for (int step = 16; step >= 1; step >>= 1) {
+                const int t = __shfl_sync(FULL_MASK, tj, pos + step - 1);
+                if (t <= x)
+                    pos += step;
+            }
+            const int t_hi = __shfl_sync(FULL_MASK, tj, pos);
+            const int t_lo = __shfl_sync(FULL_MASK, tj, pos > 0 ? pos - 1 : 0);
+            const bool over = __shfl_sync(FULL_MASK, tj, 31) <= x;
             if (lane < GRP && k0 + lane < n_local) {
-                const int64_t x = R0 + k0 + lane;
-                d.b = find_seq(s_tstart, B, x);
-                const int nt = (s_tstart[d.b + 1] - s_tstart[d.b]) / Hkv;
-                const int off = (int)(x - s_tstart[d.b]);
+                int tb, tb1;
+                if (!over) {
+                    d.b = bh + pos;
+                    tb = pos > 0 ? t_lo : t_bh;
+                    tb1 = t_hi;
+                } else {
+                    d.b = find_seq(s_tstart, B, x);
+                    tb = s_tstart[d.b];
+                    tb1 = s_tstart[d.b + 1];
+                }
+                const int nt = (tb1 - tb) / Hkv;
+                const int off = x - tb;
                 d.kvh = off / nt;
                 d.ti = off - d.kvh * nt + s_lo[d.b] / TILE;
                 const int nvalid = min(TILE, s_len[d.b] - TILE * d.ti);
@@ -1113,10 +1211,10 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         long long seg_last = -1;                // (sequence, KV head) of the previous tile
         int qn_base = 0;                        // q copies issued before this group
         int st_base = 0, rnd_base = 0;          // stage and ring round of tile k0
-        Desc cur = describe(0);
+        Desc cur = describe(0, n_local > 0 ? find_seq(s_tstart, B, R0) : 0);
         for (int k0 = 0; k0 < n_local; k0 += GRP) {
-            const Desc nxt = describe(k0 + GRP);
             const int n = min(GRP, n_local - k0);
+            const Desc nxt = describe(k0 + GRP, __shfl_sync(FULL_MASK, cur.b, n - 1));
             const bool active = lane < n;
             const long long seg = active ? (long long)cur.b * Hkv + cur.kvh : -1;
             long long prev = __shfl_up_sync(FULL_MASK, seg, 1);
@@ -1324,14 +1422,14 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         }
 
         const int stride = G * (D + 2);   // floats of one partial
-        // Tiles [seg_begin, seg_end) of a (sequence, KV head) and the CTAs
-        // that own its first and last tile.
+        // The CTAs that own the first and last tile of a (sequence, KV
+        // head).
         struct SegSpan { int c_first, c_last; };
         auto seg_span = [&](int seg) {
             const int bq = seg / Hkv, kq = seg - (seg / Hkv) * Hkv;
-            const int nt = (s_tstart[bq + 1] - s_tstart[bq]) / Hkv;
-            const int64_t sb = (int64_t)s_tstart[bq] + (int64_t)kq * nt;
-            return SegSpan{owner_of(sb, T, P), owner_of(sb + nt - 1, T, P)};
+            const int nt = seq_tiles(bq);
+            return SegSpan{owner_of(tile_cost(bq, kq, 0), CT, P),
+                           owner_of(tile_cost(bq, kq, nt - 1), CT, P)};
         };
         // Merge the partials of CTAs c0..c1 of piece `seg`, in CTA order, for
         // output idx; CTA `own` (if any) contributes (own_m, own_num, own_den)
@@ -1441,10 +1539,15 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             }
 
             const int kfirst = k0 + (w - k0 % W + W) % W;
-            for (int k = kfirst; k < k1; k += W) {
-                // tile k sits in ring stage st = k mod nst, round rnd = k / nst
-                const int rnd = k / p.nst;
-                const int st = k - rnd * p.nst;
+            // tile k sits in ring stage st = k mod nst, round rnd = k / nst
+            // (stepped along with k rather than divided out per tile)
+            int rnd = kfirst / p.nst;
+            int st = kfirst - rnd * p.nst;
+            for (int k = kfirst; k < k1; k += W, st += W) {
+                while (st >= p.nst) {
+                    st -= p.nst;
+                    ++rnd;
+                }
                 const int ti = ti0 + (k - k0);
                 const int nvalid = min(TILE, L - TILE * ti);
                 const int tlo = lo - TILE * ti;          // > 0 only in the window's first tile
@@ -1657,8 +1760,8 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             }
             named_bar_sync(1, W * 32);
 
-            const int c_first = owner_of(seg_begin, T, P);
-            const int c_last = owner_of(seg_end - 1, T, P);
+            const int c_first = owner_of(tile_cost(b, kvh, 0), CT, P);
+            const int c_last = owner_of(tile_cost(b, kvh, nt - 1), CT, P);
             const bool whole = c_first == c_last;
             const bool last_piece = xe == R1;
             const int seg = b * Hkv + kvh;

@@ -266,6 +266,26 @@ __device__ __forceinline__ uint32_t i4pair_to_half2(uint32_t w, int k)
     return h;
 }
 
+// Codes at bits 4..7 and 20..23 of w -> an fp16 pair, exactly, without a
+// shift: the biased field lands 4 bits up in the mantissa of 1024, giving
+// 1024 + 16 (code + 8); times 1/16 minus 72 is the code (every step exact).
+__device__ __forceinline__ uint32_t i4pair_hi_to_half2(uint32_t w)
+{
+    const uint32_t t = (w & 0x00F000F0u) ^ 0x64806480u;
+    uint32_t h;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(h) : "r"(t), "r"(0x2C002C00u), "r"(0xD480D480u));
+    return h;
+}
+
+// Codes at bits 0..3 and 16..19 of w -> an fp16 pair, exactly.
+__device__ __forceinline__ uint32_t i4pair_lo_to_half2(uint32_t w)
+{
+    const uint32_t t = (w & 0x000F000Fu) ^ 0x64086408u;
+    uint32_t h;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(t), "r"(0x64086408u));
+    return h;
+}
+
 // The code in the low 4 bits of x -> float, exactly (biased code in the
 // mantissa of 2^23, minus 2^23 + 8).
 __device__ __forceinline__ float i4_to_float(uint32_t x)
