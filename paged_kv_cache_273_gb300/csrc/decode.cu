@@ -69,6 +69,25 @@ bool encode_swizzled_tile_map(CUtensorMap *map, const void *base, int row_bytes,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_gather_row_map(CUtensorMap *map, const void *base, int row_bytes, int rt,
+                           const pkv_pool *pool)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    const int bs = pool->block_size;
+    const int64_t rb = (int64_t)rt * row_bytes;
+    if (!enc || rt < 1 || bs % rt != 0 || rb % 16 != 0 || rb / 8 > 256)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)(rb / 8),
+                                (cuuint64_t)pool->num_blocks * pool->num_kv_heads * (bs / rt)};
+    const cuuint64_t strides[1] = {(cuuint64_t)rb};
+    const cuuint32_t box[2] = {(cuuint32_t)(rb / 8), 1};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_heads)
 {
     const int G = num_q_heads / pool->num_kv_heads;

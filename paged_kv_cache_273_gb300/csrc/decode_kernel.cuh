@@ -111,8 +111,17 @@ struct Cfg {
     static constexpr int NP = TPL * G;             // partial dots per lane
     static constexpr int NF = G >= 2 ? G / 2 : 1;  // scores per lane after reduction
     static constexpr int VE = D / 32;              // V elements per lane
-    static constexpr int KV_BYTES = TILE * ROWB;   // one tile of K (or V)
-    static constexpr int SC_BYTES = quantized(KV) ? TILE * 2 : 0;
+    // A work unit (what a stage holds and a consumer warp takes) is SUB
+    // tiles of one (sequence, KV head): 4 for 4-bit caches on the tensor
+    // cores, whose 16-token tiles are only 1 KB of K (a copy that small is
+    // bound by the copy unit's rate per copy, and by the producer's work
+    // per stage), else 1.
+    static constexpr int SUB = (KV == PKV_I4 && mma_path(KV, G)) ? 4 : 1;
+    static constexpr int TT = TILE * SUB;          // tokens per unit
+    static constexpr int KV_BYTES = TT * ROWB;     // one unit of K (or V)
+    static constexpr int SC_BYTES = quantized(KV) ? TT * 2 : 0;
+    // block-table ids (or gathered rows) a producer lane holds per unit
+    static constexpr int NIDS = SUB > 1 ? 8 : 4;
     // a stage: the tile's K then V (the scales ride in a ring of their own,
     // so that every stage starts on a 1024-byte boundary)
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;
@@ -199,12 +208,18 @@ __host__ __device__ inline Layout make_layout(int nst, int batch, bool prefix)
     return L;
 }
 
-// The end of a piece (its warps' states merged, the result written) costs
-// about as much as this many tiles, the more the more heads it merges
-// (measured on GB300: about 1.4 us a piece at G = 4 and 3 us at G = 8,
-// against 0.15-0.17 us a tile).  The split over CTAs charges it, so that a
-// CTA whose share holds many short sequences gets fewer tiles.
-__host__ __device__ constexpr int piece_cost(int G) { return 2 + 2 * G; }
+// The end of a piece (the warps wait for the last of them, merge their
+// states and write the result) costs about as much as this many work units;
+// the split over CTAs charges it, so that a CTA whose share holds many short
+// sequences gets fewer units.  Set from timings on GB300 of the workload
+// shapes (one KV head's piece end against its units): about 1.4 us a piece
+// at G = 4 and 3 us at G = 8 against 0.15-0.17 us a 16-token tile; more, in
+// units, at G = 1 (cheap tiles) and with 64-token units (a warp that ends
+// a piece late holds the others back by up to a whole unit).
+__host__ __device__ constexpr int piece_cost(int G, int sub = 1)
+{
+    return sub > 1 ? 12 + (2 + 2 * G) / sub : (G == 1 ? 16 : 2 + 2 * G);
+}
 
 // Owner CTA of global tile x when T tiles are split evenly over P CTAs:
 // CTA c owns [floor(c*T/P), floor((c+1)*T/P)).
@@ -572,6 +587,28 @@ __device__ __forceinline__ uint32_t swz_off(uint32_t off, bool swz)
     return swz ? off ^ ((off >> 3) & 0x70u) : off;
 }
 
+// Tokens per row of the gather view of the caches for units of tt tokens:
+// a block's tokens, at most 16, at most a quarter unit (so that a unit is
+// four or eight rows).
+__host__ __device__ constexpr int gather_row_tokens(int bs, int tt)
+{
+    return bs < TILE ? (bs < tt / 4 ? bs : tt / 4) : (TILE < tt / 4 ? TILE : tt / 4);
+}
+
+// Four rows of a 2-D view of a cache (x = 0, rows r0..r3) as one gather copy
+// into shared memory at dst, laid out one after another; completion is
+// counted in bytes on the mbarrier.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, int r0, int r1,
+                                            int r2, int r3, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(smem_addr(bar))
+        : "memory");
+}
+
 // ---- tile math on the tensor cores (warp-level MMA) --------------------------
 //
 // For 16-bit, 8-bit and 4-bit caches a warp does a tile's two products as
@@ -736,7 +773,8 @@ template <int D, int G, int KV, bool QS>
 __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsigned char *sK,
                                          const unsigned char *sV, const __half *sKS,
                                          const __half *sVS, int nvalid, int tlo, float scale_log2,
-                                         int lane, uint64_t *empty_bar, int swz)
+                                         int lane, uint64_t *empty_bar, int swz,
+                                         bool release = true)
 {
     using M = MmaCfg<D, KV>;
     constexpr bool BF = MmaBf16<KV>::v;
@@ -855,9 +893,11 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
         vs0 = __half2float(sVS[gid]);
         vs1 = __half2float(sVS[gid + 8]);
     }
-    __syncwarp();
-    if (lane == 0)
-        mbar_arrive(empty_bar);
+    if (release) {
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty_bar);
+    }
 
     // ---- online softmax (log2 domain) of heads 2tig, 2tig+1 over tokens
     // gid, gid+8 of this lane; the other lanes of the head differ in gid
@@ -1038,7 +1078,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     // Tiles of sequence b: from the one holding its first attended row to the
     // one holding its last (none when no row is left to attend).
     auto seq_tiles = [&](int b) {
-        return s_len[b] > s_lo[b] ? (s_len[b] + TILE - 1) / TILE - s_lo[b] / TILE : 0;
+        return s_len[b] > s_lo[b] ? (s_len[b] + C::TT - 1) / C::TT - s_lo[b] / C::TT : 0;
     };
     // One pass over the sequences (thread t takes a contiguous run, then
     // warp and block scans): the exclusive prefixes of tiles (s_tstart) and
@@ -1051,7 +1091,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
     // consecutive, and each CTA between the owners of a segment's first and
     // last tile owns a tile of it (tile positions are consecutive there), as
     // the merge counts on.
-    constexpr int PC = piece_cost(G);
+    constexpr int PC = piece_cost(G, C::SUB);
     constexpr int NW = NTHREADS / 32;
     static_assert(NW <= 12, "scan scratch: misc[8, 32)");
     int *s_range = reinterpret_cast<int *>(smem + lay.merge);   // free until the first merge
@@ -1157,7 +1197,9 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         const int bs = p.block_size;
         const int GRP = min(32, p.nst);
         const uint64_t policy = policy_evict_first();
-        struct Desc { int b, kvh, ti, nblk; int32_t id[4]; };
+        // (with units of several tiles, id[] holds the unit's rows in the
+        // gather view of the caches, and nblk the rows holding tokens)
+        struct Desc { int b, kvh, ti, nblk; int32_t id[C::NIDS]; };
         // Tile -> (sequence, KV head, tile of the sequence) for the group's
         // consecutive tiles at once.  bh is a sequence at or before the
         // group's first tile; lane j holds the j-th sequence boundary after
@@ -1167,7 +1209,11 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         // boundaries in reach (runs of empty sequences) fall back to the
         // binary search.
         auto describe = [&](int k0, int bh) {
-            Desc d{0, 0, 0, 0, {-1, -1, -1, -1}};
+            Desc d;
+            d.b = d.kvh = d.ti = d.nblk = 0;
+#pragma unroll
+            for (int i = 0; i < C::NIDS; ++i)
+                d.id[i] = -1;
             const int x = (int)(R0 + k0) + lane;
             const int jb = bh + 1 + lane;
             const int tj = jb <= B ? s_tstart[jb] : INT_MAX;
@@ -1196,15 +1242,34 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 const int nt = (tb1 - tb) / Hkv;
                 const int off = x - tb;
                 d.kvh = off / nt;
-                d.ti = off - d.kvh * nt + s_lo[d.b] / TILE;
-                const int nvalid = min(TILE, s_len[d.b] - TILE * d.ti);
+                d.ti = off - d.kvh * nt + s_lo[d.b] / C::TT;
+                const int nvalid = min(C::TT, s_len[d.b] - C::TT * d.ti);
                 const int32_t *row = p.block_tables + (int64_t)d.b * p.max_blocks_per_seq;
-                const int first = (TILE * d.ti) >> p.bs_log2;
-                d.nblk = bs >= TILE ? 1 : (nvalid + bs - 1) >> p.bs_log2;   // 1..4 (bs >= 4)
-                d.id[0] = __ldg(row + first);
-                if (d.nblk > 1) d.id[1] = __ldg(row + first + 1);
-                if (d.nblk > 2) d.id[2] = __ldg(row + first + 2);
-                if (d.nblk > 3) d.id[3] = __ldg(row + first + 3);
+                if constexpr (C::SUB > 1) {
+                    // rows of rt tokens; rows past the last token repeat the
+                    // last row with tokens; a block id out of range gives -1
+                    // (read as row 0, the error word set)
+                    const int rt = gather_row_tokens(bs, C::TT);
+                    const int nr = C::TT / rt;
+                    d.nblk = (nvalid + rt - 1) / rt;
+#pragma unroll
+                    for (int r = 0; r < C::NIDS; ++r) {
+                        if (r < nr) {
+                            const int tok = C::TT * d.ti + (r < d.nblk ? r : d.nblk - 1) * rt;
+                            const int blk = __ldg(row + (tok >> p.bs_log2));
+                            d.id[r] = (blk >= 0 && blk < p.num_blocks)
+                                          ? (blk * Hkv + d.kvh) * (bs / rt) + (tok & (bs - 1)) / rt
+                                          : -1;
+                        }
+                    }
+                } else {
+                    const int first = (TILE * d.ti) >> p.bs_log2;
+                    d.nblk = bs >= TILE ? 1 : (nvalid + bs - 1) >> p.bs_log2;   // 1..4 (bs >= 4)
+                    d.id[0] = __ldg(row + first);
+                    if (d.nblk > 1) d.id[1] = __ldg(row + first + 1);
+                    if (d.nblk > 2) d.id[2] = __ldg(row + first + 2);
+                    if (d.nblk > 3) d.id[3] = __ldg(row + first + 3);
+                }
             }
             return d;
         };
@@ -1265,6 +1330,46 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     unsigned char *sV = sK + C::KV_BYTES;
                     unsigned char *sKS = scale_ring + st * 2 * C::SC_BYTES;
                     unsigned char *sVS = sKS + C::SC_BYTES;
+                    if constexpr (C::SUB > 1) {
+                    // A unit: its rows of rt tokens gathered four at a time
+                    // from the 2-D views of the caches (rows of rt * ROWB
+                    // bytes), the scales of the rows with tokens by cp.async.
+                    const int rt = gather_row_tokens(bs, C::TT);
+                    const int nr = C::TT / rt;
+                    bool bad = false;
+#pragma unroll
+                    for (int r = 0; r < C::NIDS; ++r)
+                        bad |= r < nr && cur.id[r] < 0;
+                    if (bad)
+                        atomicOr(p.err, PKV_EBIT_BLOCK);
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)(2 * C::KV_BYTES));
+                    reinterpret_cast<volatile int *>(misc)[MISC_ISSUED + st] = rnd + 1;
+                    const int rb = rt * C::ROWB;
+#pragma unroll
+                    for (int g4 = 0; g4 < C::NIDS / 4; ++g4) {
+                        if (4 * g4 < nr) {
+                            const int r0 = max(cur.id[4 * g4], 0), r1 = max(cur.id[4 * g4 + 1], 0);
+                            const int r2 = max(cur.id[4 * g4 + 2], 0), r3 = max(cur.id[4 * g4 + 3], 0);
+                            tma_gather4(sK + 4 * g4 * rb, &p.tm_k, r0, r1, r2, r3, &full[st]);
+                            tma_gather4(sV + 4 * g4 * rb, &p.tm_v, r0, r1, r2, r3, &full[st]);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < C::NIDS; ++r) {
+                        if (r < cur.nblk && cur.id[r] >= 0) {
+                            // scales of row r: rt halves at element id * rt
+                            const unsigned char *ksrc =
+                                reinterpret_cast<const unsigned char *>(p.k_scales + (int64_t)cur.id[r] * rt);
+                            const unsigned char *vsrc =
+                                reinterpret_cast<const unsigned char *>(p.v_scales + (int64_t)cur.id[r] * rt);
+                            for (int o = 0; o < rt * 2; o += 16) {
+                                cp_async_16b(sKS + r * rt * 2 + o, ksrc + o);
+                                cp_async_16b(sVS + r * rt * 2 + o, vsrc + o);
+                            }
+                        }
+                    }
+                    cp_async_mbar_arrive(&full[st]);
+                    } else {
                     const int rows_per_copy = bs >= TILE ? TILE : bs;
                     const uint32_t kv_copy = (uint32_t)(rows_per_copy * C::ROWB);
                     const int sc_copy = rows_per_copy * 2;
@@ -1340,6 +1445,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     }
                     if constexpr (quantized(KV))
                         cp_async_mbar_arrive(&full[st]);
+                    }
                         t_done = true;
                     }
                     if (__all_sync(FULL_MASK, q_done && t_done))
@@ -1477,7 +1583,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
             const int nt = (s_tstart[b + 1] - s_tstart[b]) / Hkv;
             const int off = (int)(x - s_tstart[b]);
             const int kvh = off / nt;
-            const int ti0 = off - kvh * nt + s_lo[b] / TILE;   // tile index in the sequence
+            const int ti0 = off - kvh * nt + s_lo[b] / C::TT;   // unit index in the sequence
             const int64_t seg_begin = (int64_t)s_tstart[b] + (int64_t)kvh * nt;
             const int64_t seg_end = seg_begin + nt;
             const int64_t xe = min(seg_end, R1);
@@ -1549,8 +1655,8 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     ++rnd;
                 }
                 const int ti = ti0 + (k - k0);
-                const int nvalid = min(TILE, L - TILE * ti);
-                const int tlo = lo - TILE * ti;          // > 0 only in the window's first tile
+                const int nvalid = min(C::TT, L - C::TT * ti);
+                const int tlo = lo - C::TT * ti;         // > 0 only in the window's first unit
                 // Warps take tiles round-robin and may drift apart, so this
                 // warp can reach tile k while the stage's previous tile
                 // (k - stages) is still landing; a parity wait alone would
@@ -1569,8 +1675,20 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 const unsigned char *sV = sK + C::KV_BYTES;
                 const __half *sKS =
                     reinterpret_cast<const __half *>(scale_ring + st * 2 * C::SC_BYTES);
-                const __half *sVS = sKS + TILE;
-                if constexpr (C::MMA) {
+                const __half *sVS = sKS + C::TT;
+                if constexpr (C::SUB > 1) {
+                    // the unit's 16-token tiles that hold attended tokens, in
+                    // order; the last one hands the stage back
+                    const int i0 = tlo > 0 ? tlo / TILE : 0;
+                    const int i1 = (nvalid + TILE - 1) / TILE;
+#pragma unroll 1
+                    for (int i = i0; i < i1; ++i)
+                        mma_tile<D, G, KV, QS>(mst, sK + i * C::KV_BYTES / C::SUB,
+                                               sV + i * C::KV_BYTES / C::SUB, sKS + i * TILE,
+                                               sVS + i * TILE, min(TILE, nvalid - i * TILE),
+                                               tlo - i * TILE, p.scale_log2, lane, &empty[st], 0,
+                                               i == i1 - 1);
+                } else if constexpr (C::MMA) {
                     mma_tile<D, G, KV, QS>(mst, sK, sV, sKS, sVS, nvalid, tlo, p.scale_log2,
                                            lane, &empty[st], swz);
                 } else {
@@ -1900,6 +2018,13 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
     // Tiles of the tensor-core tile math come by swizzled tensor copies when
     // a tile is 16 rows of one block (block size >= 16).
     prm.swz = 0;
+    if constexpr (C::SUB > 1) {
+        // units gather rows of min(bs, 16) tokens from 2-D views of the caches
+        const int rt = gather_row_tokens(pool->block_size, C::TT);
+        if (!encode_gather_row_map(&prm.tm_k, prm.k_cache, C::ROWB, rt, pool) ||
+            !encode_gather_row_map(&prm.tm_v, prm.v_cache, C::ROWB, rt, pool))
+            return PKV_ERR_CUDA;
+    }
     if constexpr (C::SWIZZLE_OK) {
         if (pool->block_size >= TILE) {
             if (!encode_swizzled_tile_map(&prm.tm_k, prm.k_cache, C::ROWB, pool) ||
@@ -1926,7 +2051,7 @@ int launch_t(const pkv_pool *pool, const Params &base, int batch, int max_seq_le
                              cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) != cudaSuccess)
         return PKV_ERR_CUDA;
     const int64_t max_tiles =
-        (int64_t)batch * pool->num_kv_heads * ((max_seq_len + TILE - 1) / TILE);
+        (int64_t)batch * pool->num_kv_heads * ((max_seq_len + C::TT - 1) / C::TT);
     int64_t P = pool->num_sms;
     if (P > max_tiles)
         P = max_tiles;

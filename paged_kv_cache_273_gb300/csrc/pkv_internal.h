@@ -128,6 +128,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 bool encode_swizzled_tile_map(CUtensorMap *map, const void *base, int row_bytes,
                               const pkv_pool *pool);
 
+// A cache [NB][Hkv][bs][row_bytes] as a 2-D tensor of rows of rt cached
+// rows each (rt divides bs; 8-byte elements), boxes of one such row, for
+// four-row gather copies.  False if the encoder is unavailable or refuses.
+bool encode_gather_row_map(CUtensorMap *map, const void *base, int row_bytes, int rt,
+                           const pkv_pool *pool);
+
 // seq_prefix / prefix_part: shared-prefix decode (null: none), see Params.
 int launch_decode(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
                   const void *k_cache, const void *v_cache, const void *k_scales,

@@ -1,7 +1,8 @@
 """A model of how the decode kernel splits a batch's tiles over its CTAs.
 
-Each (sequence, KV head) segment costs PC = 2 + 2G units for its piece end
-followed by one unit per 16-token tile; the total cost is split evenly over
+Each (sequence, KV head) segment costs PC units for its piece end (a
+constant of the kernel's configuration) followed by one unit per work unit
+of tiles; the total cost is split evenly over
 P = min(grid, cost) CTAs and a CTA owns the tiles whose cost position falls
 in its share.  The kernel finds a CTA's first and last tile from the cost
 prefix in one pass, and the owner of a tile (for the cross-CTA merge counts)
@@ -25,8 +26,7 @@ def owner_of(x, total, parts):
     return ((x + 1) * parts - 1) // total
 
 
-def split(nts, hkv, g, grid):
-    pc = 2 + 2 * g
+def split(nts, hkv, pc, grid):
     ts, cs = [0], [0]
     for nt in nts:
         ts.append(ts[-1] + nt * hkv)
@@ -55,10 +55,10 @@ def test_split_invariants():
         rng = random.Random(trial)
         B = rng.randint(1, 30)
         hkv = rng.choice([1, 2, 4, 8])
-        g = rng.choice([1, 2, 4, 8])
+        pc = rng.choice([1, 2, 6, 10, 16, 18])
         grid = rng.choice([1, 2, 5, 16, 152])
         nts = [rng.choice([0, 0, 1, 2, 3, 5, 17, 100, 400]) for _ in range(B)]
-        ts, cs, T, CT, P, pc, ranges = split(nts, hkv, g, grid)
+        ts, cs, T, CT, P, pc, ranges = split(nts, hkv, pc, grid)
         if T == 0:
             continue
         # a partition in order
@@ -84,6 +84,6 @@ def test_split_charges_piece_ends():
     # 8 long sequences and 64 one-tile ones: CTAs that take the short ones
     # take fewer tiles than an even split of tiles would give them
     nts = [400] * 8 + [1] * 64
-    ts, cs, T, CT, P, pc, ranges = split(nts, 8, 8, 16)
+    ts, cs, T, CT, P, pc, ranges = split(nts, 8, 18, 16)
     sizes = [r1 - r0 for r0, r1 in ranges]
     assert max(sizes) > T // 16 > min(sizes)
