@@ -112,11 +112,11 @@ struct Cfg {
     static constexpr int NF = G >= 2 ? G / 2 : 1;  // scores per lane after reduction
     static constexpr int VE = D / 32;              // V elements per lane
     // A work unit (what a stage holds and a consumer warp takes) is SUB
-    // tiles of one (sequence, KV head): 4 for 4-bit caches on the tensor
-    // cores, whose 16-token tiles are only 1 KB of K (a copy that small is
-    // bound by the copy unit's rate per copy, and by the producer's work
-    // per stage), else 1.
-    static constexpr int SUB = (KV == PKV_I4 && mma_path(KV, G)) ? 4 : 1;
+    // tiles of one (sequence, KV head): on the tensor cores 4 for 4-bit and
+    // 2 for 8-bit caches, whose 16-token tiles are only 1 or 2 KB of K (so
+    // many small copies are bound by the copy unit's rate per copy and by
+    // the producer's work per stage), else 1.
+    static constexpr int SUB = !mma_path(KV, G) ? 1 : KV == PKV_I4 ? 4 : KV == PKV_I8 ? 2 : 1;
     static constexpr int TT = TILE * SUB;          // tokens per unit
     static constexpr int KV_BYTES = TT * ROWB;     // one unit of K (or V)
     static constexpr int SC_BYTES = quantized(KV) ? TT * 2 : 0;
@@ -126,11 +126,12 @@ struct Cfg {
     // so that every stage starts on a 1024-byte boundary)
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;
     // The tensor-core tile math reads rows of 128 or 256 bytes through the
-    // 128-byte swizzle: with blocks of >= 16 rows its K/V tiles come by
-    // tensor copies that lay them out swizzled (16-byte chunk j of a
+    // 128-byte swizzle: with blocks of >= 16 rows its one-tile stages come
+    // by tensor copies that lay them out swizzled (16-byte chunk j of a
     // 128-byte segment s at j ^ (s mod 8)), which spreads the fragment loads
-    // over the banks.
-    static constexpr bool SWIZZLE_OK = mma_path(KV, G) && (ROWB == 128 || ROWB == 256);
+    // over the banks.  (The units' gathered rows are wider than the
+    // swizzle's 128-byte span, so they stay plain.)
+    static constexpr bool SWIZZLE_OK = mma_path(KV, G) && (ROWB == 128 || ROWB == 256) && SUB == 1;
     static constexpr int QSLOT = round_up(G * D * 4, 128);   // fits any q dtype
     static constexpr int MERGE_FLOATS = W * G * (D + 2);
     // per warp (CUDA-core tile math only): {p, p} pairs of the tile
@@ -218,7 +219,7 @@ __host__ __device__ inline Layout make_layout(int nst, int batch, bool prefix)
 // a piece late holds the others back by up to a whole unit).
 __host__ __device__ constexpr int piece_cost(int G, int sub = 1)
 {
-    return sub > 1 ? 12 + (2 + 2 * G) / sub : (G == 1 ? 16 : 2 + 2 * G);
+    return sub > 1 ? (sub == 4 ? 12 : 10) + (2 + 2 * G) / sub : (G == 1 ? 16 : 2 + 2 * G);
 }
 
 // Owner CTA of global tile x when T tiles are split evenly over P CTAs:
