@@ -115,8 +115,10 @@ struct Cfg {
     // tiles of one (sequence, KV head): on the tensor cores 4 for 4-bit and
     // 2 for 8-bit caches, whose 16-token tiles are only 1 or 2 KB of K (so
     // many small copies are bound by the copy unit's rate per copy and by
-    // the producer's work per stage), else 1.
-    static constexpr int SUB = !mma_path(KV, G) ? 1 : KV == PKV_I4 ? 4 : KV == PKV_I8 ? 2 : 1;
+    // the producer's work per stage); on the CUDA cores 2 for tiles of at
+    // most 2 KB; else 1.
+    static constexpr int SUB = mma_path(KV, G) ? (KV == PKV_I4 ? 4 : KV == PKV_I8 ? 2 : 1)
+                                               : (KV != PKV_F32 && TILE * ROWB <= 2048 ? 2 : 1);
     static constexpr int TT = TILE * SUB;          // tokens per unit
     static constexpr int KV_BYTES = TT * ROWB;     // one unit of K (or V)
     static constexpr int SC_BYTES = quantized(KV) ? TT * 2 : 0;
@@ -1247,16 +1249,21 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 const int nvalid = min(C::TT, s_len[d.b] - C::TT * d.ti);
                 const int32_t *row = p.block_tables + (int64_t)d.b * p.max_blocks_per_seq;
                 if constexpr (C::SUB > 1) {
-                    // rows of rt tokens; rows past the last token repeat the
-                    // last row with tokens; a block id out of range gives -1
-                    // (read as row 0, the error word set)
+                    // rows of rt tokens; rows before the first attended
+                    // token (a window's or a suffix's start) and past the
+                    // last token repeat the nearest row with attended tokens,
+                    // so that no other block is looked up; a block id out of
+                    // range gives -1 (read as row 0, the error word set)
                     const int rt = gather_row_tokens(bs, C::TT);
                     const int nr = C::TT / rt;
                     d.nblk = (nvalid + rt - 1) / rt;
+                    const int lead = s_lo[d.b] - C::TT * d.ti;
+                    const int r_lo = lead > 0 ? lead / rt : 0;
 #pragma unroll
                     for (int r = 0; r < C::NIDS; ++r) {
                         if (r < nr) {
-                            const int tok = C::TT * d.ti + (r < d.nblk ? r : d.nblk - 1) * rt;
+                            const int rr = r < r_lo ? r_lo : (r < d.nblk ? r : d.nblk - 1);
+                            const int tok = C::TT * d.ti + rr * rt;
                             const int blk = __ldg(row + (tok >> p.bs_log2));
                             d.id[r] = (blk >= 0 && blk < p.num_blocks)
                                           ? (blk * Hkv + d.kvh) * (bs / rt) + (tok & (bs - 1)) / rt
@@ -1355,21 +1362,23 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                             tma_gather4(sV + 4 * g4 * rb, &p.tm_v, r0, r1, r2, r3, &full[st]);
                         }
                     }
+                    if constexpr (quantized(KV)) {
 #pragma unroll
-                    for (int r = 0; r < C::NIDS; ++r) {
-                        if (r < cur.nblk && cur.id[r] >= 0) {
-                            // scales of row r: rt halves at element id * rt
-                            const unsigned char *ksrc =
-                                reinterpret_cast<const unsigned char *>(p.k_scales + (int64_t)cur.id[r] * rt);
-                            const unsigned char *vsrc =
-                                reinterpret_cast<const unsigned char *>(p.v_scales + (int64_t)cur.id[r] * rt);
-                            for (int o = 0; o < rt * 2; o += 16) {
-                                cp_async_16b(sKS + r * rt * 2 + o, ksrc + o);
-                                cp_async_16b(sVS + r * rt * 2 + o, vsrc + o);
+                        for (int r = 0; r < C::NIDS; ++r) {
+                            if (r < cur.nblk && cur.id[r] >= 0) {
+                                // scales of row r: rt halves at element id * rt
+                                const unsigned char *ksrc = reinterpret_cast<const unsigned char *>(
+                                    p.k_scales + (int64_t)cur.id[r] * rt);
+                                const unsigned char *vsrc = reinterpret_cast<const unsigned char *>(
+                                    p.v_scales + (int64_t)cur.id[r] * rt);
+                                for (int o = 0; o < rt * 2; o += 16) {
+                                    cp_async_16b(sKS + r * rt * 2 + o, ksrc + o);
+                                    cp_async_16b(sVS + r * rt * 2 + o, vsrc + o);
+                                }
                             }
                         }
+                        cp_async_mbar_arrive(&full[st]);
                     }
-                    cp_async_mbar_arrive(&full[st]);
                     } else {
                     const int rows_per_copy = bs >= TILE ? TILE : bs;
                     const uint32_t kv_copy = (uint32_t)(rows_per_copy * C::ROWB);
@@ -1677,7 +1686,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                 const __half *sKS =
                     reinterpret_cast<const __half *>(scale_ring + st * 2 * C::SC_BYTES);
                 const __half *sVS = sKS + C::TT;
-                if constexpr (C::SUB > 1) {
+                if constexpr (C::MMA && C::SUB > 1) {
                     // the unit's 16-token tiles that hold attended tokens, in
                     // order; the last one hands the stage back
                     const int i0 = tlo > 0 ? tlo / TILE : 0;
@@ -1693,141 +1702,163 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     mma_tile<D, G, KV, QS>(mst, sK, sV, sKS, sVS, nvalid, tlo, p.scale_log2,
                                            lane, &empty[st], swz);
                 } else {
-                    // After the reduction below the lane holds token t, heads g0 + r.
-                    const int t = tq + C::TQ * (ds >> 1);
-                    const int g0 = G >= 2 ? (G / 2) * (ds & 1) : 0;
+                    // one 16-token tile on the CUDA cores; `release` hands the
+                    // stage back after it
+                    auto cc_tile = [&](const unsigned char *sK, const unsigned char *sV,
+                                       const __half *sKS, const __half *sVS, int nvalid, int tlo,
+                                       bool release) {
+                        // After the reduction below the lane holds token t, heads g0 + r.
+                        const int t = tq + C::TQ * (ds >> 1);
+                        const int g0 = G >= 2 ? (G / 2) * (ds & 1) : 0;
 
-                    // ---- take this lane's part of the tile into registers and hand
-                    // the stage back at once, so that the next copy into it starts
-                    // while this warp computes
-                    uint4 kr[C::TPL][C::CPL];
-                    load_k<D, G, KV>(kr, sK, tq, ds);
-                    float ks_t = 1.0f, vs_t = 1.0f;
-                    if constexpr (quantized(KV)) {
-                        ks_t = __half2float(sKS[t]);
-                        vs_t = __half2float(sVS[t]);
-                    }
-                    // (with G = 8 the heads' accumulators need the registers; V is
-                    // then read from the stage, which is released after P.V)
-                    constexpr bool VREG = VRaw<D, KV>::IN_REGS && G <= 4;
-                    typename VRaw<D, KV>::type vr[TILE];
-                    if constexpr (VREG) {
-    #pragma unroll
-                        for (int tt = 0; tt < TILE; ++tt)
-                            vr[tt] = load_v_raw<D, KV>(sV, tt, lane);
+                        // ---- take this lane's part of the tile into registers and hand
+                        // the stage back at once, so that the next copy into it starts
+                        // while this warp computes
+                        uint4 kr[C::TPL][C::CPL];
+                        load_k<D, G, KV>(kr, sK, tq, ds);
+                        float ks_t = 1.0f, vs_t = 1.0f;
+                        if constexpr (quantized(KV)) {
+                            ks_t = __half2float(sKS[t]);
+                            vs_t = __half2float(sVS[t]);
+                        }
+                        // (with G = 8 the heads' accumulators need the registers; V is
+                        // then read from the stage, which is released after P.V)
+                        constexpr bool VREG = VRaw<D, KV>::IN_REGS && G <= 4;
+                        typename VRaw<D, KV>::type vr[TILE];
+                        if constexpr (VREG) {
+        #pragma unroll
+                            for (int tt = 0; tt < TILE; ++tt)
+                                vr[tt] = load_v_raw<D, KV>(sV, tt, lane);
+                            if (release) {
+                                __syncwarp();
+                                if (lane == 0)
+                                    mbar_arrive(&empty[st]);
+                            }
+                        }
+
+                        // ---- scores: partial dots, then reduce-scatter over the DS lanes
+                        float part[C::NP];
+        #pragma unroll
+                        for (int j = 0; j < C::NP; ++j)
+                            part[j] = 0.0f;
+                        qk_tile<D, G, KV>(part, qr, kr);
+                        reduce_scatter<C::NP, C::DS / 2>(part, ds);
+                        float s[C::NF];
+                        float kscale = p.scale_log2;
+                        if constexpr (quantized(KV))
+                            kscale *= ks_t;
+                        bool above = false;
+        #pragma unroll
+                        for (int r = 0; r < C::NF; ++r) {
+                            s[r] = (t < nvalid && t >= tlo) ? part[r] * kscale : -INFINITY;
+                            above |= s[r] > m_run[r];
+                        }
+                        // The running maximum only needs to move when some score
+                        // exceeds it (softmax is shift invariant, so any running value
+                        // that is one of the scores seen is exact); most tiles skip
+                        // the per-head maximum and the rescale.
+                        const bool moved = __any_sync(FULL_MASK, above);
+                        float corr[C::NF];
+                        if (moved) {
+        #pragma unroll
+                            for (int r = 0; r < C::NF; ++r) {
+                                float mx = s[r];
+        #pragma unroll
+                                for (int mask = 2; mask < 32; mask <<= 1)
+                                    mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, mask));
+                                const float mnew = fmaxf(m_run[r], mx);   // finite: a valid token
+                                corr[r] = exp2_approx(m_run[r] - mnew);
+                                l_run[r] *= corr[r];
+                                m_run[r] = mnew;
+                            }
+                        }
+                        float pr[C::NF];
+        #pragma unroll
+                        for (int r = 0; r < C::NF; ++r) {
+                            pr[r] = exp2_approx(s[r] - m_run[r]);
+                            l_run[r] += pr[r];
+                        }
+                        // Publish {p, p} pairs (p times the V scale for int8) and, when
+                        // the maximum moved, the rescale factors.
+                        if (G >= 2 || (ds & 1) == 0) {
+                            const float vsc = vs_t;
+                            float2 *pp = reinterpret_cast<float2 *>(ps + t * 2 * G) + g0;
+        #pragma unroll
+                            for (int r = 0; r < C::NF; ++r) {
+                                const float v = pr[r] * vsc;
+                                pp[r] = make_float2(v, v);
+                            }
+                            if (moved && tq == 0 && (ds >> 1) == 0) {
+        #pragma unroll
+                                for (int r = 0; r < C::NF; ++r)
+                                    ps[TILE * 2 * G + g0 + r] = corr[r];
+                            }
+                        }
                         __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(&empty[st]);
-                    }
 
-                    // ---- scores: partial dots, then reduce-scatter over the DS lanes
-                    float part[C::NP];
-    #pragma unroll
-                    for (int j = 0; j < C::NP; ++j)
-                        part[j] = 0.0f;
-                    qk_tile<D, G, KV>(part, qr, kr);
-                    reduce_scatter<C::NP, C::DS / 2>(part, ds);
-                    float s[C::NF];
-                    float kscale = p.scale_log2;
-                    if constexpr (quantized(KV))
-                        kscale *= ks_t;
-                    bool above = false;
-    #pragma unroll
-                    for (int r = 0; r < C::NF; ++r) {
-                        s[r] = (t < nvalid && t >= tlo) ? part[r] * kscale : -INFINITY;
-                        above |= s[r] > m_run[r];
-                    }
-                    // The running maximum only needs to move when some score
-                    // exceeds it (softmax is shift invariant, so any running value
-                    // that is one of the scores seen is exact); most tiles skip
-                    // the per-head maximum and the rescale.
-                    const bool moved = __any_sync(FULL_MASK, above);
-                    float corr[C::NF];
-                    if (moved) {
-    #pragma unroll
-                        for (int r = 0; r < C::NF; ++r) {
-                            float mx = s[r];
-    #pragma unroll
-                            for (int mask = 2; mask < 32; mask <<= 1)
-                                mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, mask));
-                            const float mnew = fmaxf(m_run[r], mx);   // finite: a valid token
-                            corr[r] = exp2_approx(m_run[r] - mnew);
-                            l_run[r] *= corr[r];
-                            m_run[r] = mnew;
+                        // ---- weighted V
+                        if (moved) {
+        #pragma unroll
+                            for (int g = 0; g < G; ++g) {
+                                const float cg = ps[TILE * 2 * G + g];
+        #pragma unroll
+                                for (int e = 0; e < C::VE; ++e)
+                                    acc[g][e] *= cg;
+                            }
                         }
-                    }
-                    float pr[C::NF];
-    #pragma unroll
-                    for (int r = 0; r < C::NF; ++r) {
-                        pr[r] = exp2_approx(s[r] - m_run[r]);
-                        l_run[r] += pr[r];
-                    }
-                    // Publish {p, p} pairs (p times the V scale for int8) and, when
-                    // the maximum moved, the rescale factors.
-                    if (G >= 2 || (ds & 1) == 0) {
-                        const float vsc = vs_t;
-                        float2 *pp = reinterpret_cast<float2 *>(ps + t * 2 * G) + g0;
-    #pragma unroll
-                        for (int r = 0; r < C::NF; ++r) {
-                            const float v = pr[r] * vsc;
-                            pp[r] = make_float2(v, v);
-                        }
-                        if (moved && tq == 0 && (ds >> 1) == 0) {
-    #pragma unroll
-                            for (int r = 0; r < C::NF; ++r)
-                                ps[TILE * 2 * G + g0 + r] = corr[r];
-                        }
-                    }
-                    __syncwarp();
-
-                    // ---- weighted V
-                    if (moved) {
-    #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float cg = ps[TILE * 2 * G + g];
-    #pragma unroll
-                            for (int e = 0; e < C::VE; ++e)
-                                acc[g][e] *= cg;
-                        }
-                    }
-                    auto pv_token = [&](int tt) {
-                        float v[C::VE];
-                        if constexpr (VREG)
-                            unpack_v<D, KV>(v, vr[tt]);
-                        else
-                            load_v<D, KV>(v, sV, tt, lane);
-                        const float *pt = ps + tt * 2 * G;
-                        if constexpr (G == 1) {
-                            const float2 w2 = *reinterpret_cast<const float2 *>(pt);
-    #pragma unroll
-                            for (int e = 0; e < C::VE; e += 2)
-                                fma2(acc[0][e], acc[0][e + 1], w2.x, w2.y, v[e], v[e + 1]);
-                        } else {
-    #pragma unroll
-                            for (int g = 0; g < G; g += 2) {
-                                const float4 w4 = *reinterpret_cast<const float4 *>(pt + 2 * g);
-    #pragma unroll
-                                for (int e = 0; e < C::VE; e += 2) {
-                                    fma2(acc[g][e], acc[g][e + 1], w4.x, w4.y, v[e], v[e + 1]);
-                                    fma2(acc[g + 1][e], acc[g + 1][e + 1], w4.z, w4.w, v[e], v[e + 1]);
+                        auto pv_token = [&](int tt) {
+                            float v[C::VE];
+                            if constexpr (VREG)
+                                unpack_v<D, KV>(v, vr[tt]);
+                            else
+                                load_v<D, KV>(v, sV, tt, lane);
+                            const float *pt = ps + tt * 2 * G;
+                            if constexpr (G == 1) {
+                                const float2 w2 = *reinterpret_cast<const float2 *>(pt);
+        #pragma unroll
+                                for (int e = 0; e < C::VE; e += 2)
+                                    fma2(acc[0][e], acc[0][e + 1], w2.x, w2.y, v[e], v[e + 1]);
+                            } else {
+        #pragma unroll
+                                for (int g = 0; g < G; g += 2) {
+                                    const float4 w4 = *reinterpret_cast<const float4 *>(pt + 2 * g);
+        #pragma unroll
+                                    for (int e = 0; e < C::VE; e += 2) {
+                                        fma2(acc[g][e], acc[g][e + 1], w4.x, w4.y, v[e], v[e + 1]);
+                                        fma2(acc[g + 1][e], acc[g + 1][e + 1], w4.z, w4.w, v[e], v[e + 1]);
+                                    }
                                 }
+                            }
+                        };
+                        if (nvalid == TILE) {
+        #pragma unroll
+                            for (int tt = 0; tt < TILE; ++tt)
+                                pv_token(tt);
+                        } else {
+        #pragma unroll
+                            for (int tt = 0; tt < TILE; ++tt)
+                                if (tt < nvalid)
+                                    pv_token(tt);
+                        }
+                        if constexpr (!VREG) {
+                            if (release) {
+                                __syncwarp();
+                                if (lane == 0)
+                                    mbar_arrive(&empty[st]);
                             }
                         }
                     };
-                    if (nvalid == TILE) {
-    #pragma unroll
-                        for (int tt = 0; tt < TILE; ++tt)
-                            pv_token(tt);
+                    if constexpr (C::SUB > 1) {
+                        // the unit's tiles that hold attended tokens, in order
+                        const int i0 = tlo > 0 ? tlo / TILE : 0;
+                        const int i1 = (nvalid + TILE - 1) / TILE;
+#pragma unroll 1
+                        for (int i = i0; i < i1; ++i)
+                            cc_tile(sK + i * C::KV_BYTES / C::SUB, sV + i * C::KV_BYTES / C::SUB,
+                                    sKS + i * TILE, sVS + i * TILE, min(TILE, nvalid - i * TILE),
+                                    tlo - i * TILE, i == i1 - 1);
                     } else {
-    #pragma unroll
-                        for (int tt = 0; tt < TILE; ++tt)
-                            if (tt < nvalid)
-                                pv_token(tt);
-                    }
-                    if constexpr (!VREG) {
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(&empty[st]);
+                        cc_tile(sK, sV, sKS, sVS, nvalid, tlo, true);
                     }
                 }
             }
