@@ -600,15 +600,15 @@ __host__ __device__ constexpr int gather_row_tokens(int bs, int tt)
 
 // Four rows of a 2-D view of a cache (x = 0, rows r0..r3) as one gather copy
 // into shared memory at dst, laid out one after another; completion is
-// counted in bytes on the mbarrier.
+// counted in bytes on the mbarrier; `policy` is an L2 cache hint.
 __device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, int r0, int r1,
-                                            int r2, int r3, uint64_t *bar)
+                                            int r2, int r3, uint64_t *bar, uint64_t policy)
 {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-        "r"(smem_addr(bar))
+        "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
 
@@ -1358,8 +1358,10 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                         if (4 * g4 < nr) {
                             const int r0 = max(cur.id[4 * g4], 0), r1 = max(cur.id[4 * g4 + 1], 0);
                             const int r2 = max(cur.id[4 * g4 + 2], 0), r3 = max(cur.id[4 * g4 + 3], 0);
-                            tma_gather4(sK + 4 * g4 * rb, &p.tm_k, r0, r1, r2, r3, &full[st]);
-                            tma_gather4(sV + 4 * g4 * rb, &p.tm_v, r0, r1, r2, r3, &full[st]);
+                            tma_gather4(sK + 4 * g4 * rb, &p.tm_k, r0, r1, r2, r3, &full[st],
+                                        policy);
+                            tma_gather4(sV + 4 * g4 * rb, &p.tm_v, r0, r1, r2, r3, &full[st],
+                                        policy);
                         }
                     }
                     if constexpr (quantized(KV)) {
