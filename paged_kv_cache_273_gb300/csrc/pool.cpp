@@ -9,6 +9,7 @@
 // systems already use").
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <new>
@@ -17,6 +18,16 @@
 #include "pkv_internal.h"
 
 namespace {
+
+// An NVTX range around an entry point's host work and launches, so that a
+// timeline profiler shows the library's calls by name (a no-op when no
+// profiler is attached).
+struct Range {
+    explicit Range(const char *name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range &) = delete;
+    Range &operator=(const Range &) = delete;
+};
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -318,6 +329,7 @@ int kv_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, 
                   void *k_cache, void *v_cache, void *k_scales, void *v_scales,
                   pkv_stream_t stream)
 {
+    Range range("pkv.kv_block_copy");
     if (!pool || n < 0)
         return PKV_ERR_INVALID;
     if (n == 0)
@@ -340,6 +352,7 @@ int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dt
               const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,
               void *k_scales, void *v_scales, pkv_stream_t stream)
 {
+    Range range("pkv.kv_append");
     if (!pool || num_tokens < 0)
         return PKV_ERR_INVALID;
     if (pkv::quantized_dtype(pool->kv_dtype)) {
@@ -427,6 +440,7 @@ int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtyp
                            float *out, void *workspace, size_t workspace_bytes,
                            pkv_stream_t stream)
 {
+    Range range("pkv.paged_decode_attention");
     return decode_call(pool, q, q_dtype, num_q_heads, k_cache, v_cache, k_scales, v_scales,
                        block_tables, max_blocks_per_seq, seq_lens, batch, max_seq_len, 0, scale,
                        out, workspace, workspace_bytes, stream);
@@ -440,6 +454,7 @@ int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype
                                   int window, float scale, float *out, void *workspace,
                                   size_t workspace_bytes, pkv_stream_t stream)
 {
+    Range range("pkv.paged_decode_attention_window");
     return decode_call(pool, q, q_dtype, num_q_heads, k_cache, v_cache, k_scales, v_scales,
                        block_tables, max_blocks_per_seq, seq_lens, batch, max_seq_len, window,
                        scale, out, workspace, workspace_bytes, stream);
@@ -539,6 +554,7 @@ int paged_decode_attention_cascade(const pkv_pool *pool, const void *q, pkv_dtyp
                                    float scale, float *out, void *workspace,
                                    size_t workspace_bytes, pkv_stream_t stream)
 {
+    Range range("pkv.paged_decode_attention_cascade");
     if (!pool || batch < 0 || max_blocks_per_seq < 0 || max_seq_len < 0 || num_q_heads < 1 ||
         num_groups < 0 || max_group_size < 0 || max_prefix_len < 0)
         return PKV_ERR_INVALID;
@@ -600,6 +616,7 @@ int paged_prefill_attention(const pkv_pool *pool, const void *q, int num_q_heads
                             const int32_t *q_start, const int32_t *seq_lens, int batch,
                             int max_q_len, float scale, float *out, pkv_stream_t stream)
 {
+    Range range("pkv.paged_prefill_attention");
     if (!pool || batch < 0 || max_blocks_per_seq < 0 || max_q_len < 0 || num_q_heads < 1 ||
         num_q_heads % pool->num_kv_heads != 0)
         return PKV_ERR_INVALID;
