@@ -89,6 +89,26 @@ def test_int8_block_sizes(bs):
     _assert_ok(run(inp))
 
 
+# Multi-tile work units (a stage of 2 or 4 tiles gathered by rows of
+# min(bs, 16, unit / 4) tokens) across block sizes: 16-bit d 64 and 8-bit
+# rows at one head per KV head on the CUDA cores, 8-bit and 4-bit rows on
+# the tensor cores.
+UNIT_CASES = [(W.F16, 64, 1, bs) for bs in (4, 8, 32, 128)] + \
+             [(W.BF16, 64, 1, 8)] + \
+             [(W.I8, 128, 4, bs) for bs in (8, 64)] + \
+             [(W.I8, 128, 1, bs) for bs in (8, 128)] + \
+             [(W.I4, 128, 4, bs) for bs in (64, 128)] + \
+             [(W.I4, 128, 1, bs) for bs in (8, 64)]
+
+
+@pytest.mark.parametrize("kv,D,G,bs", UNIT_CASES)
+def test_work_units_across_block_sizes(kv, D, G, bs):
+    q = W.F16 if kv in (W.I8, W.I4) else kv
+    lengths = [1, bs - 1 if bs > 1 else 1, 31, 32, 33, 63, 64, 65, 129, 0, 777]
+    inp = _custom("units", 2 * G, 2, D, bs, kv, lengths, q=q, src=q, seed=53 + bs + kv)
+    _assert_ok(run(inp))
+
+
 def test_int8_with_bf16_queries_and_f32_source():
     inp = _custom("q8b", 8, 2, 128, 16, W.I8, [5, 300, 17], q=W.BF16, src=W.F32, seed=31)
     _assert_ok(run(inp))

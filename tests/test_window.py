@@ -127,7 +127,8 @@ def _window_run(name, window, steps=1, free_before=False):
 @gpu
 @pytest.mark.parametrize("name,window", [("tiny", 3), ("tiny", 5), ("gpt2", 100),
                                          ("gpt2", 16), ("llama3_8b", 1000),
-                                         ("llama2_70b", 4096), ("int8", 513)])
+                                         ("llama2_70b", 4096), ("int8", 513), ("int4", 700),
+                                         ("gpt2", 40)])
 def test_gpu_window_matches_oracle(name, window):
     from paged_kv_cache_273_gb300 import pkv
     err, tol, status, zero, _, _ = _window_run(name, window)
