@@ -17,17 +17,21 @@
 //    MMAs that serve all heads of the group from one read of the tile, which
 //    cuts the instructions per tile several-fold (fp32 caches and G = 1 stay
 //    on the CUDA cores).
-//  * The batch's work is a list of 16-token tiles, ordered by (sequence,
-//    KV head, tile).  A persistent grid of one CTA per SM takes an equal,
-//    contiguous share of that list (split-K across the sequence axis,
-//    balanced to +-1 tile whatever the length mix).
-//  * In each CTA one producer warp issues bulk async copies (cp.async.bulk)
-//    of whole K and V tiles, located through the block table, into a ring of
-//    shared-memory stages guarded by mbarriers (the int8 / int4 scales ride
-//    along as 16-byte cp.async copies); 11 consumer warps take tiles
-//    round-robin, each keeping its own online-softmax state (the
-//    FlashAttention idea of never materialising the score row, from the
-//    guide's "Flash attention: don't build the giant matrix").
+//  * The batch's work is a list of work units (1, 2 or 4 16-token tiles of
+//    one sequence and KV head, by cache type), ordered by (sequence, KV
+//    head, unit).  A persistent grid of one CTA per SM takes a contiguous
+//    share of that list (split-K across the sequence axis), the shares
+//    balanced by a cost that counts each unit and charges each (sequence,
+//    KV head) piece end.
+//  * In each CTA one producer warp issues the asynchronous copies of whole
+//    K and V units, located through the block table, into a ring of
+//    shared-memory stages guarded by mbarriers: 128-byte-swizzled tensor
+//    copies for one-tile units, four-row gathers for multi-tile units,
+//    plain bulk copies for small blocks (the int8 / int4 scales ride along
+//    as 16-byte cp.async copies); 11 consumer warps take units round-robin,
+//    each keeping its own online-softmax state (the FlashAttention idea of
+//    never materialising the score row, from the guide's "Flash attention:
+//    don't build the giant matrix").
 //  * At the end of each (sequence, KV head) piece the consumer warps merge
 //    their states.  A piece that is the whole sequence is written to `out`;
 //    otherwise the CTA stores a partial (max, sum, weighted V) and the last
