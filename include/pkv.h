@@ -287,7 +287,8 @@ size_t paged_decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_h
  *              After a call that reported PKV_ERR_TIMEOUT, zero it again.
  *
  * Batch is limited to 4096 sequences per call (PKV_ERR_UNSUPPORTED beyond).
- * Split-K: the batch's K/V tiles are divided evenly over the GPU's SMs; a
+ * Split-K: the batch's K/V tiles are divided over the GPU's SMs in shares of
+ * equal cost (each tile, and each (sequence, KV head) piece end, counted); a
  * sequence split across several CTAs is merged by the last CTA to finish it.
  * The result does not depend on timing.
  */
