@@ -192,6 +192,35 @@ def test_gpu_prefill_matches_oracle(dt, D, Hq, Hkv, bs, news, cached):
     assert err <= PREFILL_TOL[dt], err
 
 
+def _random_prefill_shape(seed):
+    rng = np.random.default_rng(5000 + seed)
+    dt = str(rng.choice(["bf16", "f16"]))
+    D = int(rng.choice([64, 128]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    Hq = Hkv * int(rng.choice([1, 2, 4, 8]))
+    bs = int(rng.choice([4, 8, 16, 32, 64, 128, 256]))
+    B = int(rng.integers(1, 6))
+    edge = [1, 2, 127, 128, 129, 255, 256, 257, 511]
+    news = [int(rng.choice(edge)) if rng.random() < 0.4 else int(rng.integers(1, 900))
+            for _ in range(B)]
+    cached = [0 if rng.random() < 0.4 else int(rng.integers(0, 700)) for _ in range(B)]
+    return dt, D, Hq, Hkv, bs, news, cached
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", range(24))
+def test_gpu_prefill_random_shapes(seed):
+    # seeded random types, head sizes, groups, block sizes and prompt /
+    # cached-length mixes (tile-boundary lengths among them)
+    from paged_kv_cache_273_gb300 import pkv
+    dt, D, Hq, Hkv, bs, news, cached = _random_prefill_shape(seed)
+    err, status, same_cache, intact = _gpu_prefill_case(dt, D, Hq, Hkv, bs, news, cached,
+                                                        600 + seed)
+    assert same_cache and intact
+    assert status == pkv.PKV_OK
+    assert err <= PREFILL_TOL[dt], (err, dt, D, Hq, Hkv, bs, news, cached)
+
+
 @pytest.mark.gpu
 def test_gpu_prefill_full_size_sampled():
     """The timed prefill workload (4 prompts x 4096 new tokens, 32 q / 8 KV
