@@ -266,3 +266,39 @@ def test_gpu_cascade_bad_prefix_length_is_reported():
     out = torch.zeros((2, 1, 64), dtype=torch.float32, device=dev)
     pkv.paged_decode_attention_cascade(pool, q, kc, vc, tables, lens, 0.1, out, ws, 32, gd)
     assert pkv.pkv_check_error(pool) == pkv.PKV_ERR_BAD_INDEX
+
+
+def _random_cascade_shape(seed):
+    rng = np.random.default_rng(8000 + seed)
+    dt = int(rng.choice([pkv.PKV_F16, pkv.PKV_BF16]))
+    D = int(rng.choice([64, 128]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    bs = int(rng.choice([4, 8, 16, 32]))
+    B = int(rng.integers(2, 21))
+    lens = [int(rng.integers(1, 1500)) for _ in range(B)]
+    # one to three groups of members sharing their first blocks (a member
+    # may be shorter than the blocks it shares: the prefix is capped by it)
+    share, pblocks, free = [], [], list(rng.permutation(B))
+    for _ in range(int(rng.integers(1, 4))):
+        if len(free) < 2:
+            break
+        n = int(rng.integers(2, min(len(free), 8) + 1))
+        mem = sorted(int(x) for x in free[:n])
+        free = free[n:]
+        share.append(mem)
+        pblocks.append(int(rng.integers(1, max(2, min(lens[m] for m in mem) // bs + 2))))
+    return dt, D, Hkv * G, Hkv, bs, lens, share, pblocks
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", range(24))
+def test_gpu_cascade_random_shapes(seed):
+    # seeded random types, head sizes, groups, block sizes, sharing
+    # patterns and lengths: the cascade and the plain path against the oracle
+    dt, D, Hq, Hkv, bs, lens, share, pblocks = _random_cascade_shape(seed)
+    err, plain, status, g, finite = _cascade_case(dt, D, Hq, Hkv, bs, lens, share, pblocks,
+                                                  300 + seed)
+    assert status == pkv.PKV_OK and finite
+    assert err <= 2e-3, (err, dt, D, Hq, Hkv, bs, lens, share, pblocks)
+    assert plain <= 2e-3, plain
