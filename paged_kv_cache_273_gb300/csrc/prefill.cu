@@ -1097,14 +1097,28 @@ int launch_prefix_pass(const pkv_pool *pool, const void *q, int num_q_heads, con
     prm.part = part;
     constexpr int QT = NQH * TBQ;
     prm.nqt = ((int64_t)max_group_size * prm.group_q + QT - 1) / QT;
-    // Key chunks: about one item per SM (the chunks of a row are merged at
-    // the end), at most 16 (the partials' room), at least one tile each.
-    const int tiles = (max_prefix_len + TBK - 1) / TBK;
+    // Key chunks of kc_tiles tiles each (the chunks of a row are merged at
+    // the end; at most 16, the partials' room): the persistent CTAs take the
+    // items in waves of num_sms, so the pass lasts about waves x (kc_tiles
+    // + one tile's worth of item setup and output); the chunk size with the
+    // least such time wins, the larger on ties (fewer partials to merge).
+    const int tiles = std::max(1, (max_prefix_len + TBK - 1) / TBK);
     const int64_t base = (int64_t)prm.nqt * ngroups * pool->num_kv_heads;
-    int want = (int)std::min<int64_t>(16, std::max<int64_t>(1, (pool->num_sms + base - 1) / base));
-    want = std::min(want, std::max(tiles, 1));
-    prm.kc_tiles = std::max(1, (tiles + want - 1) / want);
-    prm.nkc = std::max(1, (tiles + prm.kc_tiles - 1) / prm.kc_tiles);
+    const int64_t sms = std::max(1, pool->num_sms);
+    int64_t best_cost = INT64_MAX;
+    prm.kc_tiles = tiles;
+    for (int kc = tiles; kc >= 1; --kc) {
+        const int64_t nkc = (tiles + kc - 1) / kc;
+        if (nkc > 16)
+            break;
+        const int64_t waves = (base * nkc + sms - 1) / sms;
+        const int64_t cost = waves * (kc + 1);
+        if (cost < best_cost) {
+            best_cost = cost;
+            prm.kc_tiles = kc;
+        }
+    }
+    prm.nkc = (tiles + prm.kc_tiles - 1) / prm.kc_tiles;
     *kc_tiles_out = prm.kc_tiles;
     const int64_t nitems = (int64_t)prm.nqt * ngroups * pool->num_kv_heads * prm.nkc;
     if (nitems >= ((int64_t)1 << 31))
