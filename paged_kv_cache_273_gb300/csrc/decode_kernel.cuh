@@ -748,6 +748,10 @@ struct MmaState {
 };
 
 // q of the piece's G heads (in shared memory, q_dtype) -> B fragments.
+// With G < 8 the MMA's 8 head columns repeat the G heads (column n holds
+// head n mod G), so that every column's scores, maxima and sums are a real
+// head's: the P.V step then carries the weights' low parts in the repeated
+// columns (see mma_tile).
 template <int D, int G, int KV, bool QS>
 __device__ __forceinline__ void load_q_mma(MmaState<D, G, KV, QS> &st, const unsigned char *qs,
                                            int q_dtype, int lane)
@@ -755,16 +759,13 @@ __device__ __forceinline__ void load_q_mma(MmaState<D, G, KV, QS> &st, const uns
     constexpr bool BF = MmaBf16<KV>::v;
     const int gid = lane >> 2, tig = lane & 3;
     const int rot = MmaCfg<D, KV>::ROTATE ? (tig >> 1) * 2 : 0;
-    const int base = gid * D + tig * (D / 4);
+    const int base = (gid % G) * D + tig * (D / 4);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float x0 = 0.0f, x1 = 0.0f;
-            if (gid < G) {
-                x0 = q_elem(qs, base + q_elem_index<D, KV>(ks, h, 0, rot), q_dtype);
-                x1 = q_elem(qs, base + q_elem_index<D, KV>(ks, h, 1, rot), q_dtype);
-            }
+            const float x0 = q_elem(qs, base + q_elem_index<D, KV>(ks, h, 0, rot), q_dtype);
+            const float x1 = q_elem(qs, base + q_elem_index<D, KV>(ks, h, 1, rot), q_dtype);
             uint32_t hi, lo;
             split_pair<BF>(x0, x1, hi, lo);
             st.qh[ks][h] = hi;
@@ -773,28 +774,22 @@ __device__ __forceinline__ void load_q_mma(MmaState<D, G, KV, QS> &st, const uns
         }
 }
 
-// One 16-token tile: scores, online softmax, weighted V.  nvalid: tokens of
-// the tile inside the sequence; tlo: first token inside the window.  The
-// stage is released (empty barrier) as soon as its last byte has been read.
+// Words of a lane's eighth of a V row (>= 2).
+template <int D, int KV>
+struct VFrag {
+    static constexpr int VW = (MmaCfg<D, KV>::VB + 3) / 4;
+};
+
+// S^T = K q^T of one 16-token tile at sK: rows gid, gid + 8 of the tile, the
+// lane's quarter of d; accumulated into s (heads 2tig, 2tig + 1).
 template <int D, int G, int KV, bool QS>
-__device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsigned char *sK,
-                                         const unsigned char *sV, const __half *sKS,
-                                         const __half *sVS, int nvalid, int tlo, float scale_log2,
-                                         int lane, uint64_t *empty_bar, int swz,
-                                         bool release = true)
+__device__ __forceinline__ void mma_scores(float (&s)[4], const MmaState<D, G, KV, QS> &st,
+                                           const unsigned char *sK, int lane, bool sw)
 {
     using M = MmaCfg<D, KV>;
     constexpr bool BF = MmaBf16<KV>::v;
     constexpr int ROWB = M::ROWB;
     const int gid = lane >> 2, tig = lane & 3;
-
-    // (tiles laid out by the swizzled tensor copies: chunk addresses go
-    // through swz_off)
-    constexpr bool CAN_SWZ = mma_path(KV, G) && (ROWB == 128 || ROWB == 256);
-    const bool sw = CAN_SWZ && swz != 0;
-
-    // ---- S^T = K q^T (rows gid, gid + 8 of the tile; the lane's quarter of d)
-    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     {
         const uint32_t k0 = gid * ROWB + tig * M::KQB;
         const uint32_t k1 = k0 + 8 * ROWB;
@@ -857,11 +852,17 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
             }
         }
     }
+}
 
-    // ---- the lane's eighth of the V rows of tokens 2tig, 2tig+1, 2tig+8,
-    // 2tig+9, and the scales; then the stage goes back to the producer
-    constexpr int VW = (M::VB + 3) / 4;           // 32-bit words per token (>= 2)
-    uint32_t vw[4][VW];
+// The lane's eighth of the V rows of tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of
+// the tile at sV.
+template <int D, int KV>
+__device__ __forceinline__ void load_v_frag(uint32_t (&vw)[4][VFrag<D, KV>::VW],
+                                            const unsigned char *sV, int lane, bool sw)
+{
+    using M = MmaCfg<D, KV>;
+    constexpr int ROWB = M::ROWB;
+    const int gid = lane >> 2, tig = lane & 3;
     {
         const int toks[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
 #pragma unroll
@@ -881,16 +882,118 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
                 vw[i][0] = x.x; vw[i][1] = x.y;
             }
         }
+    }
+}
+
+// O^T += V^T P^T for one tile: vw from load_v_frag, p0..p3 the weights of
+// (token gid, heads 2tig, 2tig+1), (token gid + 8, the same heads).
+template <int D, int G, int KV, bool QS>
+__device__ __forceinline__ void mma_pv(MmaState<D, G, KV, QS> &st,
+                                       const uint32_t (&vw)[4][VFrag<D, KV>::VW], float p0,
+                                       float p1, float p2, float p3, int lane)
+{
+    using M = MmaCfg<D, KV>;
+    constexpr bool BF = MmaBf16<KV>::v;
+    // P^T as the B fragment: (token gid | gid+8, heads 2tig, 2tig+1) pairs,
+    // transposed to (tokens 2tig, 2tig+1 | +8, head gid).  G = 8: the high
+    // and the low parts are two B fragments, two MMAs per m-tile.  G < 8:
+    // one fragment whose columns [0, G) hold the high parts and [G, 2G) the
+    // low parts of the same heads (columns n and n + G hold one head), the
+    // rest zero: one MMA per m-tile, the two sums added at the piece's end.
+    const int tig = lane & 3;
+    uint32_t ph0, pl0, ph1, pl1;
+    split_pair<BF>(p0, p1, ph0, pl0);
+    split_pair<BF>(p2, p3, ph1, pl1);
+    constexpr bool PACK = G < 8;
+    uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+    if constexpr (PACK) {
+        const bool hi_cols = 2 * tig < G, lo_cols = !hi_cols && 2 * tig < 2 * G;
+        bh0 = transpose8x8(hi_cols ? ph0 : (lo_cols ? pl0 : 0u));
+        bh1 = transpose8x8(hi_cols ? ph1 : (lo_cols ? pl1 : 0u));
+    } else {
+        bh0 = transpose8x8(ph0);
+        bh1 = transpose8x8(ph1);
+        bl0 = transpose8x8(pl0);
+        bl1 = transpose8x8(pl1);
+    }
+
+    // ---- O^T += V^T P^T, m-tile j: rows gid, gid+8 = elements 2j, 2j+1 of
+    // the lane's eighth of d
+#pragma unroll
+    for (int j = 0; j < M::MT; ++j) {
+        uint32_t a0, a1, a2, a3;
         if constexpr (KvBits<KV>::v == 16) {
-            // rows past the sequence end may hold anything (0 * NaN is NaN)
-            if (nvalid < TILE) {
+            a0 = __byte_perm(vw[0][j], vw[1][j], 0x5410u);
+            a1 = __byte_perm(vw[0][j], vw[1][j], 0x7632u);
+            a2 = __byte_perm(vw[2][j], vw[3][j], 0x5410u);
+            a3 = __byte_perm(vw[2][j], vw[3][j], 0x7632u);
+        } else if constexpr (KV == PKV_I8) {
+            // bytes 2j, 2j+1 of the token's eighth: word j / 2
+            const int w = j >> 1;
+            const uint32_t xa = vw[0][w] ^ 0x80808080u, xb = vw[1][w] ^ 0x80808080u;
+            const uint32_t xc = vw[2][w] ^ 0x80808080u, xd = vw[3][w] ^ 0x80808080u;
+            // interleave the two tokens' bytes: (A.b, B.b, A.b', B.b')
+            const uint32_t tab = (j & 1) ? __byte_perm(xa, xb, 0x7362u) : __byte_perm(xa, xb, 0x5140u);
+            const uint32_t tcd = (j & 1) ? __byte_perm(xc, xd, 0x7362u) : __byte_perm(xc, xd, 0x5140u);
+            a0 = i8pair_to_half2<0x4140u>(tab);
+            a1 = i8pair_to_half2<0x4342u>(tab);
+            a2 = i8pair_to_half2<0x4140u>(tcd);
+            a3 = i8pair_to_half2<0x4342u>(tcd);
+        } else {
+            // codes 2j, 2j+1 of the token's eighth (16 codes in two words)
+            // are byte j of it: that byte of the two tokens goes to bytes 0
+            // and 2 of one word (low nibbles: code 2j; high: code 2j + 1)
+            const int w = j >> 2, b = j & 3;
+            const uint32_t sel = (uint32_t)b | ((uint32_t)(b + 4) << 8);
+            const uint32_t tab = __byte_perm(vw[0][w], vw[1][w], sel);
+            const uint32_t tcd = __byte_perm(vw[2][w], vw[3][w], sel);
+            a0 = i4pair_lo_to_half2(tab);
+            a1 = i4pair_hi_to_half2(tab);
+            a2 = i4pair_lo_to_half2(tcd);
+            a3 = i4pair_hi_to_half2(tcd);
+        }
+        mma_16816<BF>(st.acc[j], a0, a1, a2, a3, bh0, bh1);
+        if constexpr (!PACK)
+            mma_16816<BF>(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+    }
+}
+
+// One 16-token tile: scores, online softmax, weighted V.  nvalid: tokens of
+// the tile inside the sequence; tlo: first token inside the window.  The
+// stage is released (empty barrier) as soon as its last byte has been read.
+template <int D, int G, int KV, bool QS>
+__device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsigned char *sK,
+                                         const unsigned char *sV, const __half *sKS,
+                                         const __half *sVS, int nvalid, int tlo, float scale_log2,
+                                         int lane, uint64_t *empty_bar, int swz,
+                                         bool release = true)
+{
+    using M = MmaCfg<D, KV>;
+    constexpr int ROWB = M::ROWB;
+    constexpr int VW = VFrag<D, KV>::VW;
+    const int gid = lane >> 2, tig = lane & 3;
+
+    // (tiles laid out by the swizzled tensor copies: chunk addresses go
+    // through swz_off)
+    constexpr bool CAN_SWZ = mma_path(KV, G) && (ROWB == 128 || ROWB == 256);
+    const bool sw = CAN_SWZ && swz != 0;
+
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    mma_scores<D, G, KV, QS>(s, st, sK, lane, sw);
+
+    // ---- V and the scales; then the stage goes back to the producer
+    uint32_t vw[4][VW];
+    load_v_frag<D, KV>(vw, sV, lane, sw);
+    if constexpr (KvBits<KV>::v == 16) {
+        // rows past the sequence end may hold anything (0 * NaN is NaN)
+        if (nvalid < TILE) {
+            const int toks[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (toks[i] >= nvalid)
+            for (int i = 0; i < 4; ++i)
+                if (toks[i] >= nvalid)
 #pragma unroll
-                        for (int u = 0; u < VW; ++u)
-                            vw[i][u] = 0u;
-            }
+                    for (int u = 0; u < VW; ++u)
+                        vw[i][u] = 0u;
         }
     }
     float ks0 = 1.0f, ks1 = 1.0f, vs0 = 1.0f, vs1 = 1.0f;
@@ -950,52 +1053,105 @@ __device__ __forceinline__ void mma_tile(MmaState<D, G, KV, QS> &st, const unsig
         p2 = v1 ? p2 * vs1 : 0.0f;
         p3 = v1 ? p3 * vs1 : 0.0f;
     }
-    // P^T as the B fragment: (token gid | gid+8, heads 2tig, 2tig+1) pairs,
-    // transposed to (tokens 2tig, 2tig+1 | +8, head gid)
-    uint32_t ph0, pl0, ph1, pl1;
-    split_pair<BF>(p0, p1, ph0, pl0);
-    split_pair<BF>(p2, p3, ph1, pl1);
-    const uint32_t bh0 = transpose8x8(ph0), bh1 = transpose8x8(ph1);
-    const uint32_t bl0 = transpose8x8(pl0), bl1 = transpose8x8(pl1);
+    mma_pv<D, G, KV, QS>(st, vw, p0, p1, p2, p3, lane);
+}
 
-    // ---- O^T += V^T P^T, m-tile j: rows gid, gid+8 = elements 2j, 2j+1 of
-    // the lane's eighth of d
+// A unit of NS 16-token tiles of a quantized cache (the tiles [i0, i1) hold
+// attended tokens; the others are neither read nor scored): the scores of
+// all its tiles first (NS independent MMA chains), one update of the running
+// maxima over the unit, then the weighted V of each tile, its V read from
+// the stage just before its MMAs.  The stage goes back to the producer after
+// the last V read.  (Used for 2-tile units: with 4-tile units of 4-bit
+// codes, and with the units' V taken into registers before the softmax so
+// that the stage goes back earlier, it was slower than tile by tile.)
+template <int D, int G, int KV, bool QS, int NS>
+__device__ __forceinline__ void mma_unit(MmaState<D, G, KV, QS> &st, const unsigned char *sK,
+                                         const unsigned char *sV, const __half *sKS,
+                                         const __half *sVS, int nvalid, int tlo, float scale_log2,
+                                         int lane, uint64_t *empty_bar)
+{
+    static_assert(quantized(KV), "multi-tile units of the tensor-core path are quantized");
+    using M = MmaCfg<D, KV>;
+    constexpr int TB = TILE * M::ROWB;
+    constexpr int VW = VFrag<D, KV>::VW;
+    const int gid = lane >> 2;
+    const int i0 = tlo > 0 ? tlo / TILE : 0;
+    const int i1 = (nvalid + TILE - 1) / TILE;
+
+    // ---- scores (log2 domain) of tokens gid, gid + 8 of every tile
+    float x[NS][4];
+    bool above = false;
 #pragma unroll
-    for (int j = 0; j < M::MT; ++j) {
-        uint32_t a0, a1, a2, a3;
-        if constexpr (KvBits<KV>::v == 16) {
-            a0 = __byte_perm(vw[0][j], vw[1][j], 0x5410u);
-            a1 = __byte_perm(vw[0][j], vw[1][j], 0x7632u);
-            a2 = __byte_perm(vw[2][j], vw[3][j], 0x5410u);
-            a3 = __byte_perm(vw[2][j], vw[3][j], 0x7632u);
-        } else if constexpr (KV == PKV_I8) {
-            // bytes 2j, 2j+1 of the token's eighth: word j / 2
-            const int w = j >> 1;
-            const uint32_t xa = vw[0][w] ^ 0x80808080u, xb = vw[1][w] ^ 0x80808080u;
-            const uint32_t xc = vw[2][w] ^ 0x80808080u, xd = vw[3][w] ^ 0x80808080u;
-            // interleave the two tokens' bytes: (A.b, B.b, A.b', B.b')
-            const uint32_t tab = (j & 1) ? __byte_perm(xa, xb, 0x7362u) : __byte_perm(xa, xb, 0x5140u);
-            const uint32_t tcd = (j & 1) ? __byte_perm(xc, xd, 0x7362u) : __byte_perm(xc, xd, 0x5140u);
-            a0 = i8pair_to_half2<0x4140u>(tab);
-            a1 = i8pair_to_half2<0x4342u>(tab);
-            a2 = i8pair_to_half2<0x4140u>(tcd);
-            a3 = i8pair_to_half2<0x4342u>(tcd);
-        } else {
-            // codes 2j, 2j+1 of the token's eighth (16 codes in two words)
-            // are byte j of it: that byte of the two tokens goes to bytes 0
-            // and 2 of one word (low nibbles: code 2j; high: code 2j + 1)
-            const int w = j >> 2, b = j & 3;
-            const uint32_t sel = (uint32_t)b | ((uint32_t)(b + 4) << 8);
-            const uint32_t tab = __byte_perm(vw[0][w], vw[1][w], sel);
-            const uint32_t tcd = __byte_perm(vw[2][w], vw[3][w], sel);
-            a0 = i4pair_lo_to_half2(tab);
-            a1 = i4pair_hi_to_half2(tab);
-            a2 = i4pair_lo_to_half2(tcd);
-            a3 = i4pair_hi_to_half2(tcd);
-        }
-        mma_16816<BF>(st.acc[j], a0, a1, a2, a3, bh0, bh1);
-        mma_16816<BF>(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+    for (int i = 0; i < NS; ++i) {
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (i >= i0 && i < i1)
+            mma_scores<D, G, KV, QS>(s, st, sK + i * TB, lane, false);
+        const int t0 = i * TILE + gid, t1 = t0 + 8;
+        const bool v0 = t0 < nvalid && t0 >= tlo;
+        const bool v1 = t1 < nvalid && t1 >= tlo;
+        const float sc0 = scale_log2 * __half2float(sKS[t0]);
+        const float sc1 = scale_log2 * __half2float(sKS[t1]);
+        x[i][0] = v0 ? s[0] * sc0 : -INFINITY;   // token t0, head 2tig
+        x[i][1] = v0 ? s[1] * sc0 : -INFINITY;   // token t0, head 2tig + 1
+        x[i][2] = v1 ? s[2] * sc1 : -INFINITY;   // token t1, head 2tig
+        x[i][3] = v1 ? s[3] * sc1 : -INFINITY;   // token t1, head 2tig + 1
+        above |= fmaxf(x[i][0], x[i][2]) > st.m[0] || fmaxf(x[i][1], x[i][3]) > st.m[1];
     }
+    if (__any_sync(FULL_MASK, above)) {
+        // the running maxima move (softmax is shift invariant: any running
+        // value that is one of the scores seen is exact)
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NS; ++i) {
+            mx0 = fmaxf(mx0, fmaxf(x[i][0], x[i][2]));
+            mx1 = fmaxf(mx1, fmaxf(x[i][1], x[i][3]));
+        }
+#pragma unroll
+        for (int mask = 4; mask < 32; mask <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, mask));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, mask));
+        }
+        const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
+        const float c0 = exp2_approx(st.m[0] - n0), c1 = exp2_approx(st.m[1] - n1);
+        st.m[0] = n0;
+        st.m[1] = n1;
+        st.l[0] *= c0;
+        st.l[1] *= c1;
+#pragma unroll
+        for (int j = 0; j < M::MT; ++j) {
+            st.acc[j][0] *= c0;
+            st.acc[j][2] *= c0;
+            st.acc[j][1] *= c1;
+            st.acc[j][3] *= c1;
+        }
+    }
+
+    // ---- weights and weighted V, tile by tile
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        if (i >= i0 && i < i1) {
+            uint32_t vw[4][VW];
+            load_v_frag<D, KV>(vw, sV + i * TB, lane, false);
+            const int t0 = i * TILE + gid, t1 = t0 + 8;
+            const bool v0 = t0 < nvalid && t0 >= tlo;
+            const bool v1 = t1 < nvalid && t1 >= tlo;
+            float p0 = exp2_approx(x[i][0] - st.m[0]), p1 = exp2_approx(x[i][1] - st.m[1]);
+            float p2 = exp2_approx(x[i][2] - st.m[0]), p3 = exp2_approx(x[i][3] - st.m[1]);
+            st.l[0] += p0 + p2;
+            st.l[1] += p1 + p3;
+            // V codes are dequantized through the weights: p * s_v of the
+            // token (rows outside the attended range may hold any scale)
+            const float vs0 = __half2float(sVS[t0]), vs1 = __half2float(sVS[t1]);
+            p0 = v0 ? p0 * vs0 : 0.0f;
+            p1 = v0 ? p1 * vs0 : 0.0f;
+            p2 = v1 ? p2 * vs1 : 0.0f;
+            p3 = v1 ? p3 * vs1 : 0.0f;
+            mma_pv<D, G, KV, QS>(st, vw, p0, p1, p2, p3, lane);
+        }
+    }
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(empty_bar);
 }
 
 // ---- the kernel ---------------------------------------------------------------
@@ -1181,7 +1337,6 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
         }
         __syncthreads();
     }
-    const int64_t T = s_tstart[B];
     const int64_t CT = s_cstart[B];
     const int P = (int)min((int64_t)gridDim.x, CT);
     const int cta = blockIdx.x;
@@ -1693,17 +1848,23 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
                     reinterpret_cast<const __half *>(scale_ring + st * 2 * C::SC_BYTES);
                 const __half *sVS = sKS + C::TT;
                 if constexpr (C::MMA && C::SUB > 1) {
-                    // the unit's 16-token tiles that hold attended tokens, in
-                    // order; the last one hands the stage back
-                    const int i0 = tlo > 0 ? tlo / TILE : 0;
-                    const int i1 = (nvalid + TILE - 1) / TILE;
+                    // the unit's 16-token tiles that hold attended tokens:
+                    // 2-tile units scored together, 4-tile units tile by
+                    // tile (the last one hands the stage back)
+                    if constexpr (C::SUB == 2) {
+                        mma_unit<D, G, KV, QS, C::SUB>(mst, sK, sV, sKS, sVS, nvalid, tlo,
+                                                       p.scale_log2, lane, &empty[st]);
+                    } else {
+                        const int i0 = tlo > 0 ? tlo / TILE : 0;
+                        const int i1 = (nvalid + TILE - 1) / TILE;
 #pragma unroll 1
-                    for (int i = i0; i < i1; ++i)
-                        mma_tile<D, G, KV, QS>(mst, sK + i * C::KV_BYTES / C::SUB,
-                                               sV + i * C::KV_BYTES / C::SUB, sKS + i * TILE,
-                                               sVS + i * TILE, min(TILE, nvalid - i * TILE),
-                                               tlo - i * TILE, p.scale_log2, lane, &empty[st], 0,
-                                               i == i1 - 1);
+                        for (int i = i0; i < i1; ++i)
+                            mma_tile<D, G, KV, QS>(mst, sK + i * C::KV_BYTES / C::SUB,
+                                                   sV + i * C::KV_BYTES / C::SUB, sKS + i * TILE,
+                                                   sVS + i * TILE, min(TILE, nvalid - i * TILE),
+                                                   tlo - i * TILE, p.scale_log2, lane,
+                                                   &empty[st], 0, i == i1 - 1);
+                    }
                 } else if constexpr (C::MMA) {
                     mma_tile<D, G, KV, QS>(mst, sK, sV, sKS, sVS, nvalid, tlo, p.scale_log2,
                                            lane, &empty[st], swz);
@@ -1880,6 +2041,15 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::NTHREADS, 1) paged_decode_kerne
 #pragma unroll
                     for (int mask = 4; mask < 32; mask <<= 1)
                         mst.l[r] += __shfl_xor_sync(FULL_MASK, mst.l[r], mask);
+                if constexpr (G < 8) {
+                    // columns 2tig + G, +1 (lane + G/2) hold the low-part
+                    // sums of the lane's heads
+#pragma unroll
+                    for (int j = 0; j < D / 16; ++j)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            mst.acc[j][u] += __shfl_down_sync(FULL_MASK, mst.acc[j][u], G / 2);
+                }
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int h = 2 * tig + r;
