@@ -586,11 +586,11 @@ def run_e2e(pool, inp, kc, vc, tables, ws, scale, max_len, steps, dev, stream, b
             bytes_app, world, rmax):
     """The metric end to end through the C ABI with host buffers.  Every
     step: the host computes the step's slot mapping into a pinned staging
-    buffer that already holds the step's k, v, q and lengths; one copy moves
-    the buffer to the device; kv_append and paged_decode_attention read their
-    inputs from slices of it; the output is copied back to pinned memory and
-    the host reads it.  Two steps are in flight: the host prepares step k
-    while the device runs step k - 1, and reads step k - 2's output."""
+    buffer that already holds the step's k, v, q and lengths; one
+    paged_decode_step call copies the buffer to the device, appends, attends
+    and copies the output back to pinned memory; the host reads it.  Two
+    steps are in flight: the host prepares step k while the device runs step
+    k - 1, and reads step k - 2's output."""
     import torch
     from paged_kv_cache_273_gb300 import pkv
     wl = inp.workload
@@ -612,14 +612,14 @@ def run_e2e(pool, inp, kc, vc, tables, ws, scale, max_len, steps, dev, stream, b
         hn[o_len:o_len + B * 4] = inp.lens_after_step(st).view(np.uint8)
         stage.append(h)
     d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
-    e_k = d_stage[o_k:o_k + nk].view(torch.bfloat16).view(B, Hkv, D)
-    e_v = d_stage[o_v:o_v + nk].view(torch.bfloat16).view(B, Hkv, D)
-    e_q = d_stage[o_q:o_q + nq].view(torch.bfloat16).view(B, Hq, D)
-    e_slot = d_stage[o_slot:o_slot + B * 4].view(torch.int32)
-    e_lens = d_stage[o_len:o_len + B * 4].view(torch.int32)
     out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    step = pkv.DecodeStep(pool, d_stage, pkv.StepLayout(o_k, o_v, o_q, o_slot, o_len),
+                          torch.bfloat16, torch.bfloat16, Hq, kc, vc, tables, B, max_len, scale,
+                          out, ws, stream=stream)
     h_out = [torch.empty((B, Hq, D), dtype=torch.float32).pin_memory() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
+    tables_h = np.ascontiguousarray(inp.block_tables, dtype=np.int32)
+    start = np.zeros(B, np.int32)
     checksum = [0.0]
 
     def host_read(k):
@@ -630,13 +630,10 @@ def run_e2e(pool, inp, kc, vc, tables, ws, scale, max_len, steps, dev, stream, b
         s = k % S
         if k >= 2:
             host_read(k - 2)
-        slots = stage[s].numpy()[o_slot:o_slot + B * 4].view(np.int32)
-        slots[:] = pkv.kv_slot_mapping(inp.block_tables, bs, (inp.prefix_lens + s).astype(np.int32))
-        d_stage.copy_(stage[s], non_blocking=True)
-        pkv.kv_append(pool, e_k, e_v, e_slot, kc, vc, stream=stream)
-        pkv.paged_decode_attention(pool, e_q, kc, vc, tables, e_lens, scale, out, ws, max_len,
-                                   stream=stream)
-        h_out[k % 2].copy_(out, non_blocking=True)
+        start[:] = inp.prefix_lens + s
+        pkv.kv_slot_mapping(tables_h, bs, start,
+                            out=stage[s].numpy()[o_slot:o_slot + B * 4].view(np.int32))
+        step(stage[s], h_out[k % 2])
         done[k % 2].record(stream)
 
     for w in range(4):
@@ -655,9 +652,10 @@ def run_e2e(pool, inp, kc, vc, tables, ws, scale, max_len, steps, dev, stream, b
     value = whole_job(e2e_bytes, e2e_s, world, rmax)[0] / 1e9
     return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": total,
             "d2h_bytes_per_step": out.numel() * 4, "steps": n,
-            "note": "one pinned-to-device copy of the step's inputs (k, v, q, slot mapping, "
-                    "lengths), slot mapping on the host in the step, output copied back and "
-                    "read by the host; two steps in flight"}
+            "note": "paged_decode_step per step: one pinned-to-device copy of the step's inputs "
+                    "(k, v, q, slot mapping, lengths), kv_append, attention, the output copied "
+                    "back and read by the host; slot mapping on the host in the step; two steps "
+                    "in flight"}
 
 
 def run_gpu(args):

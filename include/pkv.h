@@ -436,6 +436,49 @@ int paged_prefill_attention(const pkv_pool *pool, const void *q, int num_q_heads
                             int max_q_len, float scale, float *out, pkv_stream_t stream);
 
 /*
+ * pkv_step_layout — where one decode step's inputs sit in a staging buffer:
+ * byte offsets from its start.  B = batch, Hkv/D the pool's, Hq = the call's
+ * num_q_heads.
+ *   k_new, v_new   [B][Hkv][D] of in_dtype, offsets multiples of 16.
+ *   q              [B][Hq][D] of q_dtype, offset a multiple of 16.
+ *   slot_mapping   int32 [B] (the new token of sequence b goes to slot
+ *                  slot_mapping[b]; < 0 = no token), offset a multiple of 4.
+ *   seq_lens       int32 [B], the lengths after the append, offset a
+ *                  multiple of 4.
+ */
+typedef struct {
+    size_t k_new, v_new, q, slot_mapping, seq_lens;
+} pkv_step_layout;
+
+/*
+ * paged_decode_step — one whole decode step with the inputs and the result
+ * in host memory ([NOTES] "What happens at each decoding step": the new
+ * token's key and value are stored, then its query attends over every cached
+ * row; [GUIDE] "How the cache turns the loop cheap").  Enqueued on `stream`,
+ * in this order:
+ *   1. one host-to-device copy of in_bytes from host_in to dev_in (the
+ *      step's k_new, v_new, q, slot mapping and lengths at the offsets of
+ *      `layout`);
+ *   2. kv_append of the B new tokens (slot_mapping, k_new, v_new in dev_in);
+ *   3. paged_decode_attention of q over the caches into `out` (device);
+ *   4. if host_out is not NULL, one device-to-host copy of out
+ *      (B * Hq * D fp32) to host_out.
+ * Arguments as for kv_append and paged_decode_attention; host_in and
+ * host_out should be page-locked (cudaHostAlloc) for the copies to be
+ * asynchronous.  Nothing waits: host_in must not change, and host_out must
+ * not be read, until the stream has passed the call (an event recorded after
+ * it).  PKV_ERR_INVALID for a region of `layout` outside in_bytes or
+ * misaligned, or a NULL buffer; the calls' own errors otherwise (a failing
+ * step stops the sequence; nothing is undone).
+ */
+int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, size_t in_bytes,
+                      const pkv_step_layout *layout, pkv_dtype in_dtype, pkv_dtype q_dtype,
+                      int num_q_heads, void *k_cache, void *v_cache, void *k_scales,
+                      void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
+                      int batch, int max_seq_len, float scale, float *out, float *host_out,
+                      void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/*
  * paged_decode_attention_noalloc — paged_decode_attention for callers that
  * cannot allocate device memory.  The pages have no counterpart; this is a
  * property of this library's interface, not of the method.

@@ -446,6 +446,68 @@ int paged_decode_attention(const pkv_pool *pool, const void *q, pkv_dtype q_dtyp
                        out, workspace, workspace_bytes, stream);
 }
 
+namespace {
+
+// [off, off + bytes) inside [0, total) and off a multiple of align
+bool region_ok(size_t off, size_t bytes, size_t total, size_t align)
+{
+    return off % align == 0 && off <= total && bytes <= total - off;
+}
+
+}  // namespace
+
+int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, size_t in_bytes,
+                      const pkv_step_layout *layout, pkv_dtype in_dtype, pkv_dtype q_dtype,
+                      int num_q_heads, void *k_cache, void *v_cache, void *k_scales,
+                      void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
+                      int batch, int max_seq_len, float scale, float *out, float *host_out,
+                      void *workspace, size_t workspace_bytes, pkv_stream_t stream)
+{
+    Range range("pkv.paged_decode_step");
+    if (!pool || !layout || batch < 0 || num_q_heads < 1 ||
+        num_q_heads % pool->num_kv_heads != 0)
+        return PKV_ERR_INVALID;
+    if (in_dtype != PKV_F32 && in_dtype != PKV_F16 && in_dtype != PKV_BF16)
+        return PKV_ERR_INVALID;
+    if (q_dtype != PKV_F32 && q_dtype != PKV_F16 && q_dtype != PKV_BF16)
+        return PKV_ERR_INVALID;
+    if (batch == 0)
+        return PKV_OK;
+    if (!host_in || !dev_in || !pkv::aligned16(dev_in))
+        return PKV_ERR_INVALID;
+    const size_t B = (size_t)batch;
+    const size_t kv_bytes =
+        B * pool->num_kv_heads * pool->head_dim * (size_t)pkv::dtype_bytes(in_dtype);
+    const size_t q_bytes = B * num_q_heads * pool->head_dim * (size_t)pkv::dtype_bytes(q_dtype);
+    if (!region_ok(layout->k_new, kv_bytes, in_bytes, 16) ||
+        !region_ok(layout->v_new, kv_bytes, in_bytes, 16) ||
+        !region_ok(layout->q, q_bytes, in_bytes, 16) ||
+        !region_ok(layout->slot_mapping, B * 4, in_bytes, 4) ||
+        !region_ok(layout->seq_lens, B * 4, in_bytes, 4))
+        return PKV_ERR_INVALID;
+    if (!pool->has_device)
+        return PKV_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    unsigned char *d = static_cast<unsigned char *>(dev_in);
+    int rc = kv_append(pool, d + layout->k_new, d + layout->v_new, in_dtype,
+                       reinterpret_cast<const int32_t *>(d + layout->slot_mapping), batch,
+                       k_cache, v_cache, k_scales, v_scales, stream);
+    if (rc != PKV_OK)
+        return rc;
+    rc = paged_decode_attention(pool, d + layout->q, q_dtype, num_q_heads, k_cache, v_cache,
+                                k_scales, v_scales, block_tables, max_blocks_per_seq,
+                                reinterpret_cast<const int32_t *>(d + layout->seq_lens), batch,
+                                max_seq_len, scale, out, workspace, workspace_bytes, stream);
+    if (rc != PKV_OK || !host_out)
+        return rc;
+    const size_t out_bytes = B * num_q_heads * pool->head_dim * sizeof(float);
+    if (cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
 int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
                                   int num_q_heads, const void *k_cache, const void *v_cache,
                                   const void *k_scales, const void *v_scales,

@@ -45,7 +45,15 @@ SYMBOLS = ("pkv_status_string", "kv_block_pool_init", "kv_block_pool_destroy", "
            "kv_slot_mapping", "kv_append", "kv_block_copy", "paged_decode_workspace_bytes", "paged_decode_attention",
            "paged_decode_attention_window", "paged_prefill_attention", "kv_prefix_groups",
            "paged_decode_cascade_workspace_bytes", "paged_decode_attention_cascade",
-           "paged_decode_attention_noalloc", "pkv_selftest_wait_timeout", "pkv_check_error")
+           "paged_decode_attention_noalloc", "paged_decode_step", "pkv_selftest_wait_timeout",
+           "pkv_check_error")
+
+
+class StepLayout(ctypes.Structure):
+    """pkv_step_layout: byte offsets of one decode step's inputs in a staging
+    buffer."""
+    _fields_ = [("k_new", ctypes.c_size_t), ("v_new", ctypes.c_size_t), ("q", ctypes.c_size_t),
+                ("slot_mapping", ctypes.c_size_t), ("seq_lens", ctypes.c_size_t)]
 
 
 class PkvError(RuntimeError):
@@ -123,6 +131,9 @@ def load() -> ctypes.CDLL:
         lib.paged_decode_attention_noalloc.argtypes = [P, P, I, I, P, P, P, P, P, I, P, I, I, F,
                                                        P, P]
         lib.paged_decode_attention_noalloc.restype = I
+        lib.paged_decode_step.argtypes = [P, P, P, SZ, ctypes.POINTER(StepLayout), I, I, I, P, P,
+                                          P, P, P, I, I, I, F, P, P, P, SZ, P]
+        lib.paged_decode_step.restype = I
         lib.pkv_selftest_wait_timeout.argtypes = [P, P]
         lib.pkv_selftest_wait_timeout.restype = I
         lib.pkv_check_error.argtypes = [P, P]
@@ -285,14 +296,23 @@ def kv_reserve_slots_cow(pool: Pool, seq_lens, block_tables: np.ndarray, num_new
     return slots[:total], src[:n].copy(), dst[:n].copy()
 
 
-def kv_slot_mapping(block_tables, block_size: int, start, num_new=None) -> np.ndarray:
+def kv_slot_mapping(block_tables, block_size: int, start, num_new=None,
+                    out: np.ndarray | None = None) -> np.ndarray:
+    """Slots of the new tokens; `out` (contiguous int32 of the slot count, for
+    example a slice of a staging buffer) receives them in place if given."""
     bt = _i32(block_tables)
     st = _i32(start)
     nn = None if num_new is None else _i32(num_new)
     total = st.size if nn is None else int(nn.sum())
-    slots = np.zeros(max(total, 1), np.int32)
+    if out is None:
+        slots = np.zeros(max(total, 1), np.int32)
+    else:
+        if out.dtype != np.int32 or out.size != total or not out.flags.c_contiguous:
+            raise ValueError("out must be a contiguous int32 array of the slot count")
+        slots = out
     _check(load().kv_slot_mapping(_i32p(bt), bt.shape[1], block_size, st.size, _i32p(st),
-                                  _i32p(nn), _i32p(slots)), "kv_slot_mapping")
+                                  _i32p(nn), _i32p(slots) if slots.size else None),
+           "kv_slot_mapping")
     return slots[:total]
 
 
@@ -467,6 +487,68 @@ def paged_decode_attention_noalloc(pool: Pool, q, k_cache, v_cache, block_tables
         _dptr(k_scales), _dptr(v_scales), _dptr(block_tables), block_tables.shape[1],
         _dptr(seq_lens), B, int(max_seq_len), float(scale), _dptr(out), _stream(stream)),
         "paged_decode_attention_noalloc")
+
+
+def _hptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("expected a host tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class DecodeStep:
+    """paged_decode_step with its fixed arguments marshalled once: a serving
+    loop calls step(host_in, host_out) per decode step.  host_in: a host
+    uint8 tensor (page-locked for an asynchronous copy) holding the step's
+    inputs at the offsets of `layout` (a StepLayout); dev_in: a device uint8
+    tensor of at least host_in's size; host_out: a host fp32 tensor of
+    out's shape, or None.  Nothing waits: record an event after the call
+    and synchronize on it before reusing host_in or reading host_out."""
+
+    def __init__(self, pool: Pool, dev_in, layout: StepLayout, in_dtype, q_dtype,
+                 num_q_heads: int, k_cache, v_cache, block_tables, batch: int, max_seq_len: int,
+                 scale: float, out, workspace, k_scales=None, v_scales=None, stream=None):
+        if in_dtype not in PKV_DTYPE or q_dtype not in PKV_DTYPE:
+            raise ValueError("unsupported dtype")
+        if out.dtype != torch.float32:
+            raise ValueError("out must be float32")
+        if block_tables.dtype != torch.int32:
+            raise ValueError("block_tables must be int32")
+        if dev_in.dtype != torch.uint8:
+            raise ValueError("dev_in must be a uint8 tensor")
+        self.pool = pool
+        self.layout = layout
+        self.in_bytes = dev_in.numel()
+        self._keep = (dev_in, k_cache, v_cache, block_tables, out, workspace, k_scales,
+                      v_scales)
+        self._head = (pool.handle,)
+        self._mid = (_dptr(dev_in), ctypes.c_size_t(self.in_bytes), ctypes.byref(layout),
+                     PKV_DTYPE[in_dtype], PKV_DTYPE[q_dtype], int(num_q_heads), _dptr(k_cache),
+                     _dptr(v_cache), _dptr(k_scales), _dptr(v_scales), _dptr(block_tables),
+                     block_tables.shape[1], int(batch), int(max_seq_len), float(scale),
+                     _dptr(out))
+        self._tail = (_dptr(workspace), workspace.numel() * workspace.element_size(),
+                      _stream(stream))
+        self._fn = load().paged_decode_step
+
+    def __call__(self, host_in, host_out=None) -> None:
+        if host_in.numel() * host_in.element_size() != self.in_bytes:
+            raise ValueError("host_in must have dev_in's size")
+        _check(self._fn(*self._head, _hptr(host_in), *self._mid, _hptr(host_out),
+                        *self._tail), "paged_decode_step")
+
+
+def paged_decode_step(pool: Pool, host_in, dev_in, layout: StepLayout, in_dtype, q_dtype,
+                      num_q_heads: int, k_cache, v_cache, block_tables, batch: int,
+                      max_seq_len: int, scale: float, out, host_out, workspace, k_scales=None,
+                      v_scales=None, stream=None) -> None:
+    """One decode step with host buffers (see DecodeStep)."""
+    DecodeStep(pool, dev_in, layout, in_dtype, q_dtype, num_q_heads, k_cache, v_cache,
+               block_tables, batch, max_seq_len, scale, out, workspace, k_scales, v_scales,
+               stream)(host_in, host_out)
 
 
 def pkv_selftest_wait_timeout(pool: Pool, stream=None) -> None:
