@@ -238,6 +238,41 @@ __global__ void __launch_bounds__(256) block_copy_kernel(
     }
 }
 
+// Staging copies of a decode step with host buffers (paged_decode_step):
+// 16-byte chunks between page-locked host memory, reached through its
+// device mapping, and device memory.  Thread t of block b moves chunks
+// b*256*SC + c*256 + t (c < SC).  LOAD_FIRST: the source is not written by
+// the previous kernels of the stream (the caller's host input), so the
+// chunks are loaded before the wait for the previous kernel and stored after
+// it; with programmatic dependent launch the loads then overlap that
+// kernel's tail.  Otherwise (the device output) the wait comes first.
+constexpr int SC = 4;
+
+template <bool LOAD_FIRST>
+__global__ void __launch_bounds__(256) stage_copy_kernel(const uint4 *__restrict__ src,
+                                                         uint4 *__restrict__ dst, int64_t n)
+{
+    grid_dependents_launch();
+    const int64_t base = (int64_t)blockIdx.x * blockDim.x * SC + threadIdx.x;
+    uint4 v[SC];
+    if (!LOAD_FIRST)
+        grid_dependency_wait();
+#pragma unroll
+    for (int c = 0; c < SC; ++c) {
+        const int64_t i = base + (int64_t)c * blockDim.x;
+        if (i < n)
+            v[c] = src[i];
+    }
+    if (LOAD_FIRST)
+        grid_dependency_wait();
+#pragma unroll
+    for (int c = 0; c < SC; ++c) {
+        const int64_t i = base + (int64_t)c * blockDim.x;
+        if (i < n)
+            dst[i] = v[c];
+    }
+}
+
 int grid_for(int64_t work_items, int threads, int num_sms)
 {
     int64_t blocks = (work_items + threads - 1) / threads;
@@ -250,6 +285,30 @@ int grid_for(int64_t work_items, int threads, int num_sms)
 }
 
 }  // namespace
+
+int launch_stage_copy(const void *src, void *dst, size_t bytes, bool load_first,
+                      pkv_stream_t stream)
+{
+    if (bytes % 16 != 0 || !aligned16(src) || !aligned16(dst))
+        return PKV_ERR_INVALID;
+    const int64_t n = (int64_t)(bytes / 16);
+    if (n == 0)
+        return PKV_OK;
+    const int threads = 256;
+    const int64_t blocks = (n + threads * SC - 1) / (threads * SC);
+    if (blocks > INT32_MAX)
+        return PKV_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        load_first
+            ? launch_pdl(stage_copy_kernel<true>, dim3((unsigned)blocks), dim3(threads), 0, s,
+                         static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n)
+            : launch_pdl(stage_copy_kernel<false>, dim3((unsigned)blocks), dim3(threads), 0, s,
+                         static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n);
+    if (e != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 int launch_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, int n,
                       void *k_cache, void *v_cache, void *k_scales, void *v_scales,

@@ -67,6 +67,12 @@ int launch_prefill(const pkv_pool *pool, const void *q, int num_q_heads, const v
                    const int32_t *q_start, const int32_t *seq_lens, int batch, int max_q_len,
                    float scale, float *out, pkv_stream_t stream);
 int launch_selftest_wait_timeout(const pkv_pool *pool, pkv_stream_t stream);
+// 16-byte-chunk copy kernel of paged_decode_step (both pointers device-
+// addressable and 16-byte aligned, bytes a multiple of 16; PKV_ERR_INVALID
+// otherwise).  load_first: src is not written by earlier kernels of the
+// stream, so its loads may overlap the previous kernel.
+int launch_stage_copy(const void *src, void *dst, size_t bytes, bool load_first,
+                      pkv_stream_t stream);
 int launch_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, int n,
                       void *k_cache, void *v_cache, void *k_scales, void *v_scales,
                       pkv_stream_t stream);

@@ -454,6 +454,36 @@ bool region_ok(size_t off, size_t bytes, size_t total, size_t align)
     return off % align == 0 && off <= total && bytes <= total - off;
 }
 
+// The device address of page-locked host memory (its mapping into the device
+// address space), or null for other memory.
+void *mapped_host(const void *p)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();   // clear the error this query may leave
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Copy between host and device memory for the step: page-locked host memory
+// in whole 16-byte chunks goes through the staging kernel (programmatic
+// dependent launch keeps the stream's kernels overlapping), other memory
+// through cudaMemcpyAsync.
+int step_copy(const void *src, void *dst, size_t bytes, bool to_device, cudaStream_t s)
+{
+    const void *hs = to_device ? mapped_host(src) : src;
+    void *hd = to_device ? dst : mapped_host(dst);
+    if (hs && hd && bytes % 16 == 0 && pkv::aligned16(hs) && pkv::aligned16(hd))
+        return pkv::launch_stage_copy(hs, hd, bytes, to_device,
+                                      reinterpret_cast<pkv_stream_t>(s));
+    return cudaMemcpyAsync(dst, src, bytes,
+                           to_device ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost,
+                           s) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
 }  // namespace
 
 int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, size_t in_bytes,
@@ -488,10 +518,11 @@ int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, s
     if (!pool->has_device)
         return PKV_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    int rc = step_copy(host_in, dev_in, in_bytes, true, s);
+    if (rc != PKV_OK)
+        return rc;
     unsigned char *d = static_cast<unsigned char *>(dev_in);
-    int rc = kv_append(pool, d + layout->k_new, d + layout->v_new, in_dtype,
+    rc = kv_append(pool, d + layout->k_new, d + layout->v_new, in_dtype,
                        reinterpret_cast<const int32_t *>(d + layout->slot_mapping), batch,
                        k_cache, v_cache, k_scales, v_scales, stream);
     if (rc != PKV_OK)
@@ -503,9 +534,7 @@ int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, s
     if (rc != PKV_OK || !host_out)
         return rc;
     const size_t out_bytes = B * num_q_heads * pool->head_dim * sizeof(float);
-    if (cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return PKV_ERR_CUDA;
-    return PKV_OK;
+    return step_copy(out, host_out, out_bytes, false, s);
 }
 
 int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype q_dtype,
