@@ -71,8 +71,11 @@ def test_step_validation_without_device_work():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name,steps", [("llama3_8b", 3), ("int8", 1), ("gpt2", 1)])
-def test_step_matches_separate_calls_and_oracle(name, steps):
+@pytest.mark.parametrize("name,steps,pinned", [("llama3_8b", 3, True), ("int8", 1, True),
+                                               ("gpt2", 1, True), ("llama3_8b", 2, False)])
+def test_step_matches_separate_calls_and_oracle(name, steps, pinned):
+    # pinned host buffers are copied by the staging kernel through their
+    # device mapping, pageable ones by cudaMemcpyAsync
     import torch
     import parity_harness as PH
     inp = W.make_inputs(name)
@@ -82,9 +85,11 @@ def test_step_matches_separate_calls_and_oracle(name, steps):
     case = PH.build(inp)     # paged_decode_step
     eb = {W.F32: 4, W.F16: 2, W.BF16: 2}
     layout, total = _layout(B, Hq, Hkv, D, eb[wl.src_dtype], eb[wl.q_dtype])
-    host_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    host_in = torch.empty(total, dtype=torch.uint8)
+    host_out = torch.empty((B, Hq, D), dtype=torch.float32)
+    if pinned:
+        host_in, host_out = host_in.pin_memory(), host_out.pin_memory()
     dev_in = torch.empty(total, dtype=torch.uint8, device="cuda")
-    host_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
     out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
     step = pkv.DecodeStep(case.pool, dev_in, layout, PH._TORCH[wl.src_dtype],
                           PH._TORCH[wl.q_dtype], Hq, case.gk.tensor, case.gv.tensor,
