@@ -468,8 +468,14 @@ typedef struct {
  * asynchronous.  Nothing waits: host_in must not change, and host_out must
  * not be read, until the stream has passed the call (an event recorded after
  * it).  PKV_ERR_INVALID for a region of `layout` outside in_bytes or
- * misaligned, or a NULL buffer; the calls' own errors otherwise (a failing
- * step stops the sequence; nothing is undone).
+ * misaligned, or a NULL buffer.  The append's and the attention's argument
+ * checks run before anything is enqueued, with their usual results; an
+ * error at launch (PKV_ERR_CUDA) stops the sequence where it happened and
+ * undoes nothing.  Page-locked host buffers whose size is a multiple of 16
+ * bytes are copied by a small kernel through their device mapping (so the
+ * stream stays a chain of kernels that overlap under programmatic dependent
+ * launch); other host memory by cudaMemcpyAsync.  host_in and host_out must
+ * not overlap.
  */
 int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, size_t in_bytes,
                       const pkv_step_layout *layout, pkv_dtype in_dtype, pkv_dtype q_dtype,

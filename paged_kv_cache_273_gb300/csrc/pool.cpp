@@ -348,11 +348,13 @@ int kv_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, 
                                   stream);
 }
 
-int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
-              const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,
-              void *k_scales, void *v_scales, pkv_stream_t stream)
+namespace {
+
+// kv_append's argument checks (everything but the device).
+int append_check(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
+                 const int32_t *slot_mapping, int num_tokens, const void *k_cache,
+                 const void *v_cache, const void *k_scales, const void *v_scales)
 {
-    Range range("pkv.kv_append");
     if (!pool || num_tokens < 0)
         return PKV_ERR_INVALID;
     if (pkv::quantized_dtype(pool->kv_dtype)) {
@@ -371,6 +373,20 @@ int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dt
     if (pkv::quantized_dtype(pool->kv_dtype) && (!k_scales || !v_scales || !pkv::aligned16(k_scales) ||
                                      !pkv::aligned16(v_scales)))
         return PKV_ERR_INVALID;
+    return PKV_OK;
+}
+
+}  // namespace
+
+int kv_append(const pkv_pool *pool, const void *k_new, const void *v_new, pkv_dtype in_dtype,
+              const int32_t *slot_mapping, int num_tokens, void *k_cache, void *v_cache,
+              void *k_scales, void *v_scales, pkv_stream_t stream)
+{
+    Range range("pkv.kv_append");
+    const int rc = append_check(pool, k_new, v_new, in_dtype, slot_mapping, num_tokens, k_cache,
+                                v_cache, k_scales, v_scales);
+    if (rc != PKV_OK || num_tokens == 0)
+        return rc;
     if (!pool->has_device)
         return PKV_ERR_CUDA;
     return pkv::launch_append(pool, k_new, v_new, in_dtype, slot_mapping, num_tokens, k_cache,
@@ -386,11 +402,13 @@ size_t paged_decode_workspace_bytes(const pkv_pool *pool, int batch, int num_q_h
 
 namespace {
 
-int decode_call(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
-                const void *k_cache, const void *v_cache, const void *k_scales,
-                const void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
-                const int32_t *seq_lens, int batch, int max_seq_len, int window, float scale,
-                float *out, void *workspace, size_t workspace_bytes, pkv_stream_t stream)
+// The decode calls' argument checks (everything but the device): PKV_OK when
+// the call can be launched (or has nothing to do: batch 0).
+int decode_check(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
+                 const void *k_cache, const void *v_cache, const void *k_scales,
+                 const void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
+                 const int32_t *seq_lens, int batch, int max_seq_len, int window,
+                 const float *out, const void *workspace, size_t workspace_bytes)
 {
     if (window < 0)
         return PKV_ERR_INVALID;
@@ -421,10 +439,24 @@ int decode_call(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_
     if (pkv::quantized_dtype(pool->kv_dtype) && (!k_scales || !v_scales || !pkv::aligned16(k_scales) ||
                                      !pkv::aligned16(v_scales)))
         return PKV_ERR_INVALID;
-    if (!pool->has_device)
-        return PKV_ERR_CUDA;
     if (workspace_bytes < pkv::decode_workspace_bytes(pool, batch, num_q_heads))
         return PKV_ERR_INVALID;
+    return PKV_OK;
+}
+
+int decode_call(const pkv_pool *pool, const void *q, pkv_dtype q_dtype, int num_q_heads,
+                const void *k_cache, const void *v_cache, const void *k_scales,
+                const void *v_scales, const int32_t *block_tables, int max_blocks_per_seq,
+                const int32_t *seq_lens, int batch, int max_seq_len, int window, float scale,
+                float *out, void *workspace, size_t workspace_bytes, pkv_stream_t stream)
+{
+    const int rc = decode_check(pool, q, q_dtype, num_q_heads, k_cache, v_cache, k_scales,
+                                v_scales, block_tables, max_blocks_per_seq, seq_lens, batch,
+                                max_seq_len, window, out, workspace, workspace_bytes);
+    if (rc != PKV_OK || batch == 0)
+        return rc;
+    if (!pool->has_device)
+        return PKV_ERR_CUDA;
     return pkv::launch_decode(pool, q, q_dtype, num_q_heads, k_cache, v_cache, k_scales, v_scales,
                               block_tables, max_blocks_per_seq, seq_lens, batch, max_seq_len,
                               window, scale, out, workspace, workspace_bytes, stream);
@@ -515,16 +547,27 @@ int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, s
         !region_ok(layout->slot_mapping, B * 4, in_bytes, 4) ||
         !region_ok(layout->seq_lens, B * 4, in_bytes, 4))
         return PKV_ERR_INVALID;
+    // the append's and the attention's own checks, before any device work
+    unsigned char *d = static_cast<unsigned char *>(dev_in);
+    const int32_t *slots = reinterpret_cast<const int32_t *>(d + layout->slot_mapping);
+    const int32_t *lens = reinterpret_cast<const int32_t *>(d + layout->seq_lens);
+    int rc = append_check(pool, d + layout->k_new, d + layout->v_new, in_dtype, slots, batch,
+                          k_cache, v_cache, k_scales, v_scales);
+    if (rc == PKV_OK)
+        rc = decode_check(pool, d + layout->q, q_dtype, num_q_heads, k_cache, v_cache, k_scales,
+                          v_scales, block_tables, max_blocks_per_seq, lens, batch, max_seq_len,
+                          0, out, workspace, workspace_bytes);
+    if (rc != PKV_OK)
+        return rc;
     if (!pool->has_device)
         return PKV_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int rc = step_copy(host_in, dev_in, in_bytes, true, s);
+    rc = step_copy(host_in, dev_in, in_bytes, true, s);
     if (rc != PKV_OK)
         return rc;
-    unsigned char *d = static_cast<unsigned char *>(dev_in);
     rc = kv_append(pool, d + layout->k_new, d + layout->v_new, in_dtype,
-                       reinterpret_cast<const int32_t *>(d + layout->slot_mapping), batch,
-                       k_cache, v_cache, k_scales, v_scales, stream);
+                   reinterpret_cast<const int32_t *>(d + layout->slot_mapping), batch, k_cache,
+                   v_cache, k_scales, v_scales, stream);
     if (rc != PKV_OK)
         return rc;
     rc = paged_decode_attention(pool, d + layout->q, q_dtype, num_q_heads, k_cache, v_cache,

@@ -39,11 +39,11 @@ def test_step_validation_without_device_work():
     ptr = ctypes.c_void_p(base)
 
     def call(layout, in_dtype=pkv.PKV_F16, q_dtype=pkv.PKV_F16, hq=Hq, in_bytes=total,
-             batch=B):
+             batch=B, ws=1 << 20):
         return lib.paged_decode_step(p.handle, ptr, ptr, in_bytes,
                                      None if layout is None else ctypes.byref(layout), in_dtype,
                                      q_dtype, hq, ptr, ptr, None, None, ptr, 4, batch, 64, 0.125,
-                                     ptr, ptr, ptr, 1 << 20, None)
+                                     ptr, ptr, ptr, ws, None)
 
     def shifted(**kw):
         lay = pkv.StepLayout(good.k_new, good.v_new, good.q, good.slot_mapping, good.seq_lens)
@@ -64,6 +64,8 @@ def test_step_validation_without_device_work():
         (good, {"q_dtype": pkv.PKV_I4}),
         (good, {"hq": 3}),                                 # not a multiple of Hkv
         (good, {"batch": -1}),
+        (good, {"q_dtype": pkv.PKV_BF16}),                 # the attention's check: q type
+        (good, {"ws": 16}),                                # ... and its workspace size
     ]
     for lay, kw in bad:
         assert call(lay, **kw) == pkv.PKV_ERR_INVALID, (lay, kw)
