@@ -472,10 +472,11 @@ typedef struct {
  * checks run before anything is enqueued, with their usual results; an
  * error at launch (PKV_ERR_CUDA) stops the sequence where it happened and
  * undoes nothing.  Page-locked host buffers whose size is a multiple of 16
- * bytes are copied by a small kernel through their device mapping (so the
+ * bytes are copied by small kernels through their device mapping (so the
  * stream stays a chain of kernels that overlap under programmatic dependent
- * launch); other host memory by cudaMemcpyAsync.  host_in and host_out must
- * not overlap.
+ * launch; over fp caches the input copy and the append are one kernel);
+ * other host memory by cudaMemcpyAsync.  host_in and host_out must not
+ * overlap.
  */
 int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, size_t in_bytes,
                       const pkv_step_layout *layout, pkv_dtype in_dtype, pkv_dtype q_dtype,

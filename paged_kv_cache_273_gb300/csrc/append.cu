@@ -273,6 +273,74 @@ __global__ void __launch_bounds__(256) stage_copy_kernel(const uint4 *__restrict
     }
 }
 
+// The input side of a decode step with a page-locked host staging buffer
+// over an fp cache, in one kernel: the staging copy above, and for the
+// chunks of the new K and V rows also the append (the bit copy of
+// append_copy_kernel) into the cache slots the staged slot mapping names.
+// Host loads (the chunks, each K/V chunk's slot) come before the wait for
+// the previous kernel; the stores after it.
+struct StepIn {
+    int64_t k_new, v_new, slots;   // 16-byte chunk offsets / int32 index of the regions
+    int B, H, chunks_per_row, block_size;
+    int64_t num_slots;
+};
+
+__global__ void __launch_bounds__(256) step_in_kernel(const uint4 *__restrict__ src,
+                                                      uint4 *__restrict__ dst, int64_t n,
+                                                      StepIn a, uint4 *__restrict__ k_cache,
+                                                      uint4 *__restrict__ v_cache,
+                                                      unsigned int *__restrict__ err)
+{
+    grid_dependents_launch();
+    const int32_t *slot_mapping = reinterpret_cast<const int32_t *>(src) + a.slots;
+    const int64_t row_chunks = (int64_t)a.B * a.H * a.chunks_per_row;
+    const int64_t base = (int64_t)blockIdx.x * blockDim.x * SC + threadIdx.x;
+    uint4 v[SC];
+    int64_t kd[SC], vd[SC];   // cache chunk a K / V chunk goes to, or -1
+#pragma unroll
+    for (int c = 0; c < SC; ++c) {
+        const int64_t i = base + (int64_t)c * blockDim.x;
+        kd[c] = vd[c] = -1;
+        if (i < n) {
+            v[c] = src[i];
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                const int64_t rel = i - (kv == 0 ? a.k_new : a.v_new);
+                if (rel >= 0 && rel < row_chunks) {
+                    const int64_t row = rel / a.chunks_per_row;   // (token, head)
+                    const int chunk = (int)(rel - row * a.chunks_per_row);
+                    const int64_t t = row / a.H;
+                    const int h = (int)(row - t * a.H);
+                    const int32_t slot = slot_mapping[t];
+                    int64_t d = -1;
+                    if (slot >= 0 && (int64_t)slot < a.num_slots) {
+                        const int64_t blk = slot / a.block_size;
+                        const int64_t off = slot - blk * a.block_size;
+                        d = ((blk * a.H + h) * a.block_size + off) * a.chunks_per_row + chunk;
+                    } else if (slot >= 0) {
+                        d = -2;                                  // slot out of range
+                    }
+                    (kv == 0 ? kd[c] : vd[c]) = d;
+                }
+            }
+        }
+    }
+    grid_dependency_wait();
+#pragma unroll
+    for (int c = 0; c < SC; ++c) {
+        const int64_t i = base + (int64_t)c * blockDim.x;
+        if (i < n) {
+            dst[i] = v[c];
+            if (kd[c] >= 0)
+                k_cache[kd[c]] = v[c];
+            if (vd[c] >= 0)
+                v_cache[vd[c]] = v[c];
+            if (kd[c] == -2 || vd[c] == -2)
+                atomicOr(err, PKV_EBIT_SLOT);
+        }
+    }
+}
+
 int grid_for(int64_t work_items, int threads, int num_sms)
 {
     int64_t blocks = (work_items + threads - 1) / threads;
@@ -306,6 +374,39 @@ int launch_stage_copy(const void *src, void *dst, size_t bytes, bool load_first,
             : launch_pdl(stage_copy_kernel<false>, dim3((unsigned)blocks), dim3(threads), 0, s,
                          static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n);
     if (e != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int launch_step_in(const pkv_pool *pool, const void *src, void *dst, size_t bytes,
+                   size_t k_off, size_t v_off, size_t slot_off, int batch, void *k_cache,
+                   void *v_cache, pkv_stream_t stream)
+{
+    if (quantized_dtype(pool->kv_dtype) || bytes % 16 != 0 || k_off % 16 != 0 ||
+        v_off % 16 != 0 || slot_off % 4 != 0 || !aligned16(src) || !aligned16(dst) ||
+        !aligned16(k_cache) || !aligned16(v_cache))
+        return PKV_ERR_INVALID;
+    const int64_t n = (int64_t)(bytes / 16);
+    if (n == 0 || batch == 0)
+        return PKV_OK;
+    StepIn a;
+    a.k_new = (int64_t)(k_off / 16);
+    a.v_new = (int64_t)(v_off / 16);
+    a.slots = (int64_t)(slot_off / 4);
+    a.B = batch;
+    a.H = pool->num_kv_heads;
+    a.chunks_per_row = pool->head_dim * dtype_bytes(pool->kv_dtype) / 16;
+    a.block_size = pool->block_size;
+    a.num_slots = (int64_t)pool->num_blocks * pool->block_size;
+    const int threads = 256;
+    const int64_t blocks = (n + threads * SC - 1) / (threads * SC);
+    if (blocks > INT32_MAX)
+        return PKV_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_pdl(step_in_kernel, dim3((unsigned)blocks), dim3(threads), 0, s,
+                   static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n, a,
+                   static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+                   pool->d_err) != cudaSuccess)
         return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

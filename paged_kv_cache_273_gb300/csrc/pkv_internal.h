@@ -73,6 +73,14 @@ int launch_selftest_wait_timeout(const pkv_pool *pool, pkv_stream_t stream);
 // stream, so its loads may overlap the previous kernel.
 int launch_stage_copy(const void *src, void *dst, size_t bytes, bool load_first,
                       pkv_stream_t stream);
+// The input side of paged_decode_step over an fp cache in one kernel: the
+// staging copy of bytes from src (page-locked host memory, by its device
+// address) to dst, and the append of the batch's new K and V rows (at byte
+// offsets k_off, v_off of the buffer, slots at slot_off) into the caches.
+// PKV_ERR_INVALID for quantized pools or misaligned arguments.
+int launch_step_in(const pkv_pool *pool, const void *src, void *dst, size_t bytes,
+                   size_t k_off, size_t v_off, size_t slot_off, int batch, void *k_cache,
+                   void *v_cache, pkv_stream_t stream);
 int launch_block_copy(const pkv_pool *pool, const int32_t *src, const int32_t *dst, int n,
                       void *k_cache, void *v_cache, void *k_scales, void *v_scales,
                       pkv_stream_t stream);

@@ -562,14 +562,22 @@ int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, s
     if (!pool->has_device)
         return PKV_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    rc = step_copy(host_in, dev_in, in_bytes, true, s);
-    if (rc != PKV_OK)
-        return rc;
-    rc = kv_append(pool, d + layout->k_new, d + layout->v_new, in_dtype,
-                   reinterpret_cast<const int32_t *>(d + layout->slot_mapping), batch, k_cache,
-                   v_cache, k_scales, v_scales, stream);
-    if (rc != PKV_OK)
-        return rc;
+    const void *h = mapped_host(host_in);
+    if (h && !pkv::quantized_dtype(pool->kv_dtype) && in_bytes % 16 == 0 && pkv::aligned16(h)) {
+        // fp cache, page-locked input: the staging copy and the append are one kernel
+        rc = pkv::launch_step_in(pool, h, dev_in, in_bytes, layout->k_new, layout->v_new,
+                                 layout->slot_mapping, batch, k_cache, v_cache, stream);
+        if (rc != PKV_OK)
+            return rc;
+    } else {
+        rc = step_copy(host_in, dev_in, in_bytes, true, s);
+        if (rc != PKV_OK)
+            return rc;
+        rc = kv_append(pool, d + layout->k_new, d + layout->v_new, in_dtype, slots, batch,
+                       k_cache, v_cache, k_scales, v_scales, stream);
+        if (rc != PKV_OK)
+            return rc;
+    }
     rc = paged_decode_attention(pool, d + layout->q, q_dtype, num_q_heads, k_cache, v_cache,
                                 k_scales, v_scales, block_tables, max_blocks_per_seq,
                                 reinterpret_cast<const int32_t *>(d + layout->seq_lens), batch,
