@@ -73,14 +73,18 @@ def test_step_validation_without_device_work():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name,steps,pinned", [("llama3_8b", 3, True), ("int8", 1, True),
-                                               ("gpt2", 1, True), ("llama3_8b", 2, False)])
-def test_step_matches_separate_calls_and_oracle(name, steps, pinned):
-    # pinned host buffers are copied by the staging kernel through their
-    # device mapping, pageable ones by cudaMemcpyAsync
+@pytest.mark.parametrize("name,steps,pinned,lengths", [
+    ("llama3_8b", 3, True, None), ("int8", 1, True, None), ("gpt2", 1, True, None),
+    ("llama3_8b", 2, False, None),
+    ("gpt2", 1, True, (0, 1, 17, 0, 300, 2048, 5, 16)),     # idle sequences: slot -1
+])
+def test_step_matches_separate_calls_and_oracle(name, steps, pinned, lengths):
+    # pinned host buffers are copied by kernels through their device mapping
+    # (over fp caches the input copy and the append are one kernel),
+    # pageable ones by cudaMemcpyAsync
     import torch
     import parity_harness as PH
-    inp = W.make_inputs(name)
+    inp = W.make_inputs(name, lengths=lengths)
     wl = inp.workload
     B, Hq, Hkv, D = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     ref = PH.build(inp)      # separate kv_append / paged_decode_attention calls
