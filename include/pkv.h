@@ -462,7 +462,10 @@ typedef struct {
  *   2. kv_append of the B new tokens (slot_mapping, k_new, v_new in dev_in);
  *   3. paged_decode_attention of q over the caches into `out` (device);
  *   4. if host_out is not NULL, one device-to-host copy of out
- *      (B * Hq * D fp32) to host_out.
+ *      (B * Hq * D fp32) to host_out.  A page-locked host_out takes the
+ *      output directly instead (the attention writes it there through its
+ *      device mapping) and `out` is then left unwritten: pass host_out =
+ *      NULL to keep the result on the device.
  * Arguments as for kv_append and paged_decode_attention; host_in and
  * host_out should be page-locked (cudaHostAlloc) for the copies to be
  * asynchronous.  Nothing waits: host_in must not change, and host_out must
@@ -476,7 +479,7 @@ typedef struct {
  * stream stays a chain of kernels that overlap under programmatic dependent
  * launch; over fp caches the input copy and the append are one kernel);
  * other host memory by cudaMemcpyAsync.  host_in and host_out must not
- * overlap.
+ * overlap.  `out` must be a valid device buffer in every case.
  */
 int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, size_t in_bytes,
                       const pkv_step_layout *layout, pkv_dtype in_dtype, pkv_dtype q_dtype,

@@ -578,11 +578,16 @@ int paged_decode_step(const pkv_pool *pool, const void *host_in, void *dev_in, s
         if (rc != PKV_OK)
             return rc;
     }
+    // a page-locked host_out takes the attention's output directly, through
+    // its device mapping (the attention only writes its output)
+    void *mapped_out = host_out ? mapped_host(host_out) : nullptr;
+    const bool direct = mapped_out && pkv::aligned16(mapped_out);
     rc = paged_decode_attention(pool, d + layout->q, q_dtype, num_q_heads, k_cache, v_cache,
-                                k_scales, v_scales, block_tables, max_blocks_per_seq,
-                                reinterpret_cast<const int32_t *>(d + layout->seq_lens), batch,
-                                max_seq_len, scale, out, workspace, workspace_bytes, stream);
-    if (rc != PKV_OK || !host_out)
+                                k_scales, v_scales, block_tables, max_blocks_per_seq, lens,
+                                batch, max_seq_len, scale,
+                                direct ? static_cast<float *>(mapped_out) : out, workspace,
+                                workspace_bytes, stream);
+    if (rc != PKV_OK || !host_out || direct)
         return rc;
     const size_t out_bytes = B * num_q_heads * pool->head_dim * sizeof(float);
     return step_copy(out, host_out, out_bytes, false, s);
