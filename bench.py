@@ -653,9 +653,9 @@ def run_e2e(pool, inp, kc, vc, tables, ws, scale, max_len, steps, dev, stream, b
     return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": total,
             "d2h_bytes_per_step": out.numel() * 4, "steps": n,
             "note": "paged_decode_step per step: one pinned-to-device copy of the step's inputs "
-                    "(k, v, q, slot mapping, lengths), kv_append, attention, the output copied "
-                    "back and read by the host; slot mapping on the host in the step; two steps "
-                    "in flight"}
+                    "(k, v, q, slot mapping, lengths), kv_append, attention writing its output "
+                    "to pinned host memory, which the host reads; slot mapping on the host in "
+                    "the step; two steps in flight"}
 
 
 def run_gpu(args):
