@@ -398,7 +398,8 @@ int paged_decode_attention_window(const pkv_pool *pool, const void *q, pkv_dtype
 /*
  * paged_prefill_attention — causal attention of a batch of new tokens over
  * the paged cache: the prefill half of serving ([VIS] "Prefill and decode
- * feel different": the whole prompt in one pass, limited by arithmetic rather than memory traffic).
+ * feel different": the whole prompt in one pass, limited by arithmetic
+ * rather than memory traffic).
  * Sequence b has n_b = q_start[b+1] - q_start[b] new tokens, the last n_b of
  * its seq_lens[b] cached rows (their K and V already written by kv_append);
  * new token i sits at position p = seq_lens[b] - n_b + i and, for each query
