@@ -86,9 +86,9 @@ const char *pkv_status_string(int status);
 
 /*
  * kv_block_pool_init — describe one shared pool of fixed-size cache blocks.
- * [VIS] "PagedAttention: the cache in blocks" (blocks of a fixed number of
- * tokens drawn from one shared pool); [GUIDE] "Paging: borrow the trick
- * operating systems already use".
+ * [VIS] "PagedAttention: the cache in blocks" (every request's rows live in
+ * equal-size blocks that all come out of a single pool); [GUIDE] "Paging:
+ * borrow the trick operating systems already use".
  *
  *   out          receives the new pool (owned by the caller; free with
  *                kv_block_pool_destroy).

@@ -232,9 +232,9 @@ void orc_block_copy(void *cache, int elem_size, int num_kv_heads, int block_size
 /* ------------------------------------------------------------------ */
 /* int8 quantization of one (token, head) row.                          */
 /* [NOTES] "How serving systems tame the cost", "Quantized KV cache":   */
-/* store cached K and V at lower precision, e.g. FP16 to INT8.  The      */
-/* pages fix no scheme; this library's reading is symmetric per-token-   */
-/* per-head quantization with an fp16 scale:                             */
+/* the cached K and V may be kept in fewer bits (int8 codes in place of  */
+/* fp16 values).  The pages fix no scheme; this library's reading is     */
+/* symmetric per-token-per-head quantization with an fp16 scale:         */
 /*   amax = max |x_i|            (fp32)                                  */
 /*   s    = fp16_rne(amax / 127) (fp32 division, then round to fp16)     */
 /*   code = clamp(round_half_even(x_i / s), -127, 127)   (fp32 division) */

@@ -416,7 +416,7 @@ def test_toy_loop_row_counts_and_cache_changes_nothing():
     assert rn.tolist() == g["rows_without_cache"]
     assert rc.tolist() == g["rows_with_cache"]
     assert int(rn.sum()) == g["total_without_cache"] and int(rc.sum()) == g["total_with_cache"]
-    assert np.array_equal(on, oc)            # the cache changes the cost, never the numbers
+    assert np.array_equal(on, oc)            # caching saves work; the outputs stay identical
 
 
 def _size(text):
