@@ -127,15 +127,15 @@ int kv_block_refcount(const pkv_pool *pool, int32_t id);
 
 /*
  * kv_block_alloc — take n blocks off the free list, reference count 1 each,
- * ids written to out_ids[0..n).  Blocks are handed out on demand
- * ([GUIDE] "Paging…": handed out on demand, reclaimed when the request ends).
+ * ids written to out_ids[0..n).  A sequence takes blocks as it needs them
+ * and gives them back when it is done ([GUIDE] "Paging…").
  * All-or-nothing: PKV_ERR_NO_BLOCKS (and no change) if fewer than n are free.
  */
 int kv_block_alloc(pkv_pool *pool, int n, int32_t *out_ids);
 
 /*
  * kv_block_share — add one reference to each of ids[0..n), so that another
- * request can point at the same blocks ([VIS] "PagedAttention: the cache in
+ * request's table may list these blocks too ([VIS] "PagedAttention: the cache in
  * blocks": sequences that begin with the same prompt tokens can reference a
  * single stored copy of those tokens' blocks).
  * All-or-nothing: PKV_ERR_INVALID if any id is out of range or free.
@@ -154,10 +154,10 @@ int kv_block_free(pkv_pool *pool, const int32_t *ids, int n);
  * For each sequence b with seq_lens[b] tokens already cached and num_new[b]
  * new tokens (num_new == NULL means 1 each), allocate a new block whenever a
  * new token's position starts a block (allocation on demand, [VIS]
- * "PagedAttention: the cache in blocks": blocks are handed out as a sequence
- * grows, so each sequence has at most one partly filled block), record it in
- * the host array block_tables
- * ([B][max_blocks_per_seq], updated in place), and write the slot of every
+ * "PagedAttention: the cache in blocks": a sequence gains a block only when
+ * its tokens need one, so no more than its last block is incomplete),
+ * record it in the host array block_tables ([B][max_blocks_per_seq],
+ * updated in place), and write the slot of every
  * new token to slot_mapping (sequence-major, sum(num_new) entries).
  * All-or-nothing: PKV_ERR_NO_BLOCKS if the pool cannot cover the step,
  * PKV_ERR_INVALID if a table row would overflow max_blocks_per_seq.

@@ -556,10 +556,11 @@ int orc_paged_decode_attention(const void *q, int q_dtype, int num_q_heads, cons
 /* ------------------------------------------------------------------ */
 /* Prefill attention ([VIS] "Prefill and decode feel different": the    */
 /* prompt is processed as one batch of tokens; [GUIDE] "How the cache turns the */
-/* loop cheap": prefill computes K and V for the whole prompt and stores */
-/* them).  Sequence b has n_b new tokens, the last n_b of its seq_lens[b] */
-/* cached rows (already appended); new token i sits at position          */
-/* p = seq_lens[b] - n_b + i and attends over positions 0..p (causal),   */
+/* loop cheap": the prompt's keys and values are all made, and cached,  */
+/* in that one pass).  Sequence b has n_b new tokens, the last n_b of    */
+/* its seq_lens[b] cached rows (already appended); new token i sits at   */
+/* position p = seq_lens[b] - n_b + i and attends over positions 0..p    */
+/* (causal),                                                             */
 /* with the softmax of [NOTES] "Concept".  q rows are sequence-major:    */
 /* q[q_start[b] + i][h][:], and so is out.                                */
 /* ------------------------------------------------------------------ */

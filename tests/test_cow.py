@@ -75,7 +75,7 @@ def test_oracle_copy_on_write_keeps_every_request_private():
     pk = rng.standard_normal((prompt, H, D)).astype(np.float32)
     pv = rng.standard_normal((prompt, H, D)).astype(np.float32)
     O.append(pk, pv, O.F32, [tables[0][p // bs] * bs + p % bs for p in range(prompt)], bs, kc, vc)
-    # the other requests fork: they point at the same blocks
+    # the other requests fork: their tables list the same block ids
     for b in range(1, S):
         tables[b] = list(tables[0])
         for j in range(-(-prompt // bs)):
@@ -134,7 +134,7 @@ def test_reserve_slots_cow_copies_shared_partial_blocks_only():
     free0 = pkv.kv_num_free_blocks(p)
     lens = np.full(S, prompt, np.int32)
     slots, src, dst = pkv.kv_reserve_slots_cow(p, lens, tables)
-    # requests 0 and 1 copy the partly filled block; request 2 then holds it alone
+    # requests 0 and 1 copy the incomplete last block; request 2 then holds it alone
     assert list(src) == [part, part]
     assert len(set(dst.tolist())) == 2 and part not in dst
     assert list(tables[:, 1]) == [dst[0], dst[1], part]
