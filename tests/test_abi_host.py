@@ -136,6 +136,23 @@ def test_slot_mapping_matches_oracle():
         pkv.kv_slot_mapping(tables, 4, np.full(10, 79, np.int32), np.full(10, 2, np.int32))
 
 
+def test_slot_mapping_into_a_given_array():
+    # the in-place form a serving loop uses: slots written straight into a
+    # slice of a staging buffer, equal to the returned form
+    rng = np.random.default_rng(2)
+    tables = rng.permutation(200).reshape(10, 20).astype(np.int32)
+    start = rng.integers(0, 20 * 16, size=10).astype(np.int32)
+    stage = np.full(64, 0x7F, np.uint8)
+    out = stage[8:48].view(np.int32)
+    got = pkv.kv_slot_mapping(tables, 16, start, out=out)
+    assert got.ctypes.data == out.ctypes.data
+    assert np.array_equal(out, O.slot_mapping(tables, 16, start, np.ones(10, np.int32)))
+    assert (stage[:8] == 0x7F).all() and (stage[48:] == 0x7F).all()
+    for bad in (np.zeros(9, np.int32), np.zeros(10, np.int64), np.zeros(20, np.int32)[::2]):
+        with pytest.raises(ValueError):
+            pkv.kv_slot_mapping(tables, 16, start, out=bad)
+
+
 def test_workspace_size_formula_is_monotone():
     p = pkv.kv_block_pool_init(10, 16, 8, 128, pkv.PKV_BF16)
     a = pkv.paged_decode_workspace_bytes(p, 16, 32)
