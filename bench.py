@@ -441,7 +441,7 @@ def time_workload(name: str, dev, stream, peak: float, reps: int = 20) -> dict:
     return res
 
 
-def time_shared_prompt(dev, stream, peak: float, B=64, P=8192, reps=10, profile=False):
+def time_shared_prompt(dev, stream, peak: float | None, B=64, P=8192, reps=10, profile=False):
     """Decode attention where all B sequences share a P-token prompt (one
     copy of its blocks) and add private suffixes of 64..1024 tokens (seeded),
     on the Llama-2-70B head shape (64 q / 8 KV heads, d 128, fp16, block
@@ -940,7 +940,7 @@ def run_profile(name: str) -> int:
         print("profiled the cascade on llama2_70b: 4 calls")
         return 0
     if name == "shared_prompt_cascade":
-        time_shared_prompt(dev, stream, 6789.6, profile=True)
+        time_shared_prompt(dev, stream, None, profile=True)
         print("profiled the cascade on the shared 8192-token prompt: 4 calls")
         return 0
     d = build_device_workload(name, dev)
