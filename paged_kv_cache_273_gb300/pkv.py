@@ -505,8 +505,10 @@ class DecodeStep:
     uint8 tensor (page-locked for an asynchronous copy) holding the step's
     inputs at the offsets of `layout` (a StepLayout); dev_in: a device uint8
     tensor of at least host_in's size; host_out: a host fp32 tensor of
-    out's shape, or None.  Nothing waits: record an event after the call
-    and synchronize on it before reusing host_in or reading host_out."""
+    out's shape, or None (a page-locked host_out receives the output
+    directly and `out` is then left unwritten).  Nothing waits: record an
+    event after the call and synchronize on it before reusing host_in or
+    reading host_out."""
 
     def __init__(self, pool: Pool, dev_in, layout: StepLayout, in_dtype, q_dtype,
                  num_q_heads: int, k_cache, v_cache, block_tables, batch: int, max_seq_len: int,
