@@ -487,15 +487,17 @@ bool region_ok(size_t off, size_t bytes, size_t total, size_t align)
 }
 
 // The device address of page-locked host memory (its mapping into the device
-// address space), or null for other memory.
+// address space), or null for other memory, and for page-locked memory that
+// another device's context allocated (it need not be mapped for this one).
 void *mapped_host(const void *p)
 {
     cudaPointerAttributes a{};
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();   // clear the error this query may leave
+    int dev = -1;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();   // clear the error these queries may leave
         return nullptr;
     }
-    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+    return a.type == cudaMemoryTypeHost && a.device == dev ? a.devicePointer : nullptr;
 }
 
 // Copy between host and device memory for the step: page-locked host memory
